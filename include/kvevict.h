@@ -1,0 +1,161 @@
+/*
+ * kvevict.h -- C ABI of the GB300 (sm_103a) cumulative proxy-attention
+ * KV-cache eviction library: H2O-adapted, Keyformer-adapted (Gumbel
+ * regulariser with an annealed temperature) and PyramidKV-adapted (per-layer
+ * budget taper), all one decode step.
+ *
+ * What one step computes, for every (batch, layer, KV head) row of the cache
+ * (page "veloxquant_mlx.quantizers.keyformer module", keyformer_update steps
+ * 1-3; page "PyramidKV -- Layer-Adaptive Budget Attention-Mass Eviction",
+ * "How it works"):
+ *   1. append the new fp16 key k with score 0, its absolute position p and a
+ *      frozen Gumbel value g(seed, layer, head, p);
+ *   2. attn = softmax(K k / sqrt(D)) over every stored row, the new one
+ *      included; scores += attn;
+ *   3. if the layer's budget is exceeded, evict the lowest
+ *      score + tau(p) * g over rows j >= n_sink (lowest slot on ties); the
+ *      rows after it move down one slot in order, each key re-rotated by -1
+ *      RoPE position in fp32 and stored as fp16.
+ *
+ * Conventions shared by every entry point:
+ *  - fp16 values cross the boundary as uint16_t bit patterns (IEEE binary16).
+ *  - Device pointers are CUDA global-memory pointers on the device that was
+ *    current at kvevict_create; host pointers are plain host memory (pinned
+ *    memory lets the copies overlap with compute).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). All work
+ *    is enqueued on it; calls return before the GPU finishes unless stated.
+ *  - The caller owns every buffer it passes and keeps it alive until the
+ *    stream has passed the call. The library owns its state arena.
+ *  - Return codes: 0 on success, else one of KVEVICT_ERR_*; the message of the
+ *    last failure on the calling thread is kvevict_last_error().
+ *  - One handle is not thread-safe; use one handle per thread or lock.
+ */
+#ifndef KVEVICT_H
+#define KVEVICT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVEVICT_OK 0
+#define KVEVICT_ERR_INVALID_ARG (-1)  /* bad config, pointer or size */
+#define KVEVICT_ERR_BAD_STATE (-2)    /* call out of order (e.g. prefill after a step) */
+#define KVEVICT_ERR_CUDA (-3)         /* a CUDA runtime call failed */
+#define KVEVICT_ERR_OOM (-4)          /* device allocation failed */
+#define KVEVICT_ERR_DEVICE_CHECK (-5) /* a kernel raised its error word (bounded wait ran out) */
+
+#define KVEVICT_MAX_LAYERS 256
+#define KVEVICT_MAX_PREFILL 16384
+
+/* Cache configuration (page "veloxquant_mlx.quantizers.keyformer module",
+ * KeyformerState and init_keyformer_state; page "PyramidKV ...", Parameters). */
+typedef struct kvevict_config {
+  int32_t batch;          /* B >= 1 */
+  int32_t n_layers;       /* L, 1 .. KVEVICT_MAX_LAYERS */
+  int32_t n_kv_heads;     /* H >= 1 */
+  int32_t head_dim;       /* D, 64 or 128 */
+  int32_t avg_budget;     /* average kept rows per layer, sinks included */
+  double pyramid_beta;    /* >= 1; 1 = the same budget in every layer (plain H2O) */
+  const int32_t* layer_budgets; /* optional host array [n_layers]; overrides avg/beta */
+  int32_t n_sink;         /* leading rows never evicted, >= 0; every budget >= n_sink + 1 */
+  float tau_init;         /* Gumbel temperature at position 0, >= 0 */
+  float tau_end;          /* temperature once position >= anneal_steps, >= 0 */
+  int32_t anneal_steps;   /* >= 0; 0 = constant tau_init */
+  double rope_theta;      /* RoPE base of the model's attention, > 0 */
+  uint64_t seed;          /* base seed of the frozen Gumbel values */
+  int32_t max_prefill;    /* longest prompt kvevict_prefill will take, 0 .. KVEVICT_MAX_PREFILL */
+} kvevict_config;
+
+typedef struct kvevict kvevict_t;
+
+/* Per-layer budget taper, host only (page "PyramidKV ...", "The budget
+ * schedule"): linear from its maximum at layer 0 to its minimum at the last
+ * layer, mean avg_budget, each >= n_sink + 1; beta = 1 is flat. Half-spread
+ * h = min((beta-1)*avg, avg-(n_sink+1)); layer l gets
+ * avg + round(h*(1 - 2l/(L-1))), the offset rounded half away from zero.
+ * out: host int32[n_layers]. Errors: INVALID_ARG if beta < 1, n_layers < 0,
+ * n_sink < 0 or avg_budget < n_sink + 1. */
+int kvevict_budgets(int32_t n_layers, int32_t avg_budget, int32_t n_sink, double beta,
+                    int32_t* out);
+
+/* Validate cfg, compute the budgets and allocate the device state on the
+ * current device: per row of the cache, (budget_l + 1) x D fp16 keys plus
+ * float scores, float Gumbel values and int32 positions, and prefill scratch
+ * for max_prefill tokens. The state starts empty (position 0).
+ * Errors: INVALID_ARG (tau < 0, beta < 1, a budget <= n_sink, D not 64/128,
+ * null pointers, sizes out of range), OOM, CUDA. *out is set only on success. */
+int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out);
+
+/* Free the handle and its device memory (synchronises the device first). */
+int kvevict_destroy(kvevict_t* h);
+
+/* Return the handle to the empty state at position 0 (the arena is reused). */
+int kvevict_reset(kvevict_t* h, void* stream);
+
+/* Absorb a prompt of S tokens at positions 0..S-1 (the state must be empty).
+ * keys: device fp16 [B, L, H, S, D], each key already RoPE-rotated at its
+ * position. Scores are the column sums of the causal softmax(K K^T/sqrt(D))
+ * (the diagonal included), i.e. what S decode steps without eviction would
+ * accumulate. A row whose layer budget b is below S then bulk-evicts the
+ * S - b non-sink rows with the lowest (score + tau(S-1) * g, slot); survivors
+ * keep their order and each is re-rotated by (new slot - old slot).
+ * Errors: INVALID_ARG (null keys, S < 0 or S > max_prefill), BAD_STATE (state
+ * not empty), CUDA. */
+int kvevict_prefill(kvevict_t* h, const uint16_t* keys, int32_t S, void* stream);
+
+/* One decode step for every row at position p = kvevict_next_pos().
+ * k_new: device fp16 [B, L, H, D], RoPE-rotated at p. evicted: device int32
+ * [B, L, H] or NULL; receives the evicted slot (index into the rows after the
+ * append, 0..n) or -1 when the row was within budget. One fused kernel launch.
+ * Errors: INVALID_ARG (null k_new), CUDA. */
+int kvevict_step(kvevict_t* h, const uint16_t* k_new, int32_t* evicted, void* stream);
+
+/* T consecutive decode steps, replayed from a CUDA graph that the library
+ * captures once per (keys, evicted, T, start position) and caches.
+ * keys: device fp16 [T, B, L, H, D]; evicted: device int32 [T, B, L, H] or NULL.
+ * Errors: as kvevict_step; T < 0 is INVALID_ARG, T = 0 does nothing. */
+int kvevict_decode(kvevict_t* h, const uint16_t* keys, int32_t T, int32_t* evicted,
+                   void* stream);
+
+/* End to end from host memory: prefill S prompt keys (host fp16
+ * [B, L, H, S, D]; S may be 0) then T decode steps (host fp16 [T, B, L, H, D]),
+ * copying the inputs to the device in chunks that overlap with compute and
+ * the evicted slots back to host int32 [T, B, L, H] (or NULL). The state must
+ * be empty. Returns after the stream has finished. Device staging is allocated
+ * on first use and kept with the handle.
+ * Errors: INVALID_ARG, BAD_STATE, OOM, CUDA, DEVICE_CHECK. */
+int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S,
+                     const uint16_t* decode_keys, int32_t T, int32_t* evicted, void* stream);
+
+/* Copy one row's state to host memory (synchronises the stream). Rows
+ * are given in slot order: keys [n, D] fp16 bits, scores [n], gumbel [n],
+ * positions [n] (the original absolute position of each kept key), n =
+ * *n_kept = min(next_pos, budget of layer l). Buffers need room for
+ * budget_l + 1 rows; any of the four may be NULL. Errors: INVALID_ARG
+ * (indices out of range), CUDA, DEVICE_CHECK. */
+int kvevict_read_state(kvevict_t* h, int32_t b, int32_t l, int32_t head, uint16_t* keys,
+                       float* scores, float* gumbel, int32_t* positions, int32_t* n_kept,
+                       void* stream);
+
+/* Synchronise the stream and report a kernel error word (DEVICE_CHECK) if set. */
+int kvevict_check(kvevict_t* h, void* stream);
+
+/* Position the next decode key will occupy (= tokens absorbed so far). */
+int kvevict_next_pos(const kvevict_t* h, int64_t* p);
+
+/* Budget of layer l as resolved at create time. */
+int kvevict_layer_budget(const kvevict_t* h, int32_t l, int32_t* budget);
+
+/* Device bytes held by the handle (arena + scratch + staging). */
+int kvevict_device_bytes(const kvevict_t* h, size_t* bytes);
+
+/* Message of the last failure on the calling thread ("" if none). */
+const char* kvevict_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVEVICT_H */

@@ -1,0 +1,110 @@
+/*
+ * kvevict_oracle.h -- plain fp64 CPU oracle for cumulative proxy-attention
+ * KV-cache eviction (H2O-adapted, Keyformer-adapted, PyramidKV-adapted).
+ *
+ * TEST INFRASTRUCTURE. This oracle exists to check the CUDA library. Only the
+ * test suite, the smoke check and the benchmark's CPU-baseline leg may load
+ * it. It shares no code, header, table or constant generator with the CUDA
+ * path, and it never reads anything the CUDA path produced.
+ *
+ * Sources (page title, section):
+ *  - "veloxquant_mlx.quantizers.keyformer module": KeyformerState fields,
+ *    init_keyformer_state (validation), keyformer_update (the three per-token
+ *    steps), FUSED METAL KERNEL note (rotation in fp32, keys within 1 ULP),
+ *    GAP #1 (tau annealing, Eq. 10), GAP #2 (RoPE position remap).
+ *  - "PyramidKV -- Layer-Adaptive Budget Attention-Mass Eviction": "The budget
+ *    schedule" (worked 12-layer example) and "How it works" (per-step rule).
+ *
+ * Precision: every score, softmax and regularised score is fp64. Two steps
+ * decide a code and are taken in the precision the pages fix instead:
+ * the RoPE re-rotation of a shifted key (fp32 arithmetic, then fp16 storage;
+ * keyformer page, FUSED METAL KERNEL) and the stored Gumbel value (float32;
+ * keyformer page, KeyformerState.gumbel).
+ *
+ * Parity pins live in tests/test_oracle_*.py. One function has no pin from
+ * the pages: the Gumbel hash (the pages name no formula), so orc_gumbel is
+ * "parity unpinned" against the pages; it is pinned only to the published
+ * SplitMix64 reference outputs and to the Gumbel distribution's moments.
+ */
+#ifndef KVEVICT_ORACLE_H
+#define KVEVICT_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Per-layer budget taper. 0 on success, -1 on invalid input. */
+int orc_budgets(int32_t n_layers, int32_t avg_budget, int32_t n_sink, double beta, int32_t* out);
+
+/* SplitMix64: the output of a generator whose state was x, after one step. */
+uint64_t orc_splitmix64(uint64_t x);
+/* Hash of (seed, layer, head, position) and the frozen Gumbel value. */
+uint64_t orc_gumbel_hash(uint64_t seed, int64_t layer, int64_t head, int64_t pos);
+float orc_gumbel(uint64_t seed, int64_t layer, int64_t head, int64_t pos);
+/* Gumbel values for positions p0 .. p0+count-1 of one (layer, head). */
+void orc_gumbel_many(uint64_t seed, int64_t layer, int64_t head, int64_t p0, int64_t count, float* out);
+
+/* Annealed temperature at absolute position pos (keyformer page, GAP #1). */
+double orc_tau(double tau_init, double tau_end, int64_t anneal_steps, int64_t pos);
+
+/* IEEE binary16 helpers (round to nearest, ties to even). */
+uint16_t orc_f32_to_f16(float x);
+double orc_f16_to_f64(uint16_t h);
+void orc_f32_to_f16_array(int64_t n, const float* x, uint16_t* out);
+void orc_f16_to_f64_array(int64_t n, const uint16_t* h, double* out);
+
+/* RoPE constants for a rotation by delta positions: c[i] = f32(cos(delta*w_i)),
+ * s[i] = f32(sin(delta*w_i)), w_i = theta^(-2i/D), i < D/2. */
+void orc_rope_consts(double theta, int32_t D, int64_t delta, float* c, float* s);
+/* Rotate one fp16 row by the given constants, fp32 arithmetic, half-split pairs. */
+void orc_rotate_row(int32_t D, uint16_t* row, const float* c, const float* s);
+
+/* One decode step, append + proxy-attention accumulation. The state holds n
+ * rows; the new row goes to slot n. Returns n+1. Arrays need room for n+1 rows. */
+int32_t orc_step_accumulate(int32_t D, int32_t n, uint16_t* K, double* score, float* g,
+                            int32_t* pos, const uint16_t* k_new, int64_t p, float g_new);
+/* Regularised scores r_j = score_j + tau*g_j (fp64), for all rows. */
+void orc_regularised(int32_t n, const double* score, const float* g, double tau, double* r);
+/* Lowest slot attaining min r over j >= n_sink; -1 if no row is evictable. */
+int32_t orc_argmin(int32_t n, const double* r, int32_t n_sink);
+/* Evict slot e from an n-row state: rows after e move down one slot in order,
+ * each moved key re-rotated by -1 position. Returns n-1. */
+int32_t orc_evict(int32_t D, int32_t n, uint16_t* K, double* score, float* g, int32_t* pos,
+                  int32_t e, double theta);
+
+/* Prefill scoring: column sums of the causal softmax(K K^T / sqrt(D)), the
+ * diagonal included. keys [S, D] fp16 bits, out colsum [S]. */
+void orc_prefill_colsum(int32_t S, int32_t D, const uint16_t* keys, double* colsum);
+/* Own bulk selection: mark the S - budget non-sink rows with the lowest
+ * (r, slot); mask[j] = 1 for evicted rows. Returns the evicted count. */
+int32_t orc_prefill_select(int32_t S, int32_t budget, int32_t n_sink, const double* r, uint8_t* mask);
+/* Apply a bulk eviction mask: survivors move to consecutive slots in order,
+ * each re-rotated by (new slot - old slot). Returns the kept count. */
+int32_t orc_prefill_apply(int32_t S, int32_t D, const uint16_t* keys, const double* colsum,
+                          const float* g, const uint8_t* mask, double theta,
+                          uint16_t* K, double* score, float* g_out, int32_t* pos);
+
+/* Whole-pass driver for one head (prefill then T decode steps), with the
+ * oracle's own eviction decisions; used for the CPU baseline and self-tests.
+ * evicted[T] gets the slot evicted at each step or -1. State arrays need
+ * room for budget+1 rows. Returns the final kept count. */
+typedef struct orc_head_cfg {
+  int32_t D, budget, n_sink, layer, head;
+  double tau_init, tau_end; int64_t anneal_steps;
+  double theta; uint64_t seed;
+} orc_head_cfg;
+int32_t orc_run_head(const orc_head_cfg* cfg, int32_t S, const uint16_t* prefill_keys,
+                     int32_t T, const uint16_t* decode_keys, int32_t* evicted,
+                     uint16_t* K, double* score, float* g, int32_t* pos);
+/* The same over many heads in parallel (OpenMP); arrays are per-head strided
+ * by S*D, T*D, T and cap*D / cap. Returns the thread count used. */
+int32_t orc_run_heads(int32_t n_heads, const orc_head_cfg* cfgs, int32_t S,
+                      const uint16_t* prefill_keys, int32_t T, const uint16_t* decode_keys,
+                      int32_t* evicted, int32_t cap, uint16_t* K, double* score, float* g,
+                      int32_t* pos, int32_t* n_out, int32_t n_threads);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
