@@ -1,0 +1,592 @@
+// runtime.cu -- the C ABI declared in include/kvevict.h: validation, the
+// budget taper, the device arena, launch sequencing, the cached CUDA graph of
+// decode steps and the host-buffer pipeline. Host code only; every step of the
+// method runs in the kernels of decode.cu and prefill.cu.
+#include "kvevict.h"
+#include "kvevict_internal.cuh"
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+using kvx::LayerInfo;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+#define KV_CUDA(call)                                                                   \
+  do {                                                                                  \
+    cudaError_t e_ = (call);                                                            \
+    if (e_ != cudaSuccess)                                                              \
+      return fail(e_ == cudaErrorMemoryAllocation ? KVEVICT_ERR_OOM : KVEVICT_ERR_CUDA, \
+                  std::string(#call) + ": " + cudaGetErrorString(e_));                  \
+  } while (0)
+
+double round_half_away(double x) {
+  const double a = std::fabs(x);
+  const double f = std::floor(a);
+  const double r = (a - f >= 0.5) ? f + 1.0 : f;
+  return x < 0 ? -r : r;
+}
+
+int compute_budgets(int32_t L, int32_t avg, int32_t n_sink, double beta, int32_t* out) {
+  if (L < 0 || n_sink < 0) return fail(KVEVICT_ERR_INVALID_ARG, "n_layers and n_sink must be >= 0");
+  if (!(beta >= 1.0)) return fail(KVEVICT_ERR_INVALID_ARG, "pyramid_beta must be >= 1");
+  if (avg < n_sink + 1) return fail(KVEVICT_ERR_INVALID_ARG, "avg_budget must be >= n_sink + 1");
+  if (L == 0) return KVEVICT_OK;
+  if (L == 1) {
+    out[0] = avg;
+    return KVEVICT_OK;
+  }
+  // half-spread: steepness asks for (beta-1)*avg, the n_sink+1 floor caps it
+  const double h = std::min((beta - 1.0) * (double)avg, (double)(avg - (n_sink + 1)));
+  for (int32_t l = 0; l < L; ++l) {
+    const double t = 1.0 - 2.0 * (double)l / (double)(L - 1);
+    out[l] = avg + (int32_t)round_half_away(h * t);
+  }
+  return KVEVICT_OK;
+}
+
+// Annealed temperature at absolute position p (fp64, then the kernels' f32).
+double tau_at(const kvevict_config& c, int64_t p) {
+  if (c.anneal_steps <= 0 || c.tau_init == c.tau_end) return (double)c.tau_init;
+  const int64_t t = std::max<int64_t>(0, std::min<int64_t>(p, c.anneal_steps));
+  return (double)c.tau_init + (double)t * ((double)c.tau_end - (double)c.tau_init) / (double)c.anneal_steps;
+}
+
+template <typename T>
+cudaError_t dalloc(T** p, size_t count) {
+  *p = nullptr;
+  if (count == 0) count = 1;
+  return cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T));
+}
+
+}  // namespace
+
+struct kvevict {
+  kvevict_config cfg{};
+  int device = 0;
+  int D = 0, B = 0, L = 0, H = 0, heads = 0;
+  std::vector<int32_t> budgets;
+  std::vector<LayerInfo> layers;
+  int64_t total_rows = 0, total_meta = 0;
+  int capm_max = 0;
+  LayerInfo* d_layers = nullptr;
+  __half* K = nullptr;
+  float* score = nullptr;
+  float* gum = nullptr;
+  int32_t* pos = nullptr;
+  int32_t* pend = nullptr;
+  int* err = nullptr;
+  float* rope_c = nullptr;  // [max_delta + 1, D/2]; row d = f32(cos(-d * w_i))
+  float* rope_s = nullptr;
+  int max_delta = 1;
+  float* lse2 = nullptr;    // prefill scratch [heads, Sp_max]
+  float* colsum = nullptr;
+  int64_t Sp_max = 0;
+  size_t decode_smem = 0;
+  int64_t next_pos = 0;
+  bool stepped = false;
+  size_t bytes = 0;
+  // cached CUDA graph of a run of decode steps
+  cudaStream_t cap_stream = nullptr;
+  cudaGraphExec_t gexec = nullptr;
+  const void* g_keys = nullptr;
+  const void* g_ev = nullptr;
+  int g_T = -1;
+  int64_t g_p0 = -1;
+  // host pipeline staging
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t ev_ready[2] = {nullptr, nullptr};
+  cudaEvent_t ev_free[2] = {nullptr, nullptr};
+  uint16_t* stage[2] = {nullptr, nullptr};
+  int32_t* ev_stage[2] = {nullptr, nullptr};
+  size_t stage_elems = 0;
+  size_t ev_stage_elems = 0;
+};
+
+namespace {
+
+int64_t BLHD(const kvevict* h) { return (int64_t)h->B * h->L * h->H * h->D; }
+int64_t BLH(const kvevict* h) { return (int64_t)h->B * h->L * h->H; }
+
+kvx::DecodeArgs decode_args(kvevict* h, const uint16_t* k_new, int32_t* evicted, int64_t p) {
+  kvx::DecodeArgs a{};
+  a.k_new = reinterpret_cast<const __half*>(k_new);
+  a.K = h->K;
+  a.score = h->score;
+  a.gum = h->gum;
+  a.pos = h->pos;
+  a.pend = h->pend;
+  a.evicted = evicted;
+  a.layers = h->d_layers;
+  a.rope_c = h->rope_c + (size_t)(h->D / 2);  // row d = 1: shift by -1
+  a.rope_s = h->rope_s + (size_t)(h->D / 2);
+  a.err = h->err;
+  a.B = h->B;
+  a.L = h->L;
+  a.H = h->H;
+  a.n_sink = h->cfg.n_sink;
+  a.p = p;
+  a.tau = (float)tau_at(h->cfg, p);
+  a.scale = (float)(1.0 / std::sqrt((double)h->D));
+  a.seed = h->cfg.seed;
+  return a;
+}
+
+int enqueue_step(kvevict* h, const uint16_t* k_new, int32_t* evicted, int64_t p, cudaStream_t s) {
+  const kvx::DecodeArgs a = decode_args(h, k_new, evicted, p);
+  KV_CUDA(kvx::launch_decode_step(a, h->D, h->heads, h->decode_smem, s));
+  return KVEVICT_OK;
+}
+
+// Score and bulk-evict the prompt for batches [b0, b0 + nb); keys point at
+// batch b0's [nb, L, H, S, D] block; lse2/colsum hold nb*L*H rows of Sp.
+int enqueue_prefill(kvevict* h, const uint16_t* keys, int32_t S, int b0, int nb, float* lse2,
+                    float* colsum, cudaStream_t s) {
+  const int heads = nb * h->L * h->H;
+  const int Sp = (S + 63) / 64 * 64;
+  kvx::PrefillScoreArgs sa{};
+  sa.keys = reinterpret_cast<const __half*>(keys);
+  sa.lse2 = lse2;
+  sa.colsum = colsum;
+  sa.S = S;
+  sa.Sp = Sp;
+  sa.heads = heads;
+  sa.scale2 = (float)(1.4426950408889634 / std::sqrt((double)h->D));
+  KV_CUDA(kvx::launch_prefill_scores(sa, h->D, s));
+  kvx::PrefillSelectArgs pa{};
+  pa.keys = sa.keys;
+  pa.colsum = colsum;
+  pa.gscr = lse2;  // pass 1's output is dead once the column sums exist
+  pa.K = h->K;
+  pa.score = h->score;
+  pa.gum = h->gum;
+  pa.pos = h->pos;
+  pa.pend = h->pend;
+  pa.layers = h->d_layers;
+  pa.rope_c = h->rope_c;
+  pa.rope_s = h->rope_s;
+  pa.err = h->err;
+  pa.B = h->B;
+  pa.L = h->L;
+  pa.H = h->H;
+  pa.n_sink = h->cfg.n_sink;
+  pa.b0 = b0;
+  pa.S = S;
+  pa.Sp = Sp;
+  pa.tau = (float)tau_at(h->cfg, (int64_t)S - 1);
+  pa.seed = h->cfg.seed;
+  KV_CUDA(kvx::launch_prefill_select(pa, h->D, heads, s));
+  return KVEVICT_OK;
+}
+
+int enqueue_flush(kvevict* h, cudaStream_t s) {
+  kvx::FlushArgs f{};
+  f.K = h->K;
+  f.score = h->score;
+  f.gum = h->gum;
+  f.pos = h->pos;
+  f.pend = h->pend;
+  f.layers = h->d_layers;
+  f.rope_c = h->rope_c + (size_t)(h->D / 2);
+  f.rope_s = h->rope_s + (size_t)(h->D / 2);
+  f.B = h->B;
+  f.L = h->L;
+  f.H = h->H;
+  f.p = h->next_pos;
+  KV_CUDA(kvx::launch_flush(f, h->D, h->heads, s));
+  return KVEVICT_OK;
+}
+
+int check_error_word(kvevict* h, cudaStream_t s) {
+  KV_CUDA(cudaStreamSynchronize(s));
+  int e = 0;
+  KV_CUDA(cudaMemcpy(&e, h->err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (e != 0) {
+    char buf[96];
+    std::snprintf(buf, sizeof buf, "kernel error word set: 0x%x (%s)", e,
+                  (e & kvx::kErrWaitTimeout) ? "bounded wait ran out" : "bad index");
+    return fail(KVEVICT_ERR_DEVICE_CHECK, buf);
+  }
+  return KVEVICT_OK;
+}
+
+void free_all(kvevict* h) {
+  if (h->gexec) cudaGraphExecDestroy(h->gexec);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
+  for (int i = 0; i < 2; ++i) {
+    if (h->ev_ready[i]) cudaEventDestroy(h->ev_ready[i]);
+    if (h->ev_free[i]) cudaEventDestroy(h->ev_free[i]);
+    cudaFree(h->stage[i]);
+    cudaFree(h->ev_stage[i]);
+  }
+  cudaFree(h->d_layers);
+  cudaFree(h->K);
+  cudaFree(h->score);
+  cudaFree(h->gum);
+  cudaFree(h->pos);
+  cudaFree(h->pend);
+  cudaFree(h->err);
+  cudaFree(h->rope_c);
+  cudaFree(h->rope_s);
+  cudaFree(h->lse2);
+  cudaFree(h->colsum);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvevict_last_error(void) { return g_last_error.c_str(); }
+
+int kvevict_budgets(int32_t n_layers, int32_t avg_budget, int32_t n_sink, double beta, int32_t* out) {
+  if (n_layers > 0 && !out) return fail(KVEVICT_ERR_INVALID_ARG, "out is null");
+  return compute_budgets(n_layers, avg_budget, n_sink, beta, out);
+}
+
+int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
+  g_last_error.clear();
+  if (!cfg || !out) return fail(KVEVICT_ERR_INVALID_ARG, "cfg and out must not be null");
+  const kvevict_config& c = *cfg;
+  if (c.batch < 1 || c.n_kv_heads < 1) return fail(KVEVICT_ERR_INVALID_ARG, "batch and n_kv_heads must be >= 1");
+  if (c.n_layers < 1 || c.n_layers > KVEVICT_MAX_LAYERS)
+    return fail(KVEVICT_ERR_INVALID_ARG, "n_layers must be in [1, KVEVICT_MAX_LAYERS]");
+  if (c.head_dim != 64 && c.head_dim != 128) return fail(KVEVICT_ERR_INVALID_ARG, "head_dim must be 64 or 128");
+  if (c.n_sink < 0) return fail(KVEVICT_ERR_INVALID_ARG, "n_sink must be >= 0");
+  if (!(c.tau_init >= 0.f) || !(c.tau_end >= 0.f))
+    return fail(KVEVICT_ERR_INVALID_ARG, "tau_init and tau_end must be >= 0");
+  if (c.anneal_steps < 0) return fail(KVEVICT_ERR_INVALID_ARG, "anneal_steps must be >= 0");
+  if (!(c.rope_theta > 0.0)) return fail(KVEVICT_ERR_INVALID_ARG, "rope_theta must be > 0");
+  if (c.max_prefill < 0 || c.max_prefill > KVEVICT_MAX_PREFILL)
+    return fail(KVEVICT_ERR_INVALID_ARG, "max_prefill must be in [0, KVEVICT_MAX_PREFILL]");
+
+  std::vector<int32_t> budgets(c.n_layers);
+  if (c.layer_budgets) {
+    for (int l = 0; l < c.n_layers; ++l) budgets[l] = c.layer_budgets[l];
+  } else {
+    const int rc = compute_budgets(c.n_layers, c.avg_budget, c.n_sink, c.pyramid_beta, budgets.data());
+    if (rc != KVEVICT_OK) return rc;
+  }
+  for (int l = 0; l < c.n_layers; ++l)
+    if (budgets[l] < c.n_sink + 1)
+      return fail(KVEVICT_ERR_INVALID_ARG, "every layer budget must be >= n_sink + 1 (room to evict)");
+
+  kvevict* h = new kvevict();
+  h->cfg = c;
+  h->cfg.layer_budgets = nullptr;
+  h->D = c.head_dim;
+  h->B = c.batch;
+  h->L = c.n_layers;
+  h->H = c.n_kv_heads;
+  h->heads = c.batch * c.n_layers * c.n_kv_heads;
+  h->budgets = budgets;
+  h->layers.resize(c.n_layers);
+  int64_t rows = 0, meta = 0;
+  for (int l = 0; l < c.n_layers; ++l) {
+    LayerInfo& li = h->layers[l];
+    li.budget = budgets[l];
+    li.cap = budgets[l] + 1;
+    li.capm = (li.cap + 3) & ~3;
+    li.pad = 0;
+    li.row_base = rows;
+    li.meta_base = meta;
+    rows += (int64_t)h->B * h->H * li.cap;
+    meta += (int64_t)h->B * h->H * li.capm;
+    h->capm_max = std::max(h->capm_max, li.capm);
+  }
+  h->total_rows = rows;
+  h->total_meta = meta;
+  h->decode_smem = kvx::decode_step_smem(h->D, h->capm_max);
+  if (h->decode_smem > 227 * 1024) {
+    delete h;
+    return fail(KVEVICT_ERR_INVALID_ARG, "layer budget too large for the single-CTA decode step");
+  }
+  h->max_delta = std::max(1, c.max_prefill);
+  h->Sp_max = (int64_t)(c.max_prefill + 63) / 64 * 64;
+
+  auto bail = [&](int code) {
+    free_all(h);
+    delete h;
+    return code;
+  };
+#define KV_CUDA_CREATE(call)                                                                   \
+  do {                                                                                         \
+    cudaError_t e_ = (call);                                                                   \
+    if (e_ != cudaSuccess)                                                                     \
+      return bail(fail(e_ == cudaErrorMemoryAllocation ? KVEVICT_ERR_OOM : KVEVICT_ERR_CUDA,   \
+                       std::string(#call) + ": " + cudaGetErrorString(e_)));                   \
+  } while (0)
+
+  cudaStream_t s = (cudaStream_t)stream;
+  KV_CUDA_CREATE(cudaGetDevice(&h->device));
+  {
+    // opt-in shared memory per block on this device, less what the kernels
+    // declare statically
+    int optin = 0;
+    KV_CUDA_CREATE(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device));
+    if (h->decode_smem + 1024 > (size_t)optin ||
+        kvx::prefill_select_smem(std::max(1, c.max_prefill)) + 1024 > (size_t)optin)
+      return bail(fail(KVEVICT_ERR_INVALID_ARG, "layer budget or max_prefill too large for shared memory"));
+  }
+  KV_CUDA_CREATE(kvx::decode_step_setup(h->D, h->decode_smem));
+  KV_CUDA_CREATE(kvx::prefill_setup(h->D, c.max_prefill));
+  KV_CUDA_CREATE(dalloc(&h->d_layers, (size_t)c.n_layers));
+  KV_CUDA_CREATE(dalloc(&h->K, (size_t)rows * h->D));
+  KV_CUDA_CREATE(dalloc(&h->score, (size_t)meta));
+  KV_CUDA_CREATE(dalloc(&h->gum, (size_t)meta));
+  KV_CUDA_CREATE(dalloc(&h->pos, (size_t)meta));
+  KV_CUDA_CREATE(dalloc(&h->pend, (size_t)h->heads));
+  KV_CUDA_CREATE(dalloc(&h->err, 1));
+  const size_t half = (size_t)h->D / 2;
+  KV_CUDA_CREATE(dalloc(&h->rope_c, (size_t)(h->max_delta + 1) * half));
+  KV_CUDA_CREATE(dalloc(&h->rope_s, (size_t)(h->max_delta + 1) * half));
+  if (c.max_prefill > 0) {
+    KV_CUDA_CREATE(dalloc(&h->lse2, (size_t)h->heads * h->Sp_max));
+    KV_CUDA_CREATE(dalloc(&h->colsum, (size_t)h->heads * h->Sp_max));
+  }
+  h->bytes = (size_t)rows * h->D * 2 + (size_t)meta * 12 + (size_t)h->heads * 4 +
+             2 * (size_t)(h->max_delta + 1) * half * 4 + 2 * (size_t)h->heads * h->Sp_max * 4;
+
+  // RoPE constants for a shift back by d positions: c = f32(cos(-d w_i)),
+  // s = f32(sin(-d w_i)), w_i = theta^(-2i/D), taken in fp64.
+  std::vector<float> hc((size_t)(h->max_delta + 1) * half), hs(hc.size());
+  for (int d = 0; d <= h->max_delta; ++d)
+    for (size_t i = 0; i < half; ++i) {
+      const double w = std::pow(c.rope_theta, -(2.0 * (double)i) / (double)h->D);
+      const double ang = (double)(-d) * w;
+      hc[(size_t)d * half + i] = (float)std::cos(ang);
+      hs[(size_t)d * half + i] = (float)std::sin(ang);
+    }
+  KV_CUDA_CREATE(cudaMemcpy(h->rope_c, hc.data(), hc.size() * 4, cudaMemcpyHostToDevice));
+  KV_CUDA_CREATE(cudaMemcpy(h->rope_s, hs.data(), hs.size() * 4, cudaMemcpyHostToDevice));
+  KV_CUDA_CREATE(cudaMemcpy(h->d_layers, h->layers.data(), h->layers.size() * sizeof(LayerInfo),
+                            cudaMemcpyHostToDevice));
+  KV_CUDA_CREATE(cudaMemsetAsync(h->pend, 0xFF, (size_t)h->heads * 4, s));
+  KV_CUDA_CREATE(cudaMemsetAsync(h->err, 0, sizeof(int), s));
+  KV_CUDA_CREATE(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
+  KV_CUDA_CREATE(cudaStreamSynchronize(s));
+#undef KV_CUDA_CREATE
+  *out = h;
+  return KVEVICT_OK;
+}
+
+int kvevict_destroy(kvevict_t* h) {
+  if (!h) return KVEVICT_OK;
+  cudaDeviceSynchronize();
+  free_all(h);
+  delete h;
+  return KVEVICT_OK;
+}
+
+int kvevict_reset(kvevict_t* h, void* stream) {
+  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  cudaStream_t s = (cudaStream_t)stream;
+  KV_CUDA(cudaMemsetAsync(h->pend, 0xFF, (size_t)h->heads * 4, s));
+  KV_CUDA(cudaMemsetAsync(h->err, 0, sizeof(int), s));
+  h->next_pos = 0;
+  h->stepped = false;
+  return KVEVICT_OK;
+}
+
+int kvevict_prefill(kvevict_t* h, const uint16_t* keys, int32_t S, void* stream) {
+  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  if (S < 0 || S > h->cfg.max_prefill) return fail(KVEVICT_ERR_INVALID_ARG, "S must be in [0, max_prefill]");
+  if (S > 0 && !keys) return fail(KVEVICT_ERR_INVALID_ARG, "keys is null");
+  if (h->next_pos != 0 || h->stepped) return fail(KVEVICT_ERR_BAD_STATE, "prefill needs an empty state");
+  if (S == 0) return KVEVICT_OK;
+  const int rc = enqueue_prefill(h, keys, S, 0, h->B, h->lse2, h->colsum, (cudaStream_t)stream);
+  if (rc != KVEVICT_OK) return rc;
+  h->next_pos = S;
+  return KVEVICT_OK;
+}
+
+int kvevict_step(kvevict_t* h, const uint16_t* k_new, int32_t* evicted, void* stream) {
+  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  if (!k_new) return fail(KVEVICT_ERR_INVALID_ARG, "k_new is null");
+  const int rc = enqueue_step(h, k_new, evicted, h->next_pos, (cudaStream_t)stream);
+  if (rc != KVEVICT_OK) return rc;
+  h->next_pos += 1;
+  h->stepped = true;
+  return KVEVICT_OK;
+}
+
+int kvevict_decode(kvevict_t* h, const uint16_t* keys, int32_t T, int32_t* evicted, void* stream) {
+  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  if (T < 0) return fail(KVEVICT_ERR_INVALID_ARG, "T must be >= 0");
+  if (T == 0) return KVEVICT_OK;
+  if (!keys) return fail(KVEVICT_ERR_INVALID_ARG, "keys is null");
+  const bool hit = h->gexec && h->g_keys == keys && h->g_ev == evicted && h->g_T == T &&
+                   h->g_p0 == h->next_pos;
+  if (!hit) {
+    if (h->gexec) {
+      cudaGraphExecDestroy(h->gexec);
+      h->gexec = nullptr;
+    }
+    KV_CUDA(cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
+    int rc = KVEVICT_OK;
+    for (int32_t t = 0; t < T && rc == KVEVICT_OK; ++t)
+      rc = enqueue_step(h, keys + (size_t)t * BLHD(h), evicted ? evicted + (size_t)t * BLH(h) : nullptr,
+                        h->next_pos + t, h->cap_stream);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ce = cudaStreamEndCapture(h->cap_stream, &graph);
+    if (rc != KVEVICT_OK) {
+      if (graph) cudaGraphDestroy(graph);
+      return rc;
+    }
+    if (ce != cudaSuccess) return fail(KVEVICT_ERR_CUDA, std::string("stream capture: ") + cudaGetErrorString(ce));
+    const cudaError_t ie = cudaGraphInstantiate(&h->gexec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ie != cudaSuccess) {
+      h->gexec = nullptr;
+      return fail(KVEVICT_ERR_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(ie));
+    }
+    h->g_keys = keys;
+    h->g_ev = evicted;
+    h->g_T = T;
+    h->g_p0 = h->next_pos;
+  }
+  KV_CUDA(cudaGraphLaunch(h->gexec, (cudaStream_t)stream));
+  h->next_pos += T;
+  h->stepped = true;
+  return KVEVICT_OK;
+}
+
+int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, const uint16_t* decode_keys,
+                     int32_t T, int32_t* evicted, void* stream) {
+  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  if (S < 0 || S > h->cfg.max_prefill || T < 0) return fail(KVEVICT_ERR_INVALID_ARG, "bad S or T");
+  if ((S > 0 && !prefill_keys) || (T > 0 && !decode_keys)) return fail(KVEVICT_ERR_INVALID_ARG, "null keys");
+  if (h->next_pos != 0 || h->stepped) return fail(KVEVICT_ERR_BAD_STATE, "run_host needs an empty state");
+  cudaStream_t s = (cudaStream_t)stream;
+  // Staging: two buffers of up to 256 MiB (or one batch's prompt / one step,
+  // whichever is larger), so copies of chunk k+1 overlap compute on chunk k.
+  const size_t per_batch = (size_t)h->L * h->H * (size_t)S * h->D;
+  const size_t per_step = (size_t)BLHD(h);
+  const size_t budget_elems = (size_t)128 << 20;  // 256 MiB of fp16
+  const int bc = S > 0 ? (int)std::max<size_t>(1, std::min<size_t>(h->B, budget_elems / std::max<size_t>(per_batch, 1))) : 0;
+  const int tc = T > 0 ? (int)std::max<size_t>(1, std::min<size_t>((size_t)T, budget_elems / per_step)) : 0;
+  const size_t need = std::max((size_t)bc * per_batch, (size_t)tc * per_step);
+  if (!h->copy_stream) {
+    KV_CUDA(cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking));
+    for (int i = 0; i < 2; ++i) {
+      KV_CUDA(cudaEventCreateWithFlags(&h->ev_ready[i], cudaEventDisableTiming));
+      KV_CUDA(cudaEventCreateWithFlags(&h->ev_free[i], cudaEventDisableTiming));
+    }
+  }
+  if (need > h->stage_elems) {
+    KV_CUDA(cudaStreamSynchronize(s));
+    for (int i = 0; i < 2; ++i) {
+      cudaFree(h->stage[i]);
+      h->stage[i] = nullptr;
+      KV_CUDA(dalloc(&h->stage[i], need));
+    }
+    h->stage_elems = need;
+  }
+  const size_t ev_need = (size_t)tc * BLH(h);
+  if (evicted && ev_need > h->ev_stage_elems) {
+    for (int i = 0; i < 2; ++i) {
+      cudaFree(h->ev_stage[i]);
+      h->ev_stage[i] = nullptr;
+      KV_CUDA(dalloc(&h->ev_stage[i], ev_need));
+    }
+    h->ev_stage_elems = ev_need;
+  }
+  int k = 0;
+  // prompt, batch chunk by batch chunk
+  for (int b0 = 0; b0 < (S > 0 ? h->B : 0); b0 += bc, ++k) {
+    const int nb = std::min(bc, h->B - b0);
+    const int buf = k & 1;
+    KV_CUDA(cudaStreamWaitEvent(h->copy_stream, h->ev_free[buf], 0));
+    KV_CUDA(cudaMemcpyAsync(h->stage[buf], prefill_keys + (size_t)b0 * per_batch, (size_t)nb * per_batch * 2,
+                            cudaMemcpyHostToDevice, h->copy_stream));
+    KV_CUDA(cudaEventRecord(h->ev_ready[buf], h->copy_stream));
+    KV_CUDA(cudaStreamWaitEvent(s, h->ev_ready[buf], 0));
+    const int rc = enqueue_prefill(h, h->stage[buf], S, b0, nb, h->lse2, h->colsum, s);
+    if (rc != KVEVICT_OK) return rc;
+    KV_CUDA(cudaEventRecord(h->ev_free[buf], s));
+  }
+  h->next_pos = S;
+  // decode, step chunk by step chunk
+  for (int t0 = 0; t0 < T; t0 += tc, ++k) {
+    const int nt = std::min(tc, T - t0);
+    const int buf = k & 1;
+    KV_CUDA(cudaStreamWaitEvent(h->copy_stream, h->ev_free[buf], 0));
+    KV_CUDA(cudaMemcpyAsync(h->stage[buf], decode_keys + (size_t)t0 * per_step, (size_t)nt * per_step * 2,
+                            cudaMemcpyHostToDevice, h->copy_stream));
+    KV_CUDA(cudaEventRecord(h->ev_ready[buf], h->copy_stream));
+    KV_CUDA(cudaStreamWaitEvent(s, h->ev_ready[buf], 0));
+    for (int t = 0; t < nt; ++t) {
+      const int rc = enqueue_step(h, h->stage[buf] + (size_t)t * per_step,
+                                  evicted ? h->ev_stage[buf] + (size_t)t * BLH(h) : nullptr,
+                                  h->next_pos, s);
+      if (rc != KVEVICT_OK) return rc;
+      h->next_pos += 1;
+      h->stepped = true;
+    }
+    if (evicted)
+      KV_CUDA(cudaMemcpyAsync(evicted + (size_t)t0 * BLH(h), h->ev_stage[buf], (size_t)nt * BLH(h) * 4,
+                              cudaMemcpyDeviceToHost, s));
+    KV_CUDA(cudaEventRecord(h->ev_free[buf], s));
+  }
+  return check_error_word(h, s);
+}
+
+int kvevict_read_state(kvevict_t* h, int32_t b, int32_t l, int32_t head, uint16_t* keys, float* scores,
+                       float* gumbel, int32_t* positions, int32_t* n_kept, void* stream) {
+  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  if (b < 0 || b >= h->B || l < 0 || l >= h->L || head < 0 || head >= h->H)
+    return fail(KVEVICT_ERR_INVALID_ARG, "row index out of range");
+  cudaStream_t s = (cudaStream_t)stream;
+  int rc = enqueue_flush(h, s);
+  if (rc != KVEVICT_OK) return rc;
+  const LayerInfo& li = h->layers[l];
+  const int n = (int)std::min<int64_t>(h->next_pos, li.budget);
+  const int64_t rem = (int64_t)b * h->H + head;
+  if (keys && n > 0)
+    KV_CUDA(cudaMemcpyAsync(keys, h->K + (li.row_base + rem * li.cap) * h->D, (size_t)n * h->D * 2,
+                            cudaMemcpyDeviceToHost, s));
+  const int64_t mo = li.meta_base + rem * li.capm;
+  if (scores && n > 0) KV_CUDA(cudaMemcpyAsync(scores, h->score + mo, (size_t)n * 4, cudaMemcpyDeviceToHost, s));
+  if (gumbel && n > 0) KV_CUDA(cudaMemcpyAsync(gumbel, h->gum + mo, (size_t)n * 4, cudaMemcpyDeviceToHost, s));
+  if (positions && n > 0)
+    KV_CUDA(cudaMemcpyAsync(positions, h->pos + mo, (size_t)n * 4, cudaMemcpyDeviceToHost, s));
+  rc = check_error_word(h, s);
+  if (n_kept) *n_kept = n;
+  return rc;
+}
+
+int kvevict_check(kvevict_t* h, void* stream) {
+  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  return check_error_word(h, (cudaStream_t)stream);
+}
+
+int kvevict_next_pos(const kvevict_t* h, int64_t* p) {
+  if (!h || !p) return fail(KVEVICT_ERR_INVALID_ARG, "null argument");
+  *p = h->next_pos;
+  return KVEVICT_OK;
+}
+
+int kvevict_layer_budget(const kvevict_t* h, int32_t l, int32_t* budget) {
+  if (!h || !budget) return fail(KVEVICT_ERR_INVALID_ARG, "null argument");
+  if (l < 0 || l >= h->L) return fail(KVEVICT_ERR_INVALID_ARG, "layer out of range");
+  *budget = h->budgets[l];
+  return KVEVICT_OK;
+}
+
+int kvevict_device_bytes(const kvevict_t* h, size_t* bytes) {
+  if (!h || !bytes) return fail(KVEVICT_ERR_INVALID_ARG, "null argument");
+  *bytes = h->bytes + 2 * h->stage_elems * 2 + 2 * h->ev_stage_elems * 4;
+  return KVEVICT_OK;
+}
+
+}  // extern "C"

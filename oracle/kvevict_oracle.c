@@ -113,25 +113,31 @@ static double round_half_even(double q) {  /* q >= 0, few significant bits */
 }
 
 uint16_t orc_f32_to_f16(float xf) {
-  double x = (double)xf;
-  uint16_t sign = signbit(x) ? 0x8000u : 0u;
-  if (isnan(x)) return (uint16_t)(sign | 0x7E00u);
-  double a = fabs(x);
-  if (a >= 65520.0) return (uint16_t)(sign | 0x7C00u);         /* rounds past 65504 */
-  if (a < 0x1p-14) {                                           /* subnormal range */
-    double m = round_half_even(a * 0x1p24);                    /* exact scaling */
-    return (uint16_t)(sign | (uint16_t)m);                     /* m == 1024 is 2^-14 */
+  uint32_t u;
+  memcpy(&u, &xf, sizeof u);
+  uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+  uint32_t a = u & 0x7FFFFFFFu;
+  if (a > 0x7F800000u) return (uint16_t)(sign | 0x7E00u);       /* NaN */
+  if (a >= 0x477FF000u) return (uint16_t)(sign | 0x7C00u);      /* >= 65520 rounds past 65504 */
+  if (a < 0x38800000u) {                                        /* below 2^-14: subnormal */
+    double m = round_half_even(fabs((double)xf) * 0x1p24);      /* exact scaling */
+    return (uint16_t)(sign | (uint16_t)m);                      /* m == 1024 is 2^-14 */
   }
-  int ex;
-  (void)frexp(a, &ex);                                         /* a in [2^(ex-1), 2^ex) */
-  int E = ex - 1;
-  double m = round_half_even(ldexp(a, 10 - E));                /* in [1024, 2048] */
-  if (m >= 2048.0) { m = 1024.0; E += 1; }
-  if (E > 15) return (uint16_t)(sign | 0x7C00u);
-  return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)(m - 1024.0));
+  /* normal: rebias the exponent (127 -> 15), keep 10 of the 23 fraction bits
+   * and round the 13 dropped bits to nearest, ties to even; a carry out of
+   * the fraction correctly bumps the exponent. */
+  uint32_t e = (a >> 23) - 112u;
+  uint32_t frac = a & 0x7FFFFFu;
+  uint32_t h = (e << 10) | (frac >> 13);
+  uint32_t rest = frac & 0x1FFFu;
+  if (rest > 0x1000u || (rest == 0x1000u && (h & 1u))) h += 1u;
+  return (uint16_t)(sign | h);
 }
 
-double orc_f16_to_f64(uint16_t h) {
+/* Exact values of all 65536 binary16 patterns, from the format's definition. */
+static double f16_value[65536];
+
+static double f16_decode(uint16_t h) {
   int s = (h >> 15) & 1;
   int E = (h >> 10) & 0x1F;
   int M = h & 0x3FF;
@@ -141,6 +147,12 @@ double orc_f16_to_f64(uint16_t h) {
   else v = ldexp((double)(1024 + M), E - 25);
   return s ? -v : v;
 }
+
+__attribute__((constructor)) static void f16_table_init(void) {
+  for (uint32_t h = 0; h < 65536u; ++h) f16_value[h] = f16_decode((uint16_t)h);
+}
+
+double orc_f16_to_f64(uint16_t h) { return f16_value[h]; }
 
 void orc_f32_to_f16_array(int64_t n, const float* x, uint16_t* out) {
   for (int64_t t = 0; t < n; ++t) out[t] = orc_f32_to_f16(x[t]);

@@ -1,0 +1,265 @@
+"""CUDA path vs the fp64 oracle, through the C ABI, on seeded synthetic keys.
+
+Small configurations compare every cache row over the whole run (several TMA
+tiles, ragged tails, every edge case the method has); the five full-size
+workloads run exactly as the benchmark launches them (prompt, then one CUDA
+graph of all decode steps) and compare sampled rows over the whole run.
+"""
+import concurrent.futures as cf
+
+import numpy as np
+import pytest
+
+import workloads
+from workloads import Workload
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def kvx():
+    import kv_cache_attention_02_gb300 as k
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    k.lib()
+    return k
+
+
+@pytest.fixture(scope="module")
+def wgpu():
+    from workloads import gpu
+    gpu.lib()
+    return gpu
+
+
+def head_params(orc, wl, l, h):
+    budgets = orc.budgets(wl.n_layers, wl.avg_budget, wl.n_sink, wl.beta)
+    return orc.HeadParams(D=wl.head_dim, budget=budgets[l], n_sink=wl.n_sink, layer=l, head=h,
+                          tau_init=wl.tau_init, tau_end=wl.tau_end, anneal_steps=wl.anneal_steps,
+                          theta=wl.rope_theta, seed=wl.gumbel_seed)
+
+
+def run_gpu(kvx, wgpu, wl, rows, segments=None, mode="graph"):
+    """Run the workload on the GPU; read back the sampled rows."""
+    h = kvx.from_workload(wl)
+    pre, dec = wgpu.device_inputs(wl)
+    after_prefill = {}
+    if pre is not None:
+        h.prefill(pre)
+        after_prefill = {r: h.read_state(*r) for r in rows}
+    T = wl.decode
+    ev = torch.full((T, wl.batch, wl.n_layers, wl.n_kv_heads), -7, dtype=torch.int32, device="cuda")
+    bounds = sorted(set([0, T] + list(segments or [])))
+    checkpoints = {r: {} for r in rows}
+    for t0, t1 in zip(bounds, bounds[1:]):
+        if mode == "graph":
+            h.decode(dec[t0:t1], ev[t0:t1])
+        else:
+            for t in range(t0, t1):
+                h.step(dec[t], ev[t])
+        if t1 != T:
+            for r in rows:
+                checkpoints[r][t1] = h.read_state(*r)
+    final = {r: h.read_state(*r) for r in rows}
+    h.check()
+    evh = ev.cpu().numpy()
+    h.close()
+    del pre, dec, ev
+    torch.cuda.empty_cache()
+    return after_prefill, evh, final, checkpoints
+
+
+def compare_rows(orc, wl, rows, after_prefill, evh, final, checkpoints, threads=8):
+    import parity
+
+    def one(r):
+        b, l, hh = r
+        keys = wl.head_keys(b, l, hh, 0, wl.positions)
+        prm = head_params(orc, wl, l, hh)
+        return r, parity.run_row(orc, prm, keys[: wl.prefill] if wl.prefill else None,
+                                 keys[wl.prefill:], evh[:, b, l, hh], after_prefill.get(r), final[r],
+                                 checkpoints.get(r))
+
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        reports = dict(ex.map(one, rows))
+    bad = {r: rep.failures for r, rep in reports.items() if not rep.ok()}
+    assert not bad, f"{wl.name}: {bad}"
+    return reports
+
+
+def all_rows(wl):
+    return [(b, l, h) for b in range(wl.batch) for l in range(wl.n_layers)
+            for h in range(wl.n_kv_heads)]
+
+
+def sampled_rows(wl, k=6, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = {(0, 0, 0), (wl.batch - 1, wl.n_layers - 1, wl.n_kv_heads - 1),
+            (wl.batch // 2, wl.n_layers // 2, min(1, wl.n_kv_heads - 1))}
+    while len(rows) < k:
+        rows.add((int(rng.integers(wl.batch)), int(rng.integers(wl.n_layers)),
+                  int(rng.integers(wl.n_kv_heads))))
+    return sorted(rows)
+
+
+SMALL = [
+    Workload("pyramid_anneal_ragged", batch=2, n_layers=3, n_kv_heads=2, head_dim=128,
+             avg_budget=24, beta=2.0, n_sink=4, tau_init=1.0, tau_end=2.0, anneal_steps=40,
+             rope_theta=10000.0, gumbel_seed=7, key_seed=3, prefill=37, decode=60),
+    Workload("d64_no_sinks", batch=1, n_layers=2, n_kv_heads=3, head_dim=64, avg_budget=9,
+             beta=1.0, n_sink=0, tau_init=0.0, tau_end=0.0, anneal_steps=0, rope_theta=10000.0,
+             gumbel_seed=0, key_seed=5, prefill=0, decode=50),
+    Workload("budget_sinks_plus_one", batch=1, n_layers=1, n_kv_heads=2, head_dim=128,
+             avg_budget=5, beta=1.0, n_sink=4, tau_init=0.5, tau_end=0.5, anneal_steps=0,
+             rope_theta=500000.0, gumbel_seed=11, key_seed=6, prefill=3, decode=30),
+    Workload("prefill_equals_budget", batch=1, n_layers=1, n_kv_heads=2, head_dim=64,
+             avg_budget=16, beta=1.0, n_sink=4, tau_init=0.0, tau_end=0.0, anneal_steps=0,
+             rope_theta=10000.0, gumbel_seed=0, key_seed=7, prefill=16, decode=20),
+    Workload("multi_tile_bulk", batch=1, n_layers=2, n_kv_heads=2, head_dim=128, avg_budget=100,
+             beta=1.5, n_sink=4, tau_init=1.0, tau_end=2.0, anneal_steps=150,
+             rope_theta=500000.0, gumbel_seed=1234, key_seed=8, prefill=200, decode=150),
+    Workload("late_riser_small", batch=1, n_layers=2, n_kv_heads=2, head_dim=128, avg_budget=48,
+             beta=1.0, n_sink=4, tau_init=1.0, tau_end=2.0, anneal_steps=300,
+             rope_theta=500000.0, gumbel_seed=3, key_seed=9, prefill=0, decode=300,
+             late_riser=True),
+    workloads.TINY_H2O,
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_small_all_rows(kvx, wgpu, orc, wl):
+    rows = all_rows(wl)
+    seg = [wl.decode // 3]
+    res = run_gpu(kvx, wgpu, wl, rows, segments=seg)
+    reps = compare_rows(orc, wl, rows, *res)
+    assert sum(r.evictions for r in reps.values()) > 0
+
+
+def test_step_path_equals_graph_path(kvx, wgpu):
+    wl = SMALL[0]
+    rows = all_rows(wl)
+    a = run_gpu(kvx, wgpu, wl, rows, mode="graph")
+    b = run_gpu(kvx, wgpu, wl, rows, mode="step")
+    assert np.array_equal(a[1], b[1])
+    for r in rows:
+        for x, y in zip(a[2][r], b[2][r]):
+            assert np.array_equal(x, y)
+
+
+def test_batched_equals_single_row(kvx, wgpu):
+    # keyformer page, keyformer_update_batched: the batched step equals the
+    # per-row loop bit for bit. tau = 0 so the Gumbel hash (which keys on the
+    # layer and head index) cannot differ between the two layouts.
+    wl = Workload("batched", batch=2, n_layers=1, n_kv_heads=3, head_dim=128, avg_budget=40,
+                  beta=1.0, n_sink=4, tau_init=0.0, tau_end=0.0, anneal_steps=0,
+                  rope_theta=10000.0, gumbel_seed=0, key_seed=21, prefill=50, decode=80)
+    pre, dec = wgpu.device_inputs(wl)
+    h = kvx.from_workload(wl)
+    h.prefill(pre)
+    ev = torch.zeros((wl.decode, 2, 1, 3), dtype=torch.int32, device="cuda")
+    h.decode(dec, ev)
+    full = {(b, hh): h.read_state(b, 0, hh) for b in range(2) for hh in range(3)}
+    h.close()
+    for b in range(2):
+        for hh in range(3):
+            one = kvx.KVEvict(batch=1, n_layers=1, n_kv_heads=1, head_dim=128, avg_budget=40,
+                              n_sink=4, rope_theta=10000.0, max_prefill=50)
+            one.prefill(pre[b:b + 1, :, hh:hh + 1].contiguous())
+            ev1 = torch.zeros((wl.decode, 1, 1, 1), dtype=torch.int32, device="cuda")
+            one.decode(dec[:, b:b + 1, :, hh:hh + 1].contiguous(), ev1)
+            st = one.read_state(0, 0, 0)
+            one.close()
+            assert np.array_equal(ev1.cpu().numpy()[:, 0, 0, 0], ev.cpu().numpy()[:, b, 0, hh])
+            # keys, scores and positions; the frozen Gumbel values themselves
+            # are keyed on the head index and differ by design
+            for i in (0, 1, 3):
+                assert np.array_equal(st[i], full[(b, hh)][i])
+
+
+def test_run_host_equals_device_path(kvx, wgpu):
+    wl = SMALL[4]
+    pre, dec = wgpu.device_inputs(wl)
+    h = kvx.from_workload(wl)
+    h.prefill(pre)
+    ev = torch.zeros((wl.decode, wl.batch, wl.n_layers, wl.n_kv_heads), dtype=torch.int32,
+                     device="cuda")
+    h.decode(dec, ev)
+    want = {r: h.read_state(*r) for r in all_rows(wl)}
+    h.close()
+    h2 = kvx.from_workload(wl)
+    pre_h = pre.cpu().pin_memory()
+    dec_h = dec.cpu().pin_memory()
+    ev_h = torch.zeros(tuple(ev.shape), dtype=torch.int32).pin_memory()
+    h2.run_host(pre_h, dec_h, ev_h)
+    assert np.array_equal(ev_h.numpy(), ev.cpu().numpy())
+    for r in all_rows(wl):
+        for x, y in zip(h2.read_state(*r), want[r]):
+            assert np.array_equal(x, y)
+    h2.close()
+
+
+def test_reset_replays_identically(kvx, wgpu):
+    wl = SMALL[0]
+    pre, dec = wgpu.device_inputs(wl)
+    h = kvx.from_workload(wl)
+    outs = []
+    for _ in range(2):
+        h.reset()
+        h.prefill(pre)
+        ev = torch.zeros((wl.decode, wl.batch, wl.n_layers, wl.n_kv_heads), dtype=torch.int32,
+                         device="cuda")
+        h.decode(dec, ev)
+        outs.append((ev.cpu().numpy(), [h.read_state(*r) for r in all_rows(wl)]))
+    h.close()
+    assert np.array_equal(outs[0][0], outs[1][0])
+    for s0, s1 in zip(outs[0][1], outs[1][1]):
+        for x, y in zip(s0, s1):
+            assert np.array_equal(x, y)
+
+
+def test_state_errors(kvx, wgpu):
+    wl = SMALL[3]
+    pre, dec = wgpu.device_inputs(wl)
+    h = kvx.from_workload(wl)
+    h.step(dec[0])
+    with pytest.raises(kvx.KVEvictError) as ei:
+        h.prefill(pre)
+    assert ei.value.code == kvx.ERR_BAD_STATE
+    with pytest.raises(kvx.KVEvictError) as ei:
+        h.read_state(0, 5, 0)
+    assert ei.value.code == kvx.ERR_INVALID_ARG
+    h.close()
+
+
+@pytest.mark.parametrize("wl", list(workloads.ALL.values()), ids=lambda w: w.name)
+def test_gpu_keygen_matches_host(wgpu, wl):
+    rows = sampled_rows(wl, k=4, seed=1)
+    pre, dec = wgpu.device_inputs(wl)
+    for b, l, h in rows:
+        want = wl.head_keys(b, l, h, 0, wl.positions)
+        got = np.concatenate(
+            ([pre[b, l, h].cpu().numpy().view(np.uint16)] if pre is not None else [])
+            + [dec[:, b, l, h].cpu().numpy().view(np.uint16)])
+        assert np.array_equal(got, want)
+    del pre, dec
+    torch.cuda.empty_cache()
+
+
+FULL = [workloads.KEYFORMER_3B, workloads.PYRAMIDKV, workloads.LATE_RISER_TAU0,
+        workloads.LATE_RISER_ANNEAL, workloads.LARGE_CONTEXT]
+
+
+@pytest.mark.parametrize("wl", FULL, ids=lambda w: w.name)
+def test_full_size_sampled_rows(kvx, wgpu, orc, wl):
+    rows = sampled_rows(wl, k=8)
+    res = run_gpu(kvx, wgpu, wl, rows, segments=[wl.decode // 2])
+    reps = compare_rows(orc, wl, rows, *res, threads=8)
+    total = sum(r.evictions for r in reps.values())
+    ties = sum(r.ties for r in reps.values())
+    div = sum(r.tie_divergences for r in reps.values())
+    print(f"{wl.name}: rows {len(rows)} evictions {total} ties {ties} tie-divergences {div} "
+          f"max key ulp {max(r.max_key_ulp for r in reps.values())} "
+          f"max score rel {max(r.max_score_rel for r in reps.values()):.2e}")
+    assert total > 0
