@@ -130,6 +130,14 @@ int kvevict_decode(kvevict_t* h, const uint16_t* keys, int32_t T, int32_t* evict
 int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S,
                      const uint16_t* decode_keys, int32_t T, int32_t* evicted, void* stream);
 
+/* Apply the compaction the last decode step decided (the step kernel leaves
+ * the evicted row in place and the next step or this call removes it while
+ * re-rotating the rows that move). kvevict_read_state calls it itself; a
+ * caller that reads the device arena by other means, or that wants a step's
+ * work finished in full inside a timed region, calls it explicitly. One
+ * kernel launch; a no-op for rows with nothing pending. Errors: CUDA. */
+int kvevict_flush(kvevict_t* h, void* stream);
+
 /* Copy one row's state to host memory (synchronises the stream). Rows
  * are given in slot order: keys [n, D] fp16 bits, scores [n], gumbel [n],
  * positions [n] (the original absolute position of each kept key), n =

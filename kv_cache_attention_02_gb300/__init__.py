@@ -55,6 +55,7 @@ SIGNATURES = {
     "kvevict_run_host": (ctypes.c_int, [P, P, i32, P, i32, P, P]),
     "kvevict_read_state": (ctypes.c_int, [P, i32, i32, i32, P, P, P, P, P, P]),
     "kvevict_check": (ctypes.c_int, [P, P]),
+    "kvevict_flush": (ctypes.c_int, [P, P]),
     "kvevict_next_pos": (ctypes.c_int, [P, P]),
     "kvevict_layer_budget": (ctypes.c_int, [P, i32, P]),
     "kvevict_device_bytes": (ctypes.c_int, [P, P]),
@@ -177,7 +178,7 @@ class KVEvict:
     # ------------------------------------------------------------------ queries
     def read_state(self, b: int, l: int, h: int, stream=None):
         """(keys fp16-bits [n, D], scores f32 [n], gumbel f32 [n], positions i32 [n])."""
-        cap = self.budgets[l] + 1
+        cap = self.budgets[l] + 1 if 0 <= l < self.L else 1  # the library validates indices
         keys = np.zeros((cap, self.D), np.uint16)
         sc = np.zeros(cap, np.float32)
         g = np.zeros(cap, np.float32)
@@ -188,6 +189,10 @@ class KVEvict:
                                         _stream(stream)))
         k = n.value
         return keys[:k], sc[:k], g[:k], pos[:k]
+
+    def flush(self, stream=None):
+        """Apply the last step's pending compaction (one kernel launch)."""
+        _check(lib().kvevict_flush(self._h, _stream(stream)))
 
     def check(self, stream=None):
         _check(lib().kvevict_check(self._h, _stream(stream)))

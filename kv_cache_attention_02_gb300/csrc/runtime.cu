@@ -565,6 +565,11 @@ int kvevict_read_state(kvevict_t* h, int32_t b, int32_t l, int32_t head, uint16_
   return rc;
 }
 
+int kvevict_flush(kvevict_t* h, void* stream) {
+  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  return enqueue_flush(h, (cudaStream_t)stream);
+}
+
 int kvevict_check(kvevict_t* h, void* stream) {
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   return check_error_word(h, (cudaStream_t)stream);
