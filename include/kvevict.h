@@ -160,6 +160,33 @@ int kvevict_layer_budget(const kvevict_t* h, int32_t l, int32_t* budget);
 /* Device bytes held by the handle (arena + scratch + staging). */
 int kvevict_device_bytes(const kvevict_t* h, size_t* bytes);
 
+/* Prompt scoring that allocates nothing. The paper has no counterpart: this is
+ * for callers that cannot call cudaMalloc -- an inference engine that reserves
+ * the whole device heap for its own memory pool at start-up (a further
+ * cudaMalloc then fails or fragments that pool), or a latency-bound serving
+ * loop that cannot take cudaMalloc's implicit device-wide synchronisation.
+ * It runs the same two tensor-core passes as kvevict_prefill's scorer and
+ * writes each row's causal softmax column sums (diagonal included): the
+ * scores kvevict_prefill gives a prompt before any eviction.
+ *   keys:   device fp16 [heads, S, D], each key RoPE-rotated at its position.
+ *   colsum: device float [heads, S], written in full by the call.
+ * Working memory is a fixed 16 MiB device array inside the library, present on
+ * every GPU that loads the library until the process exits. It limits a call
+ * to 2 * heads * round_up(S, 64) <= 4,194,304 floats (for example 512 rows of
+ * 4096 tokens); a larger call returns INVALID_ARG without launching anything.
+ * Every call shares that array and leaves its contents behind; nothing in it
+ * needs to start at zero, since a call reads only entries it wrote itself
+ * (padding entries it reads are masked out). Calls whose work overlaps on the
+ * GPU (other streams, other threads) race on the array: serialise them.
+ * The first call on each device (and head_dim) looks up the array's device
+ * address and sets the kernels' shared-memory attribute, with that device
+ * current; make that first call before any stream capture. With lazy module
+ * loading the driver places the array when the library's kernels first load,
+ * which can be during that first call. Errors: INVALID_ARG (null pointers,
+ * head_dim not 64/128, negative or over-limit sizes), CUDA. */
+int kvevict_prefill_scores_noalloc(const uint16_t* keys, int32_t heads, int32_t S,
+                                   int32_t head_dim, float* colsum, void* stream);
+
 /* Message of the last failure on the calling thread ("" if none). */
 const char* kvevict_last_error(void);
 

@@ -60,6 +60,7 @@ SIGNATURES = {
     "kvevict_layer_budget": (ctypes.c_int, [P, i32, P]),
     "kvevict_device_bytes": (ctypes.c_int, [P, P]),
     "kvevict_last_error": (ctypes.c_char_p, []),
+    "kvevict_prefill_scores_noalloc": (ctypes.c_int, [P, i32, i32, i32, P, P]),
 }
 
 
@@ -92,6 +93,19 @@ def budgets(n_layers: int, avg_budget: int, n_sink: int, beta: float) -> list[in
     out = (i32 * max(1, n_layers))()
     _check(lib().kvevict_budgets(n_layers, avg_budget, n_sink, beta, ctypes.addressof(out)))
     return list(out)[:n_layers]
+
+
+def prefill_scores_noalloc(keys, colsum, stream=None):
+    """Causal column sums of prompts with no device allocation.
+
+    keys: device fp16 [heads, S, D]; colsum: device float32 [heads, S] (output).
+    For callers that cannot allocate device memory; see the C declaration of
+    kvevict_prefill_scores_noalloc for the size limit and sharing rules.
+    """
+    heads, S, D = (int(x) for x in keys.shape)
+    assert tuple(colsum.shape) == (heads, S)
+    _check(lib().kvevict_prefill_scores_noalloc(_ptr(keys), heads, S, D, _ptr(colsum),
+                                                _stream(stream)))
 
 
 def _ptr(t) -> int:

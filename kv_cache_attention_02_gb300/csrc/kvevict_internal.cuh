@@ -109,6 +109,7 @@ cudaError_t launch_flush(const FlushArgs& a, int D, int heads, cudaStream_t s);
 cudaError_t prefill_setup(int D, int max_prefill);
 size_t prefill_score_smem(int D);
 cudaError_t launch_prefill_scores(const PrefillScoreArgs& a, int D, cudaStream_t s);
+cudaError_t prefill_score_setup(int D);  // shared-memory attribute of the two scoring passes only
 size_t prefill_select_smem(int S);
 cudaError_t launch_prefill_select(const PrefillSelectArgs& a, int D, int heads, cudaStream_t s);
 

@@ -1,0 +1,135 @@
+// noalloc.cu -- prompt scoring for callers that cannot allocate device memory.
+//
+// Some callers of this library cannot call cudaMalloc: an inference engine
+// that reserves the whole device heap for its own pool at start-up (an extra
+// cudaMalloc then fails or fragments that pool), or a latency-bound serving
+// loop that cannot afford cudaMalloc's implicit device-wide synchronisation.
+// kvevict_prefill_scores_noalloc gives them the prompt scorer (causal
+// column sums, the two tensor-core passes of prefill.cu) with its working
+// memory in a fixed file-scope device array instead of an allocation. The
+// caller passes the keys and the output buffer; nothing is allocated.
+//
+// The array costs kNoAllocScratchFloats * 4 bytes (16 MiB) on every GPU that
+// loads this library, for as long as the process lives. Every call shares it:
+// calls whose work overlaps on the GPU (different streams, or other threads)
+// race on it and must be serialised by the caller.
+#include "kvevict.h"
+#include "kvevict_internal.cuh"
+
+#include <cmath>
+#include <mutex>
+#include <string>
+
+namespace kvx {
+void set_last_error(const std::string& msg);  // runtime.cu: kvevict_last_error()'s message
+}
+
+namespace {
+
+constexpr size_t kNoAllocScratchFloats = size_t(4) << 20;   // 16 MiB
+constexpr int kMaxDevices = 64;
+
+// Working memory of the allocation-free scorer: [2, heads, Sp] floats (the
+// row log-sum-exps, then the padded column sums).
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+
+std::mutex g_setup_mu;
+float* g_scratch_ptr[kMaxDevices] = {};
+bool g_setup_done[kMaxDevices][2] = {};
+
+// Copy the padded column sums [heads, Sp] to the caller's [heads, S].
+__global__ void gather_colsum_kernel(const float* src, int Sp, float* dst, int S, int64_t total) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t h = i / S;
+    const int64_t j = i - h * S;
+    dst[i] = src[h * Sp + j];
+  }
+}
+
+// Once per device (and head_dim), with that device current: resolve the
+// device address of the scratch array and set the scoring kernels' shared
+// memory attribute.
+int setup_device(int D, float** scratch) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    kvx::set_last_error(std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+    return KVEVICT_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    kvx::set_last_error("device ordinal beyond the supported 64");
+    return KVEVICT_ERR_INVALID_ARG;
+  }
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+      kvx::set_last_error(std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+      return KVEVICT_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = static_cast<float*>(p);
+  }
+  const int di = D == 64 ? 0 : 1;
+  if (!g_setup_done[dev][di]) {
+    e = kvx::prefill_score_setup(D);
+    if (e != cudaSuccess) {
+      kvx::set_last_error(std::string("prefill_score_setup: ") + cudaGetErrorString(e));
+      return KVEVICT_ERR_CUDA;
+    }
+    g_setup_done[dev][di] = true;
+  }
+  *scratch = g_scratch_ptr[dev];
+  return KVEVICT_OK;
+}
+
+}  // namespace
+
+extern "C" int kvevict_prefill_scores_noalloc(const uint16_t* keys, int32_t heads, int32_t S,
+                                              int32_t head_dim, float* colsum, void* stream) {
+  if (!keys || !colsum) {
+    kvx::set_last_error("keys and colsum must not be null");
+    return KVEVICT_ERR_INVALID_ARG;
+  }
+  if (head_dim != 64 && head_dim != 128) {
+    kvx::set_last_error("head_dim must be 64 or 128");
+    return KVEVICT_ERR_INVALID_ARG;
+  }
+  if (heads < 0 || S < 0) {
+    kvx::set_last_error("heads and S must be >= 0");
+    return KVEVICT_ERR_INVALID_ARG;
+  }
+  if (heads == 0 || S == 0) return KVEVICT_OK;
+  const int64_t Sp = ((int64_t)S + 63) / 64 * 64;
+  if (2 * (int64_t)heads * Sp > (int64_t)kNoAllocScratchFloats) {
+    kvx::set_last_error("heads * round_up(S, 64) exceeds the fixed scratch of 2,097,152 floats per pass");
+    return KVEVICT_ERR_INVALID_ARG;
+  }
+  float* scratch = nullptr;
+  const int rc = setup_device(head_dim, &scratch);
+  if (rc != KVEVICT_OK) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  kvx::PrefillScoreArgs a{};
+  a.keys = reinterpret_cast<const __half*>(keys);
+  a.lse2 = scratch;
+  a.colsum = scratch + (size_t)heads * Sp;
+  a.S = S;
+  a.Sp = (int)Sp;
+  a.heads = heads;
+  a.scale2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
+  cudaError_t e = kvx::launch_prefill_scores(a, head_dim, s);
+  if (e == cudaSuccess) {
+    const int64_t total = (int64_t)heads * S;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    gather_colsum_kernel<<<(unsigned)blocks, 256, 0, s>>>(a.colsum, (int)Sp, colsum, S, total);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    kvx::set_last_error(std::string("launch: ") + cudaGetErrorString(e));
+    return KVEVICT_ERR_CUDA;
+  }
+  return KVEVICT_OK;
+}
+

@@ -398,6 +398,20 @@ cudaError_t prefill_setup(int D, int max_prefill) {
   return e;
 }
 
+cudaError_t prefill_score_setup(int D) {
+  const int score = (int)prefill_score_smem(D);
+  const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e;
+  if (D == 64) {
+    e = cudaFuncSetAttribute(prefill_score_kernel<64, false>, attr, score);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(prefill_score_kernel<64, true>, attr, score);
+  } else {
+    e = cudaFuncSetAttribute(prefill_score_kernel<128, false>, attr, score);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(prefill_score_kernel<128, true>, attr, score);
+  }
+  return e;
+}
+
 cudaError_t launch_prefill_scores(const PrefillScoreArgs& a, int D, cudaStream_t s) {
   if (a.S <= 0 || a.heads <= 0) return cudaSuccess;
   const int nb = (a.S + kBM - 1) / kBM;

@@ -71,6 +71,10 @@ cudaError_t dalloc(T** p, size_t count) {
 
 }  // namespace
 
+namespace kvx {
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace kvx
+
 struct kvevict {
   kvevict_config cfg{};
   int device = 0;
