@@ -87,13 +87,16 @@ __global__ void __launch_bounds__(kPThreads) prefill_score_kernel(const PrefillS
   const int g = lane >> 2, c4 = lane & 3;
   const int S = a.S;
   const int nb = (S + kBM - 1) / kBM;
-  const int head = blockIdx.x;
+  // one flat grid, head-major: a head's causal blocks run together and share
+  // its keys through L2; within a head the heaviest block goes first
+  const int head = (int)(blockIdx.x / (unsigned)nb);
+  const int bidx = (int)(blockIdx.x - (unsigned)head * (unsigned)nb);
   const __half* Kh = a.keys + (size_t)head * S * D;
   const float* lse_h = a.lse2 + (size_t)head * a.Sp;
 
   // pass 1: this CTA owns rows ia (query block), visits column blocks 0..ia
   // pass 2: this CTA owns rows ja (key block, transposed), visits row blocks ja..nb-1
-  const int ablk = COLSUM ? (int)blockIdx.y : nb - 1 - (int)blockIdx.y;
+  const int ablk = COLSUM ? bidx : nb - 1 - bidx;
   const int first = COLSUM ? ablk : 0;
   const int last = COLSUM ? nb - 1 : ablk;
   const int nblk = last - first + 1;
@@ -415,7 +418,7 @@ cudaError_t prefill_score_setup(int D) {
 cudaError_t launch_prefill_scores(const PrefillScoreArgs& a, int D, cudaStream_t s) {
   if (a.S <= 0 || a.heads <= 0) return cudaSuccess;
   const int nb = (a.S + kBM - 1) / kBM;
-  const dim3 grid(a.heads, nb);  // heavy causal blocks first (blockIdx.y = 0)
+  const dim3 grid((unsigned)(a.heads * nb));
   const size_t smem = prefill_score_smem(D);
   if (D == 64) {
     prefill_score_kernel<64, false><<<grid, kPThreads, smem, s>>>(a);
