@@ -172,7 +172,7 @@ int kvevict_device_bytes(const kvevict_t* h, size_t* bytes);
  *   colsum: device float [heads, S], written in full by the call.
  * Working memory is a fixed 16 MiB device array inside the library, present on
  * every GPU that loads the library until the process exits. It limits a call
- * to 2 * heads * round_up(S, 64) <= 4,194,304 floats (for example 512 rows of
+ * to 2 * heads * round_up(S, 128) <= 4,194,304 floats (for example 512 rows of
  * 4096 tokens); a larger call returns INVALID_ARG without launching anything.
  * Every call shares that array and leaves its contents behind; nothing in it
  * needs to start at zero, since a call reads only entries it wrote itself

@@ -77,6 +77,7 @@ struct PrefillScoreArgs {
   int Sp;                  // scratch row stride: S rounded up to 64
   int heads;
   float scale2;            // log2(e) / sqrt(D)
+  int* err;                // error word for bounded waits, or null
 };
 
 struct PrefillSelectArgs {
@@ -106,10 +107,12 @@ size_t decode_step_smem(int D, int capm_max);
 cudaError_t launch_decode_step(const DecodeArgs& a, int D, int heads, size_t smem, cudaStream_t s);
 cudaError_t launch_flush(const FlushArgs& a, int D, int heads, cudaStream_t s);
 
-cudaError_t prefill_setup(int D, int max_prefill);
-size_t prefill_score_smem(int D);
-cudaError_t launch_prefill_scores(const PrefillScoreArgs& a, int D, cudaStream_t s);
-cudaError_t prefill_score_setup(int D);  // shared-memory attribute of the two scoring passes only
+cudaError_t prefill_setup(int D, int max_prefill);  // bulk-eviction kernel's shared memory
+// tcgen05/TMEM scorer (prefill_tc.cu): a.Sp must be S rounded up to kPrefillRowPad
+constexpr int kPrefillRowPad = 128;
+size_t prefill_tc_smem(int D);
+cudaError_t prefill_tc_setup(int D);
+cudaError_t launch_prefill_tc(const PrefillScoreArgs& a, int D, cudaStream_t s);
 size_t prefill_select_smem(int S);
 cudaError_t launch_prefill_select(const PrefillSelectArgs& a, int D, int heads, cudaStream_t s);
 

@@ -5,7 +5,7 @@
 // cudaMalloc then fails or fragments that pool), or a latency-bound serving
 // loop that cannot afford cudaMalloc's implicit device-wide synchronisation.
 // kvevict_prefill_scores_noalloc gives them the prompt scorer (causal
-// column sums, the two tensor-core passes of prefill.cu) with its working
+// column sums, the two tensor-core passes of prefill_tc.cu) with its working
 // memory in a fixed file-scope device array instead of an allocation. The
 // caller passes the keys and the output buffer; nothing is allocated.
 //
@@ -73,9 +73,9 @@ int setup_device(int D, float** scratch) {
   }
   const int di = D == 64 ? 0 : 1;
   if (!g_setup_done[dev][di]) {
-    e = kvx::prefill_score_setup(D);
+    e = kvx::prefill_tc_setup(D);
     if (e != cudaSuccess) {
-      kvx::set_last_error(std::string("prefill_score_setup: ") + cudaGetErrorString(e));
+      kvx::set_last_error(std::string("prefill_tc_setup: ") + cudaGetErrorString(e));
       return KVEVICT_ERR_CUDA;
     }
     g_setup_done[dev][di] = true;
@@ -101,9 +101,9 @@ extern "C" int kvevict_prefill_scores_noalloc(const uint16_t* keys, int32_t head
     return KVEVICT_ERR_INVALID_ARG;
   }
   if (heads == 0 || S == 0) return KVEVICT_OK;
-  const int64_t Sp = ((int64_t)S + 63) / 64 * 64;
+  const int64_t Sp = ((int64_t)S + kvx::kPrefillRowPad - 1) / kvx::kPrefillRowPad * kvx::kPrefillRowPad;
   if (2 * (int64_t)heads * Sp > (int64_t)kNoAllocScratchFloats) {
-    kvx::set_last_error("heads * round_up(S, 64) exceeds the fixed scratch of 2,097,152 floats per pass");
+    kvx::set_last_error("heads * round_up(S, 128) exceeds the fixed scratch of 2,097,152 floats per pass");
     return KVEVICT_ERR_INVALID_ARG;
   }
   float* scratch = nullptr;
@@ -118,7 +118,8 @@ extern "C" int kvevict_prefill_scores_noalloc(const uint16_t* keys, int32_t head
   a.Sp = (int)Sp;
   a.heads = heads;
   a.scale2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
-  cudaError_t e = kvx::launch_prefill_scores(a, head_dim, s);
+  a.err = nullptr;
+  cudaError_t e = kvx::launch_prefill_tc(a, head_dim, s);
   if (e == cudaSuccess) {
     const int64_t total = (int64_t)heads * S;
     int64_t blocks = (total + 255) / 256;

@@ -1,0 +1,413 @@
+// prefill_tc.cu -- the prompt scorer on the 5th-generation tensor cores.
+//
+// Computes, per cache row, the column sums of the causal softmax(K K^T/sqrt(D))
+// (diagonal included): what the prompt's S tokens would accumulate as S decode
+// steps without eviction (page "veloxquant_mlx.quantizers.keyformer module",
+// keyformer_update, "For each of the S incoming tokens", steps 1-2).
+//
+//   pass 1 (COLSUM = false): CTA = (row, 128-query block I); tiles J = 0..I;
+//            per query row i: lse2_i = log2 sum_{j<=i} 2^(s_ij), s = K_i.K_j*log2e/sqrt(D)
+//   pass 2 (COLSUM = true):  CTA = (row, 128-key block J); tiles I = J..nb-1 of the
+//            transposed product (TMEM lanes = key j, columns = query i);
+//            colsum_j = sum_{i>=j} 2^(s_ij - lse2_i), summed per lane in registers.
+//
+// Roles in a 192-thread CTA:
+//   warp 0      one thread issues TMA loads (3-D tensor map [heads, S, D], 128-byte
+//               swizzle, two 64-element halves per 128-row tile) into a 2-stage ring;
+//   warp 1      allocates 256 TMEM columns (two 128x128 fp32 accumulators) and one
+//               thread issues tcgen05.mma (M=128, N=128, K=16, f16 in, f32 out);
+//               tcgen05.commit releases the smem stage and publishes the accumulator;
+//   warps 2..5  the epilogue warpgroup: tcgen05.ld 32 columns at a time, mask, exp2,
+//               online row max/sum (pass 1) or masked column sums (pass 2).
+// Every mbarrier wait is bounded; on expiry the CTA sets the error word, drains
+// and frees its TMEM.
+#include "kvevict_internal.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace kvx {
+namespace {
+
+constexpr int kTB = 128;           // tile rows (M) and columns (N)
+constexpr int kTCThreads = 192;
+constexpr int kStagesTC = 2;
+constexpr int kTmemCols = 256;     // two 128-column fp32 accumulators
+
+template <int D>
+struct TCGeo {
+  static constexpr int KH = D / 64;              // 128-byte K-halves per row
+  static constexpr int HALFB = kTB * 128;        // one half tile, 16 KB
+  static constexpr int TILEB = KH * HALFB;
+  static constexpr int KSTEPS = D / 16;
+};
+
+struct TCSmem {
+  size_t a, b, lse, bars, tmem, total;
+};
+
+template <int D>
+__host__ __device__ constexpr TCSmem tc_layout() {
+  TCSmem L{};
+  size_t o = 0;
+  L.a = o;    o += TCGeo<D>::TILEB;
+  L.b = o;    o += (size_t)kStagesTC * TCGeo<D>::TILEB;
+  L.lse = o;  o += 2 * kTB * sizeof(float);
+  L.bars = o; o += 16 * 8;
+  L.tmem = o; o += 16;
+  L.total = o + 1024;  // slack to align the tile region to 1024 bytes
+  return L;
+}
+
+// ---------------------------------------------------------------- tcgen05 / TMA PTX
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), descriptor
+// version 1. The leading byte offset is unused for swizzled K-major layouts.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: f32 accumulator, A and B f16, both
+// K-major, N = 128 (N>>3 at bit 17), M = 128 (M>>4 at bit 24).
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kTB >> 3) << 17) | ((uint32_t)(kTB >> 4) << 24);
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void epi_bar() {  // named barrier for the 128 epilogue threads
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// Named barrier for the 128 epilogue threads that also ORs a predicate across
+// them, so the whole warpgroup leaves its loop together.
+__device__ __forceinline__ bool epi_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
+// Bounded wait that also watches the CTA's abort flag.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      if (err) atomicOr(err, kErrWaitTimeout);
+      return false;
+    }
+  }
+}
+
+template <int D, bool COLSUM>
+__global__ void __launch_bounds__(kTCThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const PrefillScoreArgs a) {
+  using G = TCGeo<D>;
+  constexpr TCSmem SL = tc_layout<D>();
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* smem = smem_raw + (base - raw);
+  const uint32_t sA = base + (uint32_t)SL.a;
+  const uint32_t sB = base + (uint32_t)SL.b;
+  float* lse_s = reinterpret_cast<float*>(smem + SL.lse);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SL.bars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL.tmem);
+  __shared__ int s_abort;
+  auto full = [&](int s) { return smem_addr(&bars[s]); };
+  auto empty = [&](int s) { return smem_addr(&bars[2 + s]); };
+  auto acc_full = [&](int b) { return smem_addr(&bars[4 + b]); };
+  auto acc_empty = [&](int b) { return smem_addr(&bars[6 + b]); };
+  const uint32_t a_full = smem_addr(&bars[8]);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = a.S;
+  const int nb = (S + kTB - 1) / kTB;
+  const int head = (int)(blockIdx.x / (unsigned)nb);
+  const int bidx = (int)(blockIdx.x - (unsigned)head * (unsigned)nb);
+  const int ablk = COLSUM ? bidx : nb - 1 - bidx;   // heaviest causal block first
+  const int first = COLSUM ? ablk : 0;
+  const int nblk = (COLSUM ? nb - 1 : ablk) - first + 1;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStagesTC; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), 4);
+    }
+    mbar_init(a_full, 1);
+    mbar_init(smem_addr(&bars[9]), 1);   // drain barrier (abort path only)
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  if (warp == 1) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  volatile int* abort_flag = &s_abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
+      mbar_expect_tx(a_full, G::TILEB);
+      for (int kh = 0; kh < G::KH; ++kh)
+        tma_load_3d(sA + kh * G::HALFB, &kmap, kh * 64, ablk * kTB, head, a_full);
+      int issued = 0;
+      for (int k = 0; k < nblk; ++k) {
+        const int s = k % kStagesTC;
+        if (k >= kStagesTC &&
+            !wait_or_abort(empty(s), (uint32_t)((k / kStagesTC - 1) & 1), abort_flag, a.err))
+          break;
+        mbar_expect_tx(full(s), G::TILEB);
+        for (int kh = 0; kh < G::KH; ++kh)
+          tma_load_3d(sB + s * G::TILEB + kh * G::HALFB, &kmap, kh * 64, (first + k) * kTB, head,
+                      full(s));
+        issued = k + 1;
+      }
+      if (*abort_flag) {  // give copies still in flight a moment to land before exit
+        (void)mbar_wait_bounded(a_full, 0, 10000000ull);
+        for (int k = issued > kStagesTC ? issued - kStagesTC : 0; k < issued; ++k)
+          (void)mbar_wait_bounded(full(k % kStagesTC), (uint32_t)((k / kStagesTC) & 1), 10000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && wait_or_abort(a_full, 0, abort_flag, a.err)) {
+      for (int k = 0; k < nblk; ++k) {
+        const int s = k % kStagesTC, b = k & 1;
+        if (!wait_or_abort(full(s), (uint32_t)((k / kStagesTC) & 1), abort_flag, a.err)) break;
+        if (k >= 2 && !wait_or_abort(acc_empty(b), (uint32_t)((k / 2 - 1) & 1), abort_flag, a.err))
+          break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(b * kTB);
+#pragma unroll
+        for (int kk = 0; kk < G::KSTEPS; ++kk) {
+          const uint32_t off = (uint32_t)((kk >> 2) * G::HALFB + (kk & 3) * 32);
+          tc_mma(d, sw128_desc(sA + off), sw128_desc(sB + s * G::TILEB + off), kk > 0 ? 1u : 0u);
+        }
+        tc_commit(empty(s));
+        tc_commit(acc_full(b));
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warpgroup
+    const int q = warp & 3;                       // TMEM lane quadrant of this warp
+    const int r = q * 32 + lane;                  // tile row = TMEM lane
+    const int rowA = ablk * kTB + r;              // query row i (pass 1) / key row j (pass 2)
+    const int et = tid - 64;                      // 0..127 within the epilogue
+    const float* lse_h = a.lse2 + (size_t)head * a.Sp;
+    float run_m = -INFINITY, run_l = 0.f, csum = 0.f;
+    for (int k = 0; k < nblk; ++k) {
+      const int b = k & 1;
+      const int colB0 = (first + k) * kTB;
+      if (COLSUM) lse_s[b * kTB + et] = lse_h[colB0 + et];   // this tile's 128 query lse values
+      const bool ok = wait_or_abort(acc_full(b), (uint32_t)((k / 2) & 1), abort_flag, a.err);
+      if (epi_any(!ok)) break;                    // also publishes lse_s to the warpgroup
+      tc_fence_after();
+      const bool full_tile = COLSUM ? (colB0 > ablk * kTB + kTB - 1 && colB0 + kTB <= S)
+                                    : (colB0 + kTB - 1 < ablk * kTB && ablk * kTB + kTB <= S);
+#pragma unroll 1
+      for (int c = 0; c < kTB / 32; ++c) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * kTB + c * 32), v);
+        if (!COLSUM) {
+          float cm = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int j = colB0 + c * 32 + e;
+            const float s = v[e] * a.scale2;
+            v[e] = (full_tile || (j <= rowA && j < S)) ? s : -INFINITY;
+            cm = fmaxf(cm, v[e]);
+          }
+          const float mn = fmaxf(run_m, cm);
+          if (mn != -INFINITY) {
+            float sum = 0.f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sum += exp2f(v[e] - mn);
+            run_l = run_l * exp2f(run_m - mn) + sum;
+            run_m = mn;
+          }
+        } else {
+          const float* lt = lse_s + b * kTB + c * 32;
+          float sum = 0.f;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int i = colB0 + c * 32 + e;
+            const float p = exp2f(v[e] * a.scale2 - lt[e]);
+            sum += (full_tile || (i >= rowA && i < S)) ? p : 0.f;
+          }
+          csum += sum;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty(b));
+      if (COLSUM) epi_bar();                      // lse_s[b] free for tile k+2
+    }
+    if (!*abort_flag && rowA < S) {
+      if (COLSUM)
+        a.colsum[(size_t)head * a.Sp + rowA] = csum;
+      else
+        a.lse2[(size_t)head * a.Sp + rowA] = run_m + log2f(run_l);
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  __syncthreads();
+  if (*abort_flag && tid == 32) {
+    // let any MMA still in flight finish before the accumulators are freed
+    tc_commit(smem_addr(&bars[9]));
+    (void)mbar_wait_bounded(smem_addr(&bars[9]), 0, 10000000ull);
+  }
+  __syncwarp();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+size_t prefill_tc_smem(int D) { return D == 64 ? tc_layout<64>().total : tc_layout<128>().total; }
+
+cudaError_t prefill_tc_setup(int D) {
+  const int smem = (int)prefill_tc_smem(D);
+  const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e;
+  if (D == 64) {
+    e = cudaFuncSetAttribute(prefill_tc_kernel<64, false>, attr, smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(prefill_tc_kernel<64, true>, attr, smem);
+  } else {
+    e = cudaFuncSetAttribute(prefill_tc_kernel<128, false>, attr, smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(prefill_tc_kernel<128, true>, attr, smem);
+  }
+  return e;
+}
+
+// Both passes over a.heads rows of S keys; a.Sp must be S rounded up to 128.
+cudaError_t launch_prefill_tc(const PrefillScoreArgs& a, int D, cudaStream_t s) {
+  if (a.S <= 0 || a.heads <= 0) return cudaSuccess;
+  auto enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  // keys as a 3-D tensor [heads, S, D]: box = 64 elements (128 bytes) x 128 rows x 1 row
+  CUtensorMap map;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.S, (cuuint64_t)a.heads};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.S * D * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)kTB, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(a.keys), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const int nb = (a.S + kTB - 1) / kTB;
+  const dim3 grid((unsigned)(a.heads * nb));
+  const size_t smem = prefill_tc_smem(D);
+  if (D == 64) {
+    prefill_tc_kernel<64, false><<<grid, kTCThreads, smem, s>>>(map, a);
+    prefill_tc_kernel<64, true><<<grid, kTCThreads, smem, s>>>(map, a);
+  } else {
+    prefill_tc_kernel<128, false><<<grid, kTCThreads, smem, s>>>(map, a);
+    prefill_tc_kernel<128, true><<<grid, kTCThreads, smem, s>>>(map, a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kvx

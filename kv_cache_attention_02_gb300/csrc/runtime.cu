@@ -157,7 +157,7 @@ int enqueue_step(kvevict* h, const uint16_t* k_new, int32_t* evicted, int64_t p,
 int enqueue_prefill(kvevict* h, const uint16_t* keys, int32_t S, int b0, int nb, float* lse2,
                     float* colsum, cudaStream_t s) {
   const int heads = nb * h->L * h->H;
-  const int Sp = (S + 63) / 64 * 64;
+  const int Sp = (S + kvx::kPrefillRowPad - 1) / kvx::kPrefillRowPad * kvx::kPrefillRowPad;
   kvx::PrefillScoreArgs sa{};
   sa.keys = reinterpret_cast<const __half*>(keys);
   sa.lse2 = lse2;
@@ -166,7 +166,8 @@ int enqueue_prefill(kvevict* h, const uint16_t* keys, int32_t S, int b0, int nb,
   sa.Sp = Sp;
   sa.heads = heads;
   sa.scale2 = (float)(1.4426950408889634 / std::sqrt((double)h->D));
-  KV_CUDA(kvx::launch_prefill_scores(sa, h->D, s));
+  sa.err = h->err;
+  KV_CUDA(kvx::launch_prefill_tc(sa, h->D, s));
   kvx::PrefillSelectArgs pa{};
   pa.keys = sa.keys;
   pa.colsum = colsum;
@@ -316,7 +317,7 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
     return fail(KVEVICT_ERR_INVALID_ARG, "layer budget too large for the single-CTA decode step");
   }
   h->max_delta = std::max(1, c.max_prefill);
-  h->Sp_max = (int64_t)(c.max_prefill + 63) / 64 * 64;
+  h->Sp_max = (int64_t)(c.max_prefill + kvx::kPrefillRowPad - 1) / kvx::kPrefillRowPad * kvx::kPrefillRowPad;
 
   auto bail = [&](int code) {
     free_all(h);
@@ -339,11 +340,13 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
     int optin = 0;
     KV_CUDA_CREATE(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device));
     if (h->decode_smem + 1024 > (size_t)optin ||
-        kvx::prefill_select_smem(std::max(1, c.max_prefill)) + 1024 > (size_t)optin)
+        kvx::prefill_select_smem(std::max(1, c.max_prefill)) + 1024 > (size_t)optin ||
+        kvx::prefill_tc_smem(h->D) + 1024 > (size_t)optin)
       return bail(fail(KVEVICT_ERR_INVALID_ARG, "layer budget or max_prefill too large for shared memory"));
   }
   KV_CUDA_CREATE(kvx::decode_step_setup(h->D, h->decode_smem));
   KV_CUDA_CREATE(kvx::prefill_setup(h->D, c.max_prefill));
+  KV_CUDA_CREATE(kvx::prefill_tc_setup(h->D));
   KV_CUDA_CREATE(dalloc(&h->d_layers, (size_t)c.n_layers));
   KV_CUDA_CREATE(dalloc(&h->K, (size_t)rows * h->D));
   KV_CUDA_CREATE(dalloc(&h->score, (size_t)meta));
