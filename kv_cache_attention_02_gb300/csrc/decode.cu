@@ -28,11 +28,13 @@
 namespace kvx {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kTPR = 8;                       // threads per key row
-constexpr int kRowsPerPass = kThreads / kTPR;  // 32
-constexpr int kTile = 64;                      // rows per TMA tile
-constexpr int kStages = 4;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;   // 256 threads work on key rows
+constexpr int kThreads = kConsumers + 32;         // + one TMA producer warp
+constexpr int kTPR = 8;                           // threads per key row
+constexpr int kRowsPerPass = kConsumers / kTPR;   // 32
+constexpr int kTile = 64;                         // rows per TMA tile
+constexpr int kStages = 6;
 
 template <int D>
 struct Geo {
@@ -44,7 +46,8 @@ struct Geo {
 };
 
 struct SmemLayout {
-  size_t ring, bars, slog, ssc, sg, redf, redi, total;
+  size_t ring, bars, slog, redf, redi, total;
+  size_t msc, mg, mpos;   // score / Gumbel / position copies, placed in the ring after the stream
 };
 
 template <int D>
@@ -52,61 +55,62 @@ __host__ __device__ inline SmemLayout decode_layout(int capm) {
   SmemLayout L{};
   size_t o = 0;
   L.ring = o;  o += (size_t)kStages * Geo<D>::TILEB;
-  L.bars = o;  o += 64;
+  L.bars = o;  o += 2 * 8 * (kStages + 1);
   const size_t arr = ((size_t)(capm + 4) * 4 + 127) / 128 * 128;
   L.slog = o;  o += arr;
-  L.ssc = o;   o += arr;
-  L.sg = o;    o += arr;
   L.redf = o;  o += 64 * 4;
   L.redi = o;  o += 64 * 4;
   L.total = o;
+  L.msc = L.ring;
+  L.mg = L.msc + arr;
+  L.mpos = L.mg + arr;
   return L;
 }
 
+// Largest metadata stride the ring can host after the stream (scores, Gumbel
+// values and positions: three arrays of capm floats).
+template <int D>
+__host__ __device__ constexpr int decode_max_capm() {
+  return (int)(((size_t)kStages * Geo<D>::TILEB / 3) / 128 * 128 / 4) - 4;
+}
+
+// fp16 chunk <-> float2 pairs
 template <int CH>
-__device__ __forceinline__ void unpack(const typename std::conditional<CH == 8, uint4, uint2>::type& c,
-                                       float* f) {
+__device__ __forceinline__ void unpack2(const typename std::conditional<CH == 8, uint4, uint2>::type& c,
+                                        float2* f) {
   const __half2* h = reinterpret_cast<const __half2*>(&c);
 #pragma unroll
-  for (int k = 0; k < CH / 2; ++k) {
-    const float2 v = __half22float2(h[k]);
-    f[2 * k] = v.x;
-    f[2 * k + 1] = v.y;
-  }
+  for (int k = 0; k < CH / 2; ++k) f[k] = __half22float2(h[k]);
 }
 
 template <int CH>
-__device__ __forceinline__ typename std::conditional<CH == 8, uint4, uint2>::type pack(const float* f) {
+__device__ __forceinline__ typename std::conditional<CH == 8, uint4, uint2>::type pack2(const float2* f) {
   typename std::conditional<CH == 8, uint4, uint2>::type c;
   __half2* h = reinterpret_cast<__half2*>(&c);
 #pragma unroll
-  for (int k = 0; k < CH / 2; ++k) h[k] = __halves2half2(__float2half_rn(f[2 * k]), __float2half_rn(f[2 * k + 1]));
+  for (int k = 0; k < CH / 2; ++k) h[k] = __float22half2_rn(f[k]);
   return c;
 }
 
-// Rotate the pair halves (a_i, b_i) by the shift-by-one constants: every product
-// and sum rounded to f32 (no contraction), then fp16 round-to-nearest-even.
+// Rotate pair halves (a, b) by the shift-by-one constants: x = a*c - b*s,
+// y = a*s + b*c, each product and each sum rounded to f32 on its own. Scalar
+// __fmul_rn/__fsub_rn/__fadd_rn on purpose: on sm_103a with CUDA 13.0 a packed
+// mul.rn.f32x2 + add.rn.f32x2 pair was measured to return the fused result
+// (an fp16 midpoint case came out one ULP off), which would break the op-by-op
+// fp32 rotation the stored keys must follow.
 template <int CH>
-__device__ __forceinline__ void rotate_pairs(float* a, float* b, const float* c, const float* s) {
+__device__ __forceinline__ void rotate2(float2* a, float2* b, const float2* c, const float2* s) {
 #pragma unroll
-  for (int k = 0; k < CH; ++k) {
-    const float x = __fsub_rn(__fmul_rn(a[k], c[k]), __fmul_rn(b[k], s[k]));
-    const float y = __fadd_rn(__fmul_rn(a[k], s[k]), __fmul_rn(b[k], c[k]));
-    a[k] = x;
-    b[k] = y;
+  for (int k = 0; k < CH / 2; ++k) {
+    const float x0 = __fsub_rn(__fmul_rn(a[k].x, c[k].x), __fmul_rn(b[k].x, s[k].x));
+    const float y0 = __fadd_rn(__fmul_rn(a[k].x, s[k].x), __fmul_rn(b[k].x, c[k].x));
+    const float x1 = __fsub_rn(__fmul_rn(a[k].y, c[k].y), __fmul_rn(b[k].y, s[k].y));
+    const float y1 = __fadd_rn(__fmul_rn(a[k].y, s[k].y), __fmul_rn(b[k].y, c[k].y));
+    a[k] = make_float2(x0, x1);
+    b[k] = make_float2(y0, y1);
   }
 }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
 __device__ __forceinline__ void warp_argmin(float& r, int& i) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -116,59 +120,87 @@ __device__ __forceinline__ void warp_argmin(float& r, int& i) {
   }
 }
 
-__device__ float block_max(float v, float* red) {
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  v = warp_max(v);
-  if (lane == 0) red[w] = v;
-  __syncthreads();
-  if (w == 0) {
-    v = lane < kThreads / 32 ? red[lane] : -INFINITY;
-    v = warp_max(v);
-    if (lane == 0) red[32] = v;
-  }
-  __syncthreads();
-  return red[32];
+// Combine two (max, sum of exp(x - max)) pairs.
+__device__ __forceinline__ void lse_combine(float& m, float& l, float m2, float l2) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) return;
+  l = (m == -INFINITY ? 0.f : l * expf(m - mn)) + (m2 == -INFINITY ? 0.f : l2 * expf(m2 - mn));
+  m = mn;
 }
 
-__device__ float block_sum(float v, float* red) {
+// Block-wide (max, sum) over the 256 consumer threads.
+__device__ void block_lse(float& m, float& l, float* red) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  v = warp_sum(v);
-  if (lane == 0) red[w] = v;
-  __syncthreads();
-  if (w == 0) {
-    v = lane < kThreads / 32 ? red[lane] : 0.f;
-    v = warp_sum(v);
-    if (lane == 0) red[33] = v;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+    lse_combine(m, l, m2, l2);
   }
-  __syncthreads();
-  return red[33];
+  if (lane == 0) { red[w] = m; red[16 + w] = l; }
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+  if (w == 0) {
+    m = lane < kConsumerWarps ? red[lane] : -INFINITY;
+    l = lane < kConsumerWarps ? red[16 + lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+      lse_combine(m, l, m2, l2);
+    }
+    if (lane == 0) { red[32] = m; red[33] = l; }
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+  m = red[32];
+  l = red[33];
 }
 
 __device__ int block_argmin(float r, int i, float* redf, int* redi) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   warp_argmin(r, i);
   if (lane == 0) { redf[40 + w] = r; redi[40 + w] = i; }
-  __syncthreads();
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
   if (w == 0) {
-    r = lane < kThreads / 32 ? redf[40 + lane] : INFINITY;
-    i = lane < kThreads / 32 ? redi[40 + lane] : INT_MAX;
+    r = lane < kConsumerWarps ? redf[40 + lane] : INFINITY;
+    i = lane < kConsumerWarps ? redi[40 + lane] : INT_MAX;
     warp_argmin(r, i);
     if (lane == 0) redi[63] = i;
   }
-  __syncthreads();
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
   return redi[63];
 }
 
+__device__ __forceinline__ void mbar_arrive_cta(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bounded wait that also gives up as soon as another thread raised the abort flag.
+__device__ __forceinline__ bool wait_watch(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicOr(err, kErrWaitTimeout);
+      return false;
+    }
+  }
+}
+
 template <int D>
-__global__ void __launch_bounds__(kThreads) decode_step_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeArgs a) {
   using G = Geo<D>;
   using Chunk = typename G::Chunk;
   constexpr int CH = G::CH, HALF = G::HALF;
 
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x;
-  const int c = tid & (kTPR - 1);   // chunk index within a row
-  const int rg = tid >> 3;          // row within a pass
+  const int warp = tid >> 5, lane = tid & 31;
+  const int c = tid & (kTPR - 1);   // chunk index within a row (consumers)
+  const int rg = tid >> 3;          // row within a pass (consumers)
 
   const int head = blockIdx.x;
   const int BH = a.B * a.H;
@@ -179,14 +211,18 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const DecodeArgs 
   const LayerInfo li = a.layers[l];
   const SmemLayout SL = decode_layout<D>(li.capm);
   unsigned char* ring = smem + SL.ring;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SL.bars);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SL.bars);   // full[kStages], empty[kStages], meta
   float* s_log = reinterpret_cast<float*>(smem + SL.slog);
-  float* s_sc = reinterpret_cast<float*>(smem + SL.ssc);
-  float* s_g = reinterpret_cast<float*>(smem + SL.sg);
+  float* s_sc = reinterpret_cast<float*>(smem + SL.msc);          // valid after the stream
+  float* s_g = reinterpret_cast<float*>(smem + SL.mg);
+  int32_t* s_pos = reinterpret_cast<int32_t*>(smem + SL.mpos);
   float* redf = reinterpret_cast<float*>(smem + SL.redf);
   int* redi = reinterpret_cast<int*>(smem + SL.redi);
   __shared__ float s_gnew;
   __shared__ int s_abort;
+  auto full = [&](int s) { return smem_addr(&bars[s]); };
+  auto empty = [&](int s) { return smem_addr(&bars[kStages + s]); };
+  const uint32_t meta_bar = smem_addr(&bars[2 * kStages]);
 
   const int n = (int)(a.p < (int64_t)li.budget ? a.p : (int64_t)li.budget);  // rows before append
   const int e_prev = a.pend[head];                                          // dead row or -1
@@ -195,6 +231,8 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const DecodeArgs 
   const int NR = nphys + 1;                                                 // + the new row
   const bool evict = (n + 1) > li.budget;
   const int ntiles = (nphys + kTile - 1) / kTile;
+  const int pos0 = (e_prev + 1) & ~3;          // 16-byte aligned start of the moving positions
+  const bool move_pos = shift && e_prev + 1 < nphys;
 
   __half* Kg = a.K + (li.row_base + (int64_t)rem * li.cap) * D;
   float* scg = a.score + li.meta_base + (int64_t)rem * li.capm;
@@ -203,149 +241,155 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const DecodeArgs 
   const __half* qg = a.k_new + (((int64_t)b * a.L + l) * a.H + hh) * D;
 
   if (tid == 0) {
-    for (int s = 0; s <= kStages; ++s) mbar_init(smem_addr(&bars[s]), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), kConsumerWarps);
+    }
+    mbar_init(meta_bar, 1);
     fence_mbar_init();
     s_abort = 0;
   }
   __syncthreads();
+  volatile int* abort_flag = &s_abort;
 
-  int issued = 0;  // tiles issued so far (thread 0 only)
-  if (tid == 0) {
-    if (nphys > 0) {
-      const uint32_t mbytes = (uint32_t)(((nphys + 3) & ~3) * 4);
-      mbar_expect_tx(smem_addr(&bars[kStages]), 2 * mbytes);
-      bulk_g2s(smem_addr(s_sc), scg, mbytes, smem_addr(&bars[kStages]));
-      bulk_g2s(smem_addr(s_g), gg, mbytes, smem_addr(&bars[kStages]));
-    }
-    for (; issued < ntiles && issued < kStages; ++issued) {
-      const int rows = min(kTile, nphys - issued * kTile);
-      const uint32_t bytes = (uint32_t)rows * G::ROWB;
-      const uint32_t bar = smem_addr(&bars[issued % kStages]);
-      mbar_expect_tx(bar, bytes);
-      bulk_g2s(smem_addr(ring + (size_t)(issued % kStages) * G::TILEB),
-               Kg + (size_t)issued * kTile * D, bytes, bar);
-    }
-  }
+  float run_m = -INFINITY, run_l = 0.f;   // this thread's share of the softmax statistics
+  Chunk q_lo{}, q_hi{};
+  float gnew = 0.f;
 
-  // The proxy query (the new key) and the shift-by-one RoPE constants this
-  // thread's pair indices need, kept in registers for the whole pass.
-  const Chunk q_lo = *reinterpret_cast<const Chunk*>(qg + c * CH);
-  const Chunk q_hi = *reinterpret_cast<const Chunk*>(qg + HALF + c * CH);
-  float qa[CH], qb[CH], rc[CH], rs[CH];
-  unpack<CH>(q_lo, qa);
-  unpack<CH>(q_hi, qb);
-#pragma unroll
-  for (int k = 0; k < CH; ++k) {
-    rc[k] = a.rope_c[c * CH + k];
-    rs[k] = a.rope_s[c * CH + k];
-  }
-  if (tid == 32) s_gnew = gumbel_at(a.seed, l, hh, a.p);
-  if (tid < 32) {  // logit of the new row against itself
-    float d = 0.f;
-#pragma unroll
-    for (int k = 0; k < CH; ++k) d = fmaf(qa[k], qa[k], fmaf(qb[k], qb[k], d));
-    d += __shfl_xor_sync(0xffffffffu, d, 1);
-    d += __shfl_xor_sync(0xffffffffu, d, 2);
-    d += __shfl_xor_sync(0xffffffffu, d, 4);
-    if (tid == 0) s_log[nphys] = d * a.scale;
-  }
-
-  // ---------------------------------------------------------------- stream K
-  bool abort = false;
-  int t = 0;
-  for (; t < ntiles; ++t) {
-    const int st = t % kStages;
-    const bool ok = mbar_wait_bounded(smem_addr(&bars[st]), (uint32_t)((t / kStages) & 1));
-    if (__syncthreads_or(!ok)) { abort = true; break; }
-    const unsigned char* tile = ring + (size_t)st * G::TILEB;
-    const int r0 = t * kTile;
-#pragma unroll
-    for (int pass = 0; pass < kTile / kRowsPerPass; ++pass) {
-      const int rr = pass * kRowsPerPass + rg;
-      const int R = r0 + rr;
-      const bool live = (R < nphys) && (R != e_prev);
-      float dot = 0.f;
-      if (live) {
-        const unsigned char* row = tile + (size_t)rr * G::ROWB;
-        Chunk lo = *reinterpret_cast<const Chunk*>(row + c * CH * 2);
-        Chunk hi = *reinterpret_cast<const Chunk*>(row + (HALF + c * CH) * 2);
-        float fa[CH], fb[CH];
-        unpack<CH>(lo, fa);
-        unpack<CH>(hi, fb);
-        if (shift && R > e_prev) {   // apply last step's compaction to this row
-          rotate_pairs<CH>(fa, fb, rc, rs);
-          lo = pack<CH>(fa);
-          hi = pack<CH>(fb);
-          unpack<CH>(lo, fa);         // the stored fp16 values are what gets scored
-          unpack<CH>(hi, fb);
-          __half* dst = Kg + (size_t)(R - 1) * D;
-          *reinterpret_cast<Chunk*>(dst + c * CH) = lo;
-          *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = hi;
-        }
-        float d0 = 0.f, d1 = 0.f;
-#pragma unroll
-        for (int k = 0; k < CH; ++k) {
-          d0 = fmaf(fa[k], qa[k], d0);
-          d1 = fmaf(fb[k], qb[k], d1);
-        }
-        dot = d0 + d1;
+  if (warp == kConsumerWarps) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int t = 0;
+      for (; t < ntiles; ++t) {
+        const int s = t % kStages;
+        if (t >= kStages && !wait_watch(empty(s), (uint32_t)((t / kStages - 1) & 1), abort_flag, a.err))
+          break;
+        const int rows = min(kTile, nphys - t * kTile);
+        const uint32_t bytes = (uint32_t)rows * G::ROWB;
+        mbar_expect_tx(full(s), bytes);
+        bulk_g2s(smem_addr(ring + (size_t)s * G::TILEB), Kg + (size_t)t * kTile * D, bytes, full(s));
       }
-      dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-      dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-      dot += __shfl_xor_sync(0xffffffffu, dot, 4);
-      if (live && c == 0) s_log[R] = dot * a.scale;
+      const int issued = t;
+      bool drained = true;   // every issued tile consumed, so the ring is free
+      for (int u = issued > kStages ? issued - kStages : 0; u < issued && drained; ++u)
+        drained = wait_watch(empty(u % kStages), (uint32_t)((u / kStages) & 1), abort_flag, a.err);
+      if (drained && !*abort_flag && nphys > 0) {
+        // metadata (scores, Gumbel values, moving positions) into the freed ring
+        const uint32_t mbytes = (uint32_t)(((nphys + 3) & ~3) * 4);
+        const uint32_t pbytes = move_pos ? (uint32_t)(((nphys - pos0 + 3) & ~3) * 4) : 0u;
+        mbar_expect_tx(meta_bar, 2 * mbytes + pbytes);
+        bulk_g2s(smem_addr(s_sc), scg, mbytes, meta_bar);
+        bulk_g2s(smem_addr(s_g), gg, mbytes, meta_bar);
+        if (pbytes) bulk_g2s(smem_addr(s_pos), pg + pos0, pbytes, meta_bar);
+      } else if (!drained) {
+        // give copies still in flight a moment to land before the CTA leaves
+        for (int u = issued > kStages ? issued - kStages : 0; u < issued; ++u)
+          (void)mbar_wait_bounded(full(u % kStages), (uint32_t)((u / kStages) & 1), 10000000ull);
+      }
     }
-    __syncthreads();  // every thread is done with stage st
-    if (tid == 0 && issued < ntiles) {
-      const int rows = min(kTile, nphys - issued * kTile);
-      const uint32_t bytes = (uint32_t)rows * G::ROWB;
-      const uint32_t bar = smem_addr(&bars[issued % kStages]);
-      mbar_expect_tx(bar, bytes);
-      bulk_g2s(smem_addr(ring + (size_t)(issued % kStages) * G::TILEB),
-               Kg + (size_t)issued * kTile * D, bytes, bar);
-      ++issued;
+  } else {
+    // ---------------------------------------------------------- consumers
+    // The proxy query (the new key) and the shift-by-one RoPE constants of this
+    // thread's pair indices stay in registers for the whole pass.
+    q_lo = *reinterpret_cast<const Chunk*>(qg + c * CH);
+    q_hi = *reinterpret_cast<const Chunk*>(qg + HALF + c * CH);
+    float2 qa[CH / 2], qb[CH / 2], rc[CH / 2], rs[CH / 2];
+    unpack2<CH>(q_lo, qa);
+    unpack2<CH>(q_hi, qb);
+#pragma unroll
+    for (int k = 0; k < CH / 2; ++k) {
+      rc[k] = make_float2(a.rope_c[c * CH + 2 * k], a.rope_c[c * CH + 2 * k + 1]);
+      rs[k] = make_float2(a.rope_s[c * CH + 2 * k], a.rope_s[c * CH + 2 * k + 1]);
+    }
+    if (tid == 32) s_gnew = gumbel_at(a.seed, l, hh, a.p);
+    if (tid < 32) {  // logit of the new row against itself
+      float2 d2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < CH / 2; ++k) d2 = __ffma2_rn(qa[k], qa[k], __ffma2_rn(qb[k], qb[k], d2));
+      float d = d2.x + d2.y;
+      d += __shfl_xor_sync(0xffffffffu, d, 1);
+      d += __shfl_xor_sync(0xffffffffu, d, 2);
+      d += __shfl_xor_sync(0xffffffffu, d, 4);
+      if (tid == 0) {
+        s_log[nphys] = d * a.scale;
+        run_m = d * a.scale;
+        run_l = 1.f;
+      }
+    }
+    for (int t = 0; t < ntiles; ++t) {
+      const int st = t % kStages;
+      if (!wait_watch(full(st), (uint32_t)((t / kStages) & 1), abort_flag, a.err)) break;
+      const unsigned char* tile = ring + (size_t)st * G::TILEB;
+      const int r0 = t * kTile;
+#pragma unroll
+      for (int pass = 0; pass < kTile / kRowsPerPass; ++pass) {
+        const int rr = pass * kRowsPerPass + rg;
+        const int R = r0 + rr;
+        const bool live = (R < nphys) && (R != e_prev);
+        float dot = 0.f;
+        if (live) {
+          const unsigned char* row = tile + (size_t)rr * G::ROWB;
+          Chunk lo = *reinterpret_cast<const Chunk*>(row + c * CH * 2);
+          Chunk hi = *reinterpret_cast<const Chunk*>(row + (HALF + c * CH) * 2);
+          float2 fa[CH / 2], fb[CH / 2];
+          unpack2<CH>(lo, fa);
+          unpack2<CH>(hi, fb);
+          if (shift && R > e_prev) {   // apply last step's compaction to this row
+            rotate2<CH>(fa, fb, rc, rs);
+            lo = pack2<CH>(fa);
+            hi = pack2<CH>(fb);
+            unpack2<CH>(lo, fa);        // the stored fp16 values are what gets scored
+            unpack2<CH>(hi, fb);
+            __half* dst = Kg + (size_t)(R - 1) * D;
+            *reinterpret_cast<Chunk*>(dst + c * CH) = lo;
+            *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = hi;
+          }
+          float2 d2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int k = 0; k < CH / 2; ++k) d2 = __ffma2_rn(fa[k], qa[k], __ffma2_rn(fb[k], qb[k], d2));
+          dot = d2.x + d2.y;
+        }
+        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+        if (live && c == 0) {
+          const float sv = dot * a.scale;
+          s_log[R] = sv;
+          if (sv > run_m) {
+            run_l = run_l * expf(run_m - sv) + 1.f;
+            run_m = sv;
+          } else {
+            run_l += expf(sv - run_m);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(empty(st));
     }
   }
-  if (!abort && nphys > 0) {
-    const bool ok = mbar_wait_bounded(smem_addr(&bars[kStages]), 0);
-    if (__syncthreads_or(!ok)) abort = true;
-  }
-  if (abort) {
-    // Record the failure, then wait (briefly, bounded) for copies still in flight.
-    if (tid == 0) {
-      atomicOr(a.err, kErrWaitTimeout);
-      for (int u = t; u < issued; ++u)
-        (void)mbar_wait_bounded(smem_addr(&bars[u % kStages]), (uint32_t)((u / kStages) & 1),
-                                10000000ull);
-      if (nphys > 0) (void)mbar_wait_bounded(smem_addr(&bars[kStages]), 0, 10000000ull);
-    }
-    __syncthreads();
+
+  // every consumer is done with the stream (and s_log); wait for the metadata
+  if (__syncthreads_or(*abort_flag)) return;
+  if (nphys > 0 && warp < kConsumerWarps &&
+      !wait_watch(meta_bar, 0, abort_flag, a.err)) { /* abort flagged */ }
+  if (__syncthreads_or(*abort_flag)) {
+    if (tid == kConsumers) (void)mbar_wait_bounded(meta_bar, 0, 10000000ull);
     return;
   }
-  __syncthreads();
+  if (warp == kConsumerWarps) return;   // the producer warp is done
 
   // ---------------------------------------------------------------- softmax
-  float m = -INFINITY;
-  for (int R = tid; R < NR; R += kThreads)
-    if (R != e_prev) m = fmaxf(m, s_log[R]);
-  m = block_max(m, redf);
-  float lsum = 0.f;
-  for (int R = tid; R < NR; R += kThreads)
-    if (R != e_prev) {
-      const float ex = expf(s_log[R] - m);
-      s_log[R] = ex;
-      lsum += ex;
-    }
-  lsum = block_sum(lsum, redf);
+  block_lse(run_m, run_l, redf);
+  const float m = run_m, lsum = run_l;
 
   // ------------------------------------------------- accumulate + select
-  const float gnew = s_gnew;
+  gnew = s_gnew;
   float best_r = INFINITY;
   int best_R = INT_MAX;
-  for (int R = tid; R < NR; R += kThreads) {
+  for (int R = tid; R < NR; R += kConsumers) {
     if (R == e_prev) continue;
     const float old = R < nphys ? s_sc[R] : 0.f;
-    const float ns = old + s_log[R] / lsum;
+    const float ns = old + expf(s_log[R] - m) / lsum;
     s_log[R] = ns;
     if (evict && R >= a.n_sink) {
       const float gv = R < nphys ? s_g[R] : gnew;
@@ -357,15 +401,12 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const DecodeArgs 
   if (evict) R_e = block_argmin(best_r, best_R, redf, redi);
 
   // ---------------------------------------------------------------- write back
-  for (int R = tid; R < NR; R += kThreads)
+  for (int R = tid; R < NR; R += kConsumers)
     if (R != e_prev) scg[R - ((shift && R > e_prev) ? 1 : 0)] = s_log[R];
-  if (shift) {
-    for (int R = e_prev + 1 + tid; R < nphys; R += kThreads) gg[R - 1] = s_g[R];
-    for (int base = e_prev + 1; base < nphys; base += kThreads) {
-      const int R = base + tid;
-      const int v = R < nphys ? pg[R] : 0;
-      __syncthreads();
-      if (R < nphys) pg[R - 1] = v;
+  if (move_pos) {
+    for (int R = e_prev + 1 + tid; R < nphys; R += kConsumers) {
+      gg[R - 1] = s_g[R];
+      pg[R - 1] = s_pos[R - pos0];
     }
   }
   if (R_e != nphys && tid < kTPR) {   // the new key, unless it was evicted itself
@@ -387,7 +428,7 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const DecodeArgs 
 // keys re-rotated by -1 position. Read a chunk of rows into registers, barrier,
 // write them one slot lower; chunks ascend so no row is overwritten unread.
 template <int D>
-__global__ void __launch_bounds__(kThreads) flush_kernel(const FlushArgs a) {
+__global__ void __launch_bounds__(kConsumers) flush_kernel(const FlushArgs a) {
   using G = Geo<D>;
   using Chunk = typename G::Chunk;
   constexpr int CH = G::CH, HALF = G::HALF;
@@ -405,11 +446,11 @@ __global__ void __launch_bounds__(kThreads) flush_kernel(const FlushArgs a) {
   float* scg = a.score + li.meta_base + (int64_t)rem * li.capm;
   float* gg = a.gum + li.meta_base + (int64_t)rem * li.capm;
   int32_t* pg = a.pos + li.meta_base + (int64_t)rem * li.capm;
-  float rc[CH], rs[CH];
+  float2 rc[CH / 2], rs[CH / 2];
 #pragma unroll
-  for (int k = 0; k < CH; ++k) {
-    rc[k] = a.rope_c[c * CH + k];
-    rs[k] = a.rope_s[c * CH + k];
+  for (int k = 0; k < CH / 2; ++k) {
+    rc[k] = make_float2(a.rope_c[c * CH + 2 * k], a.rope_c[c * CH + 2 * k + 1]);
+    rs[k] = make_float2(a.rope_s[c * CH + 2 * k], a.rope_s[c * CH + 2 * k + 1]);
   }
   for (int base = e + 1; base < nphys; base += kRowsPerPass) {
     const int R = base + rg;
@@ -424,13 +465,13 @@ __global__ void __launch_bounds__(kThreads) flush_kernel(const FlushArgs a) {
     }
     __syncthreads();
     if (live) {
-      float fa[CH], fb[CH];
-      unpack<CH>(lo, fa);
-      unpack<CH>(hi, fb);
-      rotate_pairs<CH>(fa, fb, rc, rs);
+      float2 fa[CH / 2], fb[CH / 2];
+      unpack2<CH>(lo, fa);
+      unpack2<CH>(hi, fb);
+      rotate2<CH>(fa, fb, rc, rs);
       __half* dst = Kg + (size_t)(R - 1) * D;
-      *reinterpret_cast<Chunk*>(dst + c * CH) = pack<CH>(fa);
-      *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = pack<CH>(fb);
+      *reinterpret_cast<Chunk*>(dst + c * CH) = pack2<CH>(fa);
+      *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = pack2<CH>(fb);
       if (c == 0) { scg[R - 1] = sv; gg[R - 1] = gv; pg[R - 1] = pv; }
     }
     __syncthreads();
@@ -441,6 +482,8 @@ __global__ void __launch_bounds__(kThreads) flush_kernel(const FlushArgs a) {
 }  // namespace
 
 size_t decode_step_smem(int D, int capm_max) {
+  const int lim = D == 64 ? decode_max_capm<64>() : decode_max_capm<128>();
+  if (capm_max > lim) return (size_t)-1;   // the ring cannot host this row's metadata
   return D == 64 ? decode_layout<64>(capm_max).total : decode_layout<128>(capm_max).total;
 }
 
@@ -462,9 +505,9 @@ cudaError_t launch_decode_step(const DecodeArgs& a, int D, int heads, size_t sme
 cudaError_t launch_flush(const FlushArgs& a, int D, int heads, cudaStream_t s) {
   if (heads <= 0) return cudaSuccess;
   if (D == 64)
-    flush_kernel<64><<<heads, kThreads, 0, s>>>(a);
+    flush_kernel<64><<<heads, kConsumers, 0, s>>>(a);
   else
-    flush_kernel<128><<<heads, kThreads, 0, s>>>(a);
+    flush_kernel<128><<<heads, kConsumers, 0, s>>>(a);
   return cudaGetLastError();
 }
 
