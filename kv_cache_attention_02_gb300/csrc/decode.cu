@@ -111,6 +111,34 @@ __device__ __forceinline__ void rotate2(float2* a, float2* b, const float2* c, c
   }
 }
 
+// fp32 accumulation of fp16 x fp16 products with the mixed-precision FMA
+// (the product of two fp16 values is exact in f32, so this equals converting
+// both operands and using an f32 FMA). Two independent chains, one per chunk.
+__device__ __forceinline__ float fma_f16(__half a, __half b, float c) {
+  float d;
+  asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(__half_as_ushort(a)), "h"(__half_as_ushort(b)), "f"(c));
+  return d;
+}
+template <int CH>
+__device__ __forceinline__ float dot_chunks(const typename std::conditional<CH == 8, uint4, uint2>::type& klo,
+                                            const typename std::conditional<CH == 8, uint4, uint2>::type& khi,
+                                            const typename std::conditional<CH == 8, uint4, uint2>::type& qlo,
+                                            const typename std::conditional<CH == 8, uint4, uint2>::type& qhi) {
+  const __half2* a = reinterpret_cast<const __half2*>(&klo);
+  const __half2* b = reinterpret_cast<const __half2*>(&khi);
+  const __half2* qa = reinterpret_cast<const __half2*>(&qlo);
+  const __half2* qb = reinterpret_cast<const __half2*>(&qhi);
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int k = 0; k < CH / 2; ++k) {
+    s0 = fma_f16(__low2half(a[k]), __low2half(qa[k]), s0);
+    s1 = fma_f16(__low2half(b[k]), __low2half(qb[k]), s1);
+    s0 = fma_f16(__high2half(a[k]), __high2half(qa[k]), s0);
+    s1 = fma_f16(__high2half(b[k]), __high2half(qb[k]), s1);
+  }
+  return s0 + s1;
+}
+
 __device__ __forceinline__ void warp_argmin(float& r, int& i) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -293,9 +321,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
     // thread's pair indices stay in registers for the whole pass.
     q_lo = *reinterpret_cast<const Chunk*>(qg + c * CH);
     q_hi = *reinterpret_cast<const Chunk*>(qg + HALF + c * CH);
-    float2 qa[CH / 2], qb[CH / 2], rc[CH / 2], rs[CH / 2];
-    unpack2<CH>(q_lo, qa);
-    unpack2<CH>(q_hi, qb);
+    float2 rc[CH / 2], rs[CH / 2];
 #pragma unroll
     for (int k = 0; k < CH / 2; ++k) {
       rc[k] = make_float2(a.rope_c[c * CH + 2 * k], a.rope_c[c * CH + 2 * k + 1]);
@@ -303,10 +329,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
     }
     if (tid == 32) s_gnew = gumbel_at(a.seed, l, hh, a.p);
     if (tid < 32) {  // logit of the new row against itself
-      float2 d2 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int k = 0; k < CH / 2; ++k) d2 = __ffma2_rn(qa[k], qa[k], __ffma2_rn(qb[k], qb[k], d2));
-      float d = d2.x + d2.y;
+      float d = dot_chunks<CH>(q_lo, q_hi, q_lo, q_hi);
       d += __shfl_xor_sync(0xffffffffu, d, 1);
       d += __shfl_xor_sync(0xffffffffu, d, 2);
       d += __shfl_xor_sync(0xffffffffu, d, 4);
@@ -321,40 +344,44 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
       if (!wait_watch(full(st), (uint32_t)((t / kStages) & 1), abort_flag, a.err)) break;
       const unsigned char* tile = ring + (size_t)st * G::TILEB;
       const int r0 = t * kTile;
+      constexpr int P = kTile / kRowsPerPass;   // rows per thread in this tile
+      Chunk lo[P], hi[P];
+      bool live[P];
+      int Rr[P];
 #pragma unroll
-      for (int pass = 0; pass < kTile / kRowsPerPass; ++pass) {
+      for (int pass = 0; pass < P; ++pass) {     // both rows' loads first
         const int rr = pass * kRowsPerPass + rg;
-        const int R = r0 + rr;
-        const bool live = (R < nphys) && (R != e_prev);
-        float dot = 0.f;
-        if (live) {
-          const unsigned char* row = tile + (size_t)rr * G::ROWB;
-          Chunk lo = *reinterpret_cast<const Chunk*>(row + c * CH * 2);
-          Chunk hi = *reinterpret_cast<const Chunk*>(row + (HALF + c * CH) * 2);
-          float2 fa[CH / 2], fb[CH / 2];
-          unpack2<CH>(lo, fa);
-          unpack2<CH>(hi, fb);
-          if (shift && R > e_prev) {   // apply last step's compaction to this row
-            rotate2<CH>(fa, fb, rc, rs);
-            lo = pack2<CH>(fa);
-            hi = pack2<CH>(fb);
-            unpack2<CH>(lo, fa);        // the stored fp16 values are what gets scored
-            unpack2<CH>(hi, fb);
-            __half* dst = Kg + (size_t)(R - 1) * D;
-            *reinterpret_cast<Chunk*>(dst + c * CH) = lo;
-            *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = hi;
-          }
-          float2 d2 = make_float2(0.f, 0.f);
+        Rr[pass] = r0 + rr;
+        live[pass] = (Rr[pass] < nphys) && (Rr[pass] != e_prev);
+        const unsigned char* row = tile + (size_t)rr * G::ROWB;
+        lo[pass] = *reinterpret_cast<const Chunk*>(row + c * CH * 2);
+        hi[pass] = *reinterpret_cast<const Chunk*>(row + (HALF + c * CH) * 2);
+      }
+      float dot[P];
 #pragma unroll
-          for (int k = 0; k < CH / 2; ++k) d2 = __ffma2_rn(fa[k], qa[k], __ffma2_rn(fb[k], qb[k], d2));
-          dot = d2.x + d2.y;
+      for (int pass = 0; pass < P; ++pass) {
+        if (live[pass] && shift && Rr[pass] > e_prev) {   // apply last step's compaction
+          float2 fa[CH / 2], fb[CH / 2];
+          unpack2<CH>(lo[pass], fa);
+          unpack2<CH>(hi[pass], fb);
+          rotate2<CH>(fa, fb, rc, rs);
+          lo[pass] = pack2<CH>(fa);                      // the stored fp16 values are scored
+          hi[pass] = pack2<CH>(fb);
+          __half* dst = Kg + (size_t)(Rr[pass] - 1) * D;
+          *reinterpret_cast<Chunk*>(dst + c * CH) = lo[pass];
+          *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = hi[pass];
         }
-        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-        dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-        dot += __shfl_xor_sync(0xffffffffu, dot, 4);
-        if (live && c == 0) {
-          const float sv = dot * a.scale;
-          s_log[R] = sv;
+        dot[pass] = live[pass] ? dot_chunks<CH>(lo[pass], hi[pass], q_lo, q_hi) : 0.f;
+      }
+#pragma unroll
+      for (int o = 1; o < kTPR; o <<= 1)
+#pragma unroll
+        for (int pass = 0; pass < P; ++pass) dot[pass] += __shfl_xor_sync(0xffffffffu, dot[pass], o);
+#pragma unroll
+      for (int pass = 0; pass < P; ++pass) {
+        if (live[pass] && c == 0) {
+          const float sv = dot[pass] * a.scale;
+          s_log[Rr[pass]] = sv;
           if (sv > run_m) {
             run_l = run_l * expf(run_m - sv) + 1.f;
             run_m = sv;
