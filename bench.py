@@ -104,7 +104,8 @@ def oracle_pass(wl, rows, threads=0):
     prms = [oracle.HeadParams(D=wl.head_dim, budget=budgets[l], n_sink=wl.n_sink, layer=l, head=h,
                               tau_init=wl.tau_init, tau_end=wl.tau_end,
                               anneal_steps=wl.anneal_steps, theta=wl.rope_theta,
-                              seed=wl.gumbel_seed) for (b, l, h) in rows]
+                              seed=wl.gumbel_seed, recent=wl.recent, mode=wl.score_mode)
+            for (b, l, h) in rows]
     keys = [wl.head_keys(b, l, h, 0, wl.positions) for (b, l, h) in rows]
     pk = np.stack([k[: wl.prefill] for k in keys]) if wl.prefill else None
     dk = np.stack([k[wl.prefill:] for k in keys])

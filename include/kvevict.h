@@ -13,7 +13,8 @@
  *   2. attn = softmax(K k / sqrt(D)) over every stored row, the new one
  *      included; scores += attn;
  *   3. if the layer's budget is exceeded, evict the lowest
- *      score + tau(p) * g over rows j >= n_sink (lowest slot on ties); the
+ *      score + tau(p) * g over rows n_sink <= j < n+1-recent (lowest slot on
+ *      ties); the
  *      rows after it move down one slot in order, each key re-rotated by -1
  *      RoPE position in fp32 and stored as fp16.
  *
@@ -67,7 +68,17 @@ typedef struct kvevict_config {
   double rope_theta;      /* RoPE base of the model's attention, > 0 */
   uint64_t seed;          /* base seed of the frozen Gumbel values */
   int32_t max_prefill;    /* longest prompt kvevict_prefill will take, 0 .. KVEVICT_MAX_PREFILL */
+  int32_t recent;         /* trailing protected window, >= 0; 0 = off (keyformer page,
+                             KeyformerState.recent); every budget >= n_sink + recent + 1 */
+  int32_t score_mode;     /* KVEVICT_SCORE_CUMULATIVE (H2O rule) or KVEVICT_SCORE_CURRENT */
 } kvevict_config;
+
+/* Score modes (page "PyramidKV ...", method table): cumulative attention mass
+ * (H2O-adapted, Keyformer-adapted, PyramidKV-adapted) or the current step's
+ * attention weight (TOVA-adapted; a prompt then scores each token by the
+ * prompt's last token's attention). */
+#define KVEVICT_SCORE_CUMULATIVE 0
+#define KVEVICT_SCORE_CURRENT 1
 
 typedef struct kvevict kvevict_t;
 

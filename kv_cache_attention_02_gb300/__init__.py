@@ -20,6 +20,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvevict.so")
 
 OK, ERR_INVALID_ARG, ERR_BAD_STATE, ERR_CUDA, ERR_OOM, ERR_DEVICE_CHECK = 0, -1, -2, -3, -4, -5
+SCORE_CUMULATIVE, SCORE_CURRENT = 0, 1
 MAX_LAYERS = 256
 MAX_PREFILL = 16384
 
@@ -32,7 +33,7 @@ class Config(ctypes.Structure):
     _fields_ = [("batch", i32), ("n_layers", i32), ("n_kv_heads", i32), ("head_dim", i32),
                 ("avg_budget", i32), ("pyramid_beta", f64), ("layer_budgets", P), ("n_sink", i32),
                 ("tau_init", f32), ("tau_end", f32), ("anneal_steps", i32), ("rope_theta", f64),
-                ("seed", u64), ("max_prefill", i32)]
+                ("seed", u64), ("max_prefill", i32), ("recent", i32), ("score_mode", i32)]
 
 
 class KVEvictError(RuntimeError):
@@ -132,14 +133,15 @@ class KVEvict:
                  avg_budget: int = 512, pyramid_beta: float = 1.0, layer_budgets=None,
                  n_sink: int = 4, tau_init: float = 0.0, tau_end: float = 0.0,
                  anneal_steps: int = 0, rope_theta: float = 10000.0, seed: int = 0,
-                 max_prefill: int = 0, stream=None):
+                 max_prefill: int = 0, recent: int = 0, score_mode: int = SCORE_CUMULATIVE,
+                 stream=None):
         self._lb = None
         if layer_budgets is not None:
             self._lb = (i32 * n_layers)(*layer_budgets)
         self.cfg = Config(batch, n_layers, n_kv_heads, head_dim, avg_budget, pyramid_beta,
                           ctypes.addressof(self._lb) if self._lb is not None else None, n_sink,
                           tau_init, tau_end, anneal_steps, rope_theta, seed & (2 ** 64 - 1),
-                          max_prefill)
+                          max_prefill, recent, score_mode)
         self._h = P()
         _check(lib().kvevict_create(ctypes.addressof(self.cfg), _stream(stream),
                                     ctypes.addressof(self._h)))
@@ -234,4 +236,5 @@ def from_workload(wl, stream=None) -> KVEvict:
                    head_dim=wl.head_dim, avg_budget=wl.avg_budget, pyramid_beta=wl.beta,
                    n_sink=wl.n_sink, tau_init=wl.tau_init, tau_end=wl.tau_end,
                    anneal_steps=wl.anneal_steps, rope_theta=wl.rope_theta, seed=wl.gumbel_seed,
-                   max_prefill=wl.prefill, stream=stream)
+                   max_prefill=wl.prefill, recent=getattr(wl, "recent", 0),
+                   score_mode=getattr(wl, "score_mode", SCORE_CUMULATIVE), stream=stream)

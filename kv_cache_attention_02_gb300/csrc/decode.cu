@@ -415,10 +415,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
   int best_R = INT_MAX;
   for (int R = tid; R < NR; R += kConsumers) {
     if (R == e_prev) continue;
-    const float old = R < nphys ? s_sc[R] : 0.f;
-    const float ns = old + expf(s_log[R] - m) / lsum;
+    const float attn = expf(s_log[R] - m) / lsum;
+    const float ns = a.mode ? attn : (R < nphys ? s_sc[R] : 0.f) + attn;   // current-step or cumulative
     s_log[R] = ns;
-    if (evict && R >= a.n_sink) {
+    const int j = R - ((shift && R > e_prev) ? 1 : 0);                    // slot after the append
+    if (evict && R >= a.n_sink && j < n + 1 - a.recent) {
       const float gv = R < nphys ? s_g[R] : gnew;
       const float r = fmaf(a.tau, gv, ns);
       if (r < best_r) { best_r = r; best_R = R; }
@@ -447,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
     const int e_log = evict ? R_e - ((shift && R_e > e_prev) ? 1 : 0) : -1;
     a.pend[head] = e_log;
     if (a.evicted) a.evicted[((int64_t)b * a.L + l) * a.H + hh] = e_log;
-    if (evict && (R_e < a.n_sink || R_e > nphys)) atomicOr(a.err, kErrBadIndex);
+    if (evict && (R_e < a.n_sink || R_e > nphys || e_log >= n + 1 - a.recent)) atomicOr(a.err, kErrBadIndex);
   }
 }
 

@@ -50,6 +50,8 @@ struct DecodeArgs {
   const float* rope_s;     // [D/2] sin(-w_i)
   int* err;
   int B, L, H, n_sink;
+  int recent;              // trailing protected window
+  int mode;                // 0 cumulative scores, 1 current-step scores
   int64_t p;               // absolute position of the incoming key
   float tau;               // tau(p)
   float scale;             // 1/sqrt(D)
@@ -94,6 +96,7 @@ struct PrefillSelectArgs {
   const float* rope_s;
   int* err;
   int B, L, H, n_sink;
+  int recent;              // trailing protected window
   int b0;                  // first batch index of this launch
   int S;
   int Sp;                  // scratch row stride
@@ -108,6 +111,8 @@ cudaError_t launch_decode_step(const DecodeArgs& a, int D, int heads, size_t sme
 cudaError_t launch_flush(const FlushArgs& a, int D, int heads, cudaStream_t s);
 
 cudaError_t prefill_setup(int D, int max_prefill);  // bulk-eviction kernel's shared memory
+// current-step (TOVA) prompt scores: softmax of the last prompt key against every prompt key
+cudaError_t launch_prefill_lastrow(const PrefillScoreArgs& a, int D, cudaStream_t s);
 // tcgen05/TMEM scorer (prefill_tc.cu): a.Sp must be S rounded up to kPrefillRowPad
 constexpr int kPrefillRowPad = 128;
 size_t prefill_tc_smem(int D);

@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(kSThreads) prefill_select_kernel(const Prefill
     return;
   }
 
-  const int m = S - a.n_sink;       // evictable rows
+  const int m = S - a.n_sink - a.recent;   // evictable rows: not a sink, not in the recent window
   int P2 = 1;
   while (P2 < m) P2 <<= 1;
   uint64_t* keys = reinterpret_cast<uint64_t*>(smem);
@@ -168,6 +168,67 @@ __global__ void __launch_bounds__(kSThreads) prefill_select_kernel(const Prefill
   if (tid == 0) a.pend[slot] = -1;
 }
 
+// Current-step (TOVA-adapted) prompt scores: the prompt's last key attends
+// over every prompt key; score_j = softmax_j(K_j . k_{S-1} / sqrt(D)). One CTA
+// per cache row, 8 threads per key row, fp16 products accumulated in f32.
+template <int D>
+__global__ void __launch_bounds__(256) prefill_lastrow_kernel(const PrefillScoreArgs a) {
+  constexpr int CH = D / 16, HALF = D / 2;
+  using Chunk = typename std::conditional<CH == 8, uint4, uint2>::type;
+  extern __shared__ __align__(128) unsigned char smem[];
+  float* lg = reinterpret_cast<float*>(smem);          // [S] base-2 logits
+  __shared__ float red[64];
+  const int tid = threadIdx.x, c = tid & 7, rg = tid >> 3, lane = tid & 31, w = tid >> 5;
+  const int S = a.S;
+  const __half* Kh = a.keys + (size_t)blockIdx.x * S * D;
+  const __half* q = Kh + (size_t)(S - 1) * D;
+  const Chunk qlo = *reinterpret_cast<const Chunk*>(q + c * CH);
+  const Chunk qhi = *reinterpret_cast<const Chunk*>(q + HALF + c * CH);
+  const __half2* qa = reinterpret_cast<const __half2*>(&qlo);
+  const __half2* qb = reinterpret_cast<const __half2*>(&qhi);
+  float mx = -INFINITY;
+  for (int j0 = 0; j0 < S; j0 += 32) {
+    const int j = j0 + rg;
+    float dot = 0.f;
+    if (j < S) {
+      const Chunk klo = *reinterpret_cast<const Chunk*>(Kh + (size_t)j * D + c * CH);
+      const Chunk khi = *reinterpret_cast<const Chunk*>(Kh + (size_t)j * D + HALF + c * CH);
+      const __half2* ka = reinterpret_cast<const __half2*>(&klo);
+      const __half2* kb = reinterpret_cast<const __half2*>(&khi);
+#pragma unroll
+      for (int k = 0; k < CH / 2; ++k) {
+        const float2 x = __half22float2(ka[k]), y = __half22float2(kb[k]);
+        const float2 u = __half22float2(qa[k]), v = __half22float2(qb[k]);
+        dot = fmaf(x.x, u.x, fmaf(x.y, u.y, fmaf(y.x, v.x, fmaf(y.y, v.y, dot))));
+      }
+    }
+    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+    if (j < S && c == 0) {
+      lg[j] = dot * a.scale2;
+      mx = fmaxf(mx, lg[j]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) red[w] = mx;
+  __syncthreads();
+  mx = -INFINITY;
+  for (int i = 0; i < 8; ++i) mx = fmaxf(mx, red[i]);
+  float sum = 0.f;
+  for (int j = tid; j < S; j += 256) sum += exp2f(lg[j] - mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  __syncthreads();
+  if (lane == 0) red[w] = sum;
+  __syncthreads();
+  sum = 0.f;
+  for (int i = 0; i < 8; ++i) sum += red[i];
+  float* out = a.colsum + (size_t)blockIdx.x * a.Sp;
+  for (int j = tid; j < S; j += 256) out[j] = exp2f(lg[j] - mx) / sum;
+}
+
 }  // namespace
 
 size_t prefill_select_smem(int S) {
@@ -178,9 +239,27 @@ size_t prefill_select_smem(int S) {
 
 cudaError_t prefill_setup(int D, int max_prefill) {
   const int select = (int)prefill_select_smem(max_prefill > 0 ? max_prefill : 1);
+  const int last = (max_prefill > 0 ? max_prefill : 1) * (int)sizeof(float);
   const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  if (D == 64) return cudaFuncSetAttribute(prefill_select_kernel<64>, attr, select);
-  return cudaFuncSetAttribute(prefill_select_kernel<128>, attr, select);
+  cudaError_t e;
+  if (D == 64) {
+    e = cudaFuncSetAttribute(prefill_select_kernel<64>, attr, select);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(prefill_lastrow_kernel<64>, attr, last);
+  } else {
+    e = cudaFuncSetAttribute(prefill_select_kernel<128>, attr, select);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(prefill_lastrow_kernel<128>, attr, last);
+  }
+  return e;
+}
+
+cudaError_t launch_prefill_lastrow(const PrefillScoreArgs& a, int D, cudaStream_t s) {
+  if (a.S <= 0 || a.heads <= 0) return cudaSuccess;
+  const size_t smem = (size_t)a.S * sizeof(float);
+  if (D == 64)
+    prefill_lastrow_kernel<64><<<a.heads, 256, smem, s>>>(a);
+  else
+    prefill_lastrow_kernel<128><<<a.heads, 256, smem, s>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_select(const PrefillSelectArgs& a, int D, int heads, cudaStream_t s) {

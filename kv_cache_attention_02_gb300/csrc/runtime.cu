@@ -139,6 +139,8 @@ kvx::DecodeArgs decode_args(kvevict* h, const uint16_t* k_new, int32_t* evicted,
   a.L = h->L;
   a.H = h->H;
   a.n_sink = h->cfg.n_sink;
+  a.recent = h->cfg.recent;
+  a.mode = h->cfg.score_mode;
   a.p = p;
   a.tau = (float)tau_at(h->cfg, p);
   a.scale = (float)(1.0 / std::sqrt((double)h->D));
@@ -167,7 +169,10 @@ int enqueue_prefill(kvevict* h, const uint16_t* keys, int32_t S, int b0, int nb,
   sa.heads = heads;
   sa.scale2 = (float)(1.4426950408889634 / std::sqrt((double)h->D));
   sa.err = h->err;
-  KV_CUDA(kvx::launch_prefill_tc(sa, h->D, s));
+  if (h->cfg.score_mode == KVEVICT_SCORE_CURRENT)
+    KV_CUDA(kvx::launch_prefill_lastrow(sa, h->D, s));
+  else
+    KV_CUDA(kvx::launch_prefill_tc(sa, h->D, s));
   kvx::PrefillSelectArgs pa{};
   pa.keys = sa.keys;
   pa.colsum = colsum;
@@ -185,6 +190,7 @@ int enqueue_prefill(kvevict* h, const uint16_t* keys, int32_t S, int b0, int nb,
   pa.L = h->L;
   pa.H = h->H;
   pa.n_sink = h->cfg.n_sink;
+  pa.recent = h->cfg.recent;
   pa.b0 = b0;
   pa.S = S;
   pa.Sp = Sp;
@@ -274,6 +280,9 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
   if (!(c.rope_theta > 0.0)) return fail(KVEVICT_ERR_INVALID_ARG, "rope_theta must be > 0");
   if (c.max_prefill < 0 || c.max_prefill > KVEVICT_MAX_PREFILL)
     return fail(KVEVICT_ERR_INVALID_ARG, "max_prefill must be in [0, KVEVICT_MAX_PREFILL]");
+  if (c.recent < 0) return fail(KVEVICT_ERR_INVALID_ARG, "recent must be >= 0");
+  if (c.score_mode != KVEVICT_SCORE_CUMULATIVE && c.score_mode != KVEVICT_SCORE_CURRENT)
+    return fail(KVEVICT_ERR_INVALID_ARG, "score_mode must be KVEVICT_SCORE_CUMULATIVE or KVEVICT_SCORE_CURRENT");
 
   std::vector<int32_t> budgets(c.n_layers);
   if (c.layer_budgets) {
@@ -283,8 +292,9 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
     if (rc != KVEVICT_OK) return rc;
   }
   for (int l = 0; l < c.n_layers; ++l)
-    if (budgets[l] < c.n_sink + 1)
-      return fail(KVEVICT_ERR_INVALID_ARG, "every layer budget must be >= n_sink + 1 (room to evict)");
+    if (budgets[l] < c.n_sink + c.recent + 1)
+      return fail(KVEVICT_ERR_INVALID_ARG,
+                  "every layer budget must be >= n_sink + recent + 1 (room to evict)");
 
   kvevict* h = new kvevict();
   h->cfg = c;

@@ -43,7 +43,7 @@ i32, i64, u64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_d
 class HeadCfg(ctypes.Structure):
     _fields_ = [("D", i32), ("budget", i32), ("n_sink", i32), ("layer", i32), ("head", i32),
                 ("tau_init", f64), ("tau_end", f64), ("anneal_steps", i64),
-                ("theta", f64), ("seed", u64)]
+                ("theta", f64), ("seed", u64), ("recent", i32), ("mode", i32)]
 
 
 def lib():
@@ -63,12 +63,13 @@ def lib():
             "orc_f16_to_f64_array": (None, [i64, P, P]),
             "orc_rope_consts": (None, [f64, i32, i64, P, P]),
             "orc_rotate_row": (None, [i32, P, P, P]),
-            "orc_step_accumulate": (i32, [i32, i32, P, P, P, P, P, i64, ctypes.c_float]),
+            "orc_step_accumulate": (i32, [i32, i32, P, P, P, P, P, i64, ctypes.c_float, i32]),
             "orc_regularised": (None, [i32, P, P, f64, P]),
-            "orc_argmin": (i32, [i32, P, i32]),
+            "orc_argmin": (i32, [i32, P, i32, i32]),
             "orc_evict": (i32, [i32, i32, P, P, P, P, i32, f64]),
             "orc_prefill_colsum": (None, [i32, i32, P, P]),
-            "orc_prefill_select": (i32, [i32, i32, i32, P, P]),
+            "orc_prefill_select": (i32, [i32, i32, i32, i32, P, P]),
+            "orc_prefill_lastrow": (None, [i32, i32, P, P]),
             "orc_prefill_apply": (i32, [i32, i32, P, P, P, P, f64, P, P, P, P]),
             "orc_run_head": (i32, [P, i32, P, i32, P, P, P, P, P, P]),
             "orc_run_heads": (i32, [i32, P, i32, P, i32, P, P, i32, P, P, P, P, P, i32]),
@@ -140,6 +141,17 @@ def rotate_row(row: np.ndarray, c: np.ndarray, s: np.ndarray) -> np.ndarray:
     return r
 
 
+SCORE_CUMULATIVE, SCORE_CURRENT = 0, 1
+
+
+def prefill_lastrow(keys: np.ndarray) -> np.ndarray:
+    keys = np.ascontiguousarray(keys, dtype=np.uint16)
+    S, D = keys.shape
+    out = np.zeros(S, dtype=np.float64)
+    lib().orc_prefill_lastrow(S, D, _p(keys), _p(out))
+    return out
+
+
 def prefill_colsum(keys: np.ndarray) -> np.ndarray:
     keys = np.ascontiguousarray(keys, dtype=np.uint16)
     S, D = keys.shape
@@ -161,10 +173,13 @@ class HeadParams:
     anneal_steps: int
     theta: float
     seed: int
+    recent: int = 0
+    mode: int = SCORE_CUMULATIVE
 
     def cstruct(self) -> HeadCfg:
         return HeadCfg(self.D, self.budget, self.n_sink, self.layer, self.head, self.tau_init,
-                       self.tau_end, self.anneal_steps, self.theta, self.seed)
+                       self.tau_end, self.anneal_steps, self.theta, self.seed, self.recent,
+                       self.mode)
 
 
 class OracleHead:
@@ -189,7 +204,7 @@ class OracleHead:
     def prefill_scores(self, keys: np.ndarray):
         """Column sums, Gumbel values and regularised scores of a prompt."""
         S = keys.shape[0]
-        colsum = prefill_colsum(keys)
+        colsum = prefill_lastrow(keys) if self.prm.mode == SCORE_CURRENT else prefill_colsum(keys)
         g = gumbel(self.prm.seed, self.prm.layer, self.prm.head, 0, S)
         t = tau(self.prm.tau_init, self.prm.tau_end, self.prm.anneal_steps, S - 1)
         r = colsum + t * g.astype(np.float64)
@@ -198,7 +213,7 @@ class OracleHead:
     def prefill_select(self, r: np.ndarray) -> np.ndarray:
         S = r.shape[0]
         mask = np.zeros(S, dtype=np.uint8)
-        rc = lib().orc_prefill_select(S, self.prm.budget, self.prm.n_sink,
+        rc = lib().orc_prefill_select(S, self.prm.budget, self.prm.n_sink, self.prm.recent,
                                       _p(np.ascontiguousarray(r, np.float64)), _p(mask))
         if rc < 0:
             raise ValueError("not enough evictable rows")
@@ -229,7 +244,7 @@ class OracleHead:
         gn = float(gumbel(self.prm.seed, self.prm.layer, self.prm.head, p, 1)[0])
         k = np.ascontiguousarray(k_new, dtype=np.uint16)
         self.n = lib().orc_step_accumulate(self.prm.D, self.n, _p(self.K), _p(self.score),
-                                           _p(self.g), _p(self.pos), _p(k), p, gn)
+                                           _p(self.g), _p(self.pos), _p(k), p, gn, self.prm.mode)
         self.next_pos = p + 1
         return self.n
 
@@ -243,10 +258,10 @@ class OracleHead:
 
     def select(self) -> int:
         self.regularised()
-        return int(lib().orc_argmin(self.n, _p(self.r), self.prm.n_sink))
+        return int(lib().orc_argmin(self.n, _p(self.r), self.prm.n_sink, self.prm.recent))
 
     def evict(self, e: int):
-        if not (self.prm.n_sink <= e < self.n):
+        if not (self.prm.n_sink <= e < self.n - self.prm.recent):
             raise ValueError(f"slot {e} is not evictable")
         self.n = lib().orc_evict(self.prm.D, self.n, _p(self.K), _p(self.score), _p(self.g),
                                  _p(self.pos), e, self.prm.theta)

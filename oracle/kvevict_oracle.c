@@ -203,9 +203,12 @@ void orc_rotate_row(int32_t D, uint16_t* row, const float* c, const float* s) {
  * attn = softmax(K k_i / sqrt(D)), scores += attn, new tokens start at 0.
  * The softmax runs over every stored row including the one just appended
  * (reading: the benchmark specification fixes this order).
+ * mode ORC_SCORE_CURRENT is the TOVA-adapted row of the PyramidKV page's
+ * method table ("current-step attention weight"): scores = attn instead.
  * ------------------------------------------------------------------------- */
 int32_t orc_step_accumulate(int32_t D, int32_t n, uint16_t* K, double* score, float* g,
-                            int32_t* pos, const uint16_t* k_new, int64_t p, float g_new) {
+                            int32_t* pos, const uint16_t* k_new, int64_t p, float g_new,
+                            int32_t mode) {
   memcpy(K + (size_t)n * D, k_new, sizeof(uint16_t) * (size_t)D);
   score[n] = 0.0;
   g[n] = g_new;
@@ -224,7 +227,11 @@ int32_t orc_step_accumulate(int32_t D, int32_t n, uint16_t* K, double* score, fl
   for (int32_t j = 1; j < n1; ++j) if (logit[j] > m) m = logit[j];
   double l = 0.0;
   for (int32_t j = 0; j < n1; ++j) l += exp(logit[j] - m);
-  for (int32_t j = 0; j < n1; ++j) score[j] += exp(logit[j] - m) / l;
+  for (int32_t j = 0; j < n1; ++j) {
+    double attn = exp(logit[j] - m) / l;
+    if (mode == ORC_SCORE_CURRENT) score[j] = attn;   /* TOVA-adapted: this step's weight */
+    else score[j] += attn;                            /* H2O rule: cumulative mass */
+  }
   free(logit);
   return n1;
 }
@@ -236,11 +243,13 @@ void orc_regularised(int32_t n, const double* score, const float* g, double tau,
 }
 
 /* Keyformer page, step 3, and PyramidKV page, "How it works" step 3: evict the
- * lowest non-protected row; the first n_sink rows are protected (+inf).
- * Ties go to the lowest slot (reading fixed by the benchmark specification). */
-int32_t orc_argmin(int32_t n, const double* r, int32_t n_sink) {
+ * lowest non-protected row; the first n_sink rows are protected (+inf), and so
+ * are the last `recent` rows (keyformer page, KeyformerState.recent: the
+ * trailing protected window, 0 = off). Ties go to the lowest slot (reading
+ * fixed by the benchmark specification). */
+int32_t orc_argmin(int32_t n, const double* r, int32_t n_sink, int32_t recent) {
   int32_t best = -1;
-  for (int32_t j = n_sink; j < n; ++j)
+  for (int32_t j = n_sink; j < n - recent; ++j)
     if (best < 0 || r[j] < r[best]) best = j;
   return best;
 }
@@ -302,15 +311,39 @@ void orc_prefill_colsum(int32_t S, int32_t D, const uint16_t* keys, double* cols
   free(kd);
 }
 
+/* TOVA-adapted prompt scores: the attention the prompt's last token pays to
+ * every prompt token, softmax(K k_{S-1} / sqrt(D)) over all S rows (reading:
+ * "current-step attention weight" at the end of the prompt). */
+void orc_prefill_lastrow(int32_t S, int32_t D, const uint16_t* keys, double* score) {
+  if (S <= 0) return;
+  double* logit = (double*)malloc(sizeof(double) * (size_t)S);
+  const uint16_t* q = keys + (size_t)(S - 1) * D;
+  double inv_sqrt_d = 1.0 / sqrt((double)D);
+  double m = -INFINITY;
+  for (int32_t j = 0; j < S; ++j) {
+    double dot = 0.0;
+    for (int32_t d = 0; d < D; ++d)
+      dot += orc_f16_to_f64(keys[(size_t)j * D + d]) * orc_f16_to_f64(q[d]);
+    logit[j] = dot * inv_sqrt_d;
+    if (logit[j] > m) m = logit[j];
+  }
+  double l = 0.0;
+  for (int32_t j = 0; j < S; ++j) l += exp(logit[j] - m);
+  for (int32_t j = 0; j < S; ++j) score[j] = exp(logit[j] - m) / l;
+  free(logit);
+}
+
 /* Bulk eviction after the prompt (reading: score the whole prompt, then evict
  * the S - budget lowest (r, slot) non-sink rows at once; lower slot first
  * among equal r). */
-int32_t orc_prefill_select(int32_t S, int32_t budget, int32_t n_sink, const double* r, uint8_t* mask) {
+int32_t orc_prefill_select(int32_t S, int32_t budget, int32_t n_sink, int32_t recent,
+                           const double* r, uint8_t* mask) {
   for (int32_t j = 0; j < S; ++j) mask[j] = 0;
   int32_t want = S - budget;
   if (want <= 0) return 0;
-  /* order the non-sink rows by (r, slot) and take the first `want` */
-  int32_t m = S - n_sink;
+  /* order the unprotected rows (not a sink, not among the last `recent`) by
+   * (r, slot) and take the first `want` */
+  int32_t m = S - n_sink - recent;
   if (m < want) return -1;
   int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)(m > 0 ? m : 1));
   for (int32_t t = 0; t < m; ++t) idx[t] = n_sink + t;
@@ -362,11 +395,12 @@ int32_t orc_run_head(const orc_head_cfg* cfg, int32_t S, const uint16_t* prefill
     float* gp = (float*)malloc(sizeof(float) * (size_t)S);
     double* r = (double*)malloc(sizeof(double) * (size_t)S);
     uint8_t* mask = (uint8_t*)malloc((size_t)S);
-    orc_prefill_colsum(S, D, prefill_keys, colsum);
+    if (cfg->mode == ORC_SCORE_CURRENT) orc_prefill_lastrow(S, D, prefill_keys, colsum);
+    else orc_prefill_colsum(S, D, prefill_keys, colsum);
     for (int32_t j = 0; j < S; ++j) gp[j] = orc_gumbel(cfg->seed, cfg->layer, cfg->head, j);
     double tau = orc_tau(cfg->tau_init, cfg->tau_end, cfg->anneal_steps, S - 1);
     for (int32_t j = 0; j < S; ++j) r[j] = colsum[j] + tau * (double)gp[j];
-    orc_prefill_select(S, budget, cfg->n_sink, r, mask);
+    orc_prefill_select(S, budget, cfg->n_sink, cfg->recent, r, mask);
     n = orc_prefill_apply(S, D, prefill_keys, colsum, gp, mask, cfg->theta, K, score, g, pos);
     free(mask); free(r); free(gp); free(colsum);
   }
@@ -377,11 +411,12 @@ int32_t orc_run_head(const orc_head_cfg* cfg, int32_t S, const uint16_t* prefill
   for (int32_t t = 0; t < T; ++t) {
     int64_t p = (int64_t)S + t;
     float gn = orc_gumbel(cfg->seed, cfg->layer, cfg->head, p);
-    int32_t n1 = orc_step_accumulate(D, n, K, score, g, pos, decode_keys + (size_t)t * D, p, gn);
+    int32_t n1 = orc_step_accumulate(D, n, K, score, g, pos, decode_keys + (size_t)t * D, p, gn,
+                                     cfg->mode);
     if (n1 > budget) {
       double tau = orc_tau(cfg->tau_init, cfg->tau_end, cfg->anneal_steps, p);
       orc_regularised(n1, score, g, tau, r);
-      int32_t e = orc_argmin(n1, r, cfg->n_sink);
+      int32_t e = orc_argmin(n1, r, cfg->n_sink, cfg->recent);
       if (evicted) evicted[t] = e;
       n = evict_with_consts(D, n1, K, score, g, pos, e, c, s);
     } else {

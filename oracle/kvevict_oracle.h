@@ -60,14 +60,20 @@ void orc_rope_consts(double theta, int32_t D, int64_t delta, float* c, float* s)
 /* Rotate one fp16 row by the given constants, fp32 arithmetic, half-split pairs. */
 void orc_rotate_row(int32_t D, uint16_t* row, const float* c, const float* s);
 
+/* Score modes: cumulative attention mass (H2O rule, Keyformer, PyramidKV) or
+ * the current step's attention weight (TOVA-adapted). */
+#define ORC_SCORE_CUMULATIVE 0
+#define ORC_SCORE_CURRENT 1
+
 /* One decode step, append + proxy-attention accumulation. The state holds n
  * rows; the new row goes to slot n. Returns n+1. Arrays need room for n+1 rows. */
 int32_t orc_step_accumulate(int32_t D, int32_t n, uint16_t* K, double* score, float* g,
-                            int32_t* pos, const uint16_t* k_new, int64_t p, float g_new);
+                            int32_t* pos, const uint16_t* k_new, int64_t p, float g_new,
+                            int32_t mode);
 /* Regularised scores r_j = score_j + tau*g_j (fp64), for all rows. */
 void orc_regularised(int32_t n, const double* score, const float* g, double tau, double* r);
-/* Lowest slot attaining min r over j >= n_sink; -1 if no row is evictable. */
-int32_t orc_argmin(int32_t n, const double* r, int32_t n_sink);
+/* Lowest slot attaining min r over n_sink <= j < n - recent; -1 if none. */
+int32_t orc_argmin(int32_t n, const double* r, int32_t n_sink, int32_t recent);
 /* Evict slot e from an n-row state: rows after e move down one slot in order,
  * each moved key re-rotated by -1 position. Returns n-1. */
 int32_t orc_evict(int32_t D, int32_t n, uint16_t* K, double* score, float* g, int32_t* pos,
@@ -76,9 +82,13 @@ int32_t orc_evict(int32_t D, int32_t n, uint16_t* K, double* score, float* g, in
 /* Prefill scoring: column sums of the causal softmax(K K^T / sqrt(D)), the
  * diagonal included. keys [S, D] fp16 bits, out colsum [S]. */
 void orc_prefill_colsum(int32_t S, int32_t D, const uint16_t* keys, double* colsum);
-/* Own bulk selection: mark the S - budget non-sink rows with the lowest
- * (r, slot); mask[j] = 1 for evicted rows. Returns the evicted count. */
-int32_t orc_prefill_select(int32_t S, int32_t budget, int32_t n_sink, const double* r, uint8_t* mask);
+/* TOVA-adapted prompt scores: the last prompt token's attention over the prompt. */
+void orc_prefill_lastrow(int32_t S, int32_t D, const uint16_t* keys, double* score);
+/* Own bulk selection: mark the S - budget unprotected rows (not among the
+ * first n_sink or the last `recent`) with the lowest (r, slot); mask[j] = 1
+ * for evicted rows. Returns the evicted count, -1 if there is no room. */
+int32_t orc_prefill_select(int32_t S, int32_t budget, int32_t n_sink, int32_t recent,
+                           const double* r, uint8_t* mask);
 /* Apply a bulk eviction mask: survivors move to consecutive slots in order,
  * each re-rotated by (new slot - old slot). Returns the kept count. */
 int32_t orc_prefill_apply(int32_t S, int32_t D, const uint16_t* keys, const double* colsum,
@@ -93,6 +103,7 @@ typedef struct orc_head_cfg {
   int32_t D, budget, n_sink, layer, head;
   double tau_init, tau_end; int64_t anneal_steps;
   double theta; uint64_t seed;
+  int32_t recent, mode;
 } orc_head_cfg;
 int32_t orc_run_head(const orc_head_cfg* cfg, int32_t S, const uint16_t* prefill_keys,
                      int32_t T, const uint16_t* decode_keys, int32_t* evicted,

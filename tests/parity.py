@@ -52,10 +52,10 @@ def _scale(head, j: int, tau: float) -> float:
     return abs(head.r[j]) + abs(head.score[j]) + abs(tau * float(head.g[j]))
 
 
-def _tie_set(head, tau: float, n_sink: int) -> tuple[list[int], float]:
+def _tie_set(head, tau: float, n_sink: int, recent: int = 0) -> tuple[list[int], float]:
     n = head.n
     r = head.r[:n]
-    cand = np.arange(n_sink, n)
+    cand = np.arange(n_sink, n - recent)
     order = cand[np.argsort(r[cand], kind="stable")]
     best = int(order[0])
     ties = [best]
@@ -133,12 +133,13 @@ def run_row(orc, prm, prefill_keys, decode_keys, gpu_ev, gpu_after_prefill=None,
                 # A boundary tie: every row the two disagree on must sit within
                 # TIE_REL of the oracle's cut between evicted and kept rows.
                 t = orc.tau(prm.tau_init, prm.tau_end, prm.anneal_steps, S - 1)
-                rs = np.sort(r[prm.n_sink:])
+                rs = np.sort(r[prm.n_sink:S - prm.recent])
                 k = S - prm.budget
                 scale = np.abs(r) + np.abs(colsum) + np.abs(t * g.astype(np.float64))
                 gpu_only = np.nonzero((gmask == 1) & (mask == 0))[0]
                 orc_only = np.nonzero((gmask == 0) & (mask == 1))[0]
                 valid = (gmask.sum() == mask.sum() and np.all(gpu_only >= prm.n_sink)
+                         and np.all(gpu_only < S - prm.recent)
                          and np.all(r[gpu_only] - rs[k - 1] <= TIE_REL * scale[gpu_only])
                          and np.all(rs[k] - r[orc_only] <= TIE_REL * scale[orc_only]))
                 if not valid:
@@ -165,7 +166,7 @@ def run_row(orc, prm, prefill_keys, decode_keys, gpu_ev, gpu_after_prefill=None,
         rep.evictions += 1
         tau = orc.tau(prm.tau_init, prm.tau_end, prm.anneal_steps, head.next_pos - 1)
         head.regularised()
-        ties, gap = _tie_set(head, tau, prm.n_sink)
+        ties, gap = _tie_set(head, tau, prm.n_sink, prm.recent)
         if len(ties) > 1:
             rep.ties += 1
         e = ties[0]

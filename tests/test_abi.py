@@ -50,7 +50,10 @@ def test_budgets_match_page_and_oracle(kvx, orc):
     (dict(tau_end=-0.5), "tau"),
     (dict(pyramid_beta=0.5), "beta"),
     (dict(max_prefill=20000), "max_prefill"),
-    (dict(layer_budgets=[10, 4]), "n_sink + 1"),
+    (dict(layer_budgets=[10, 4]), "room to evict"),
+    (dict(avg_budget=8, recent=4), "room to evict"),     # budget 8 < n_sink 4 + recent 4 + 1
+    (dict(recent=-1), "recent"),
+    (dict(score_mode=2), "score_mode"),
     (dict(n_layers=0), "n_layers"),
     (dict(batch=0), "batch"),
     (dict(anneal_steps=-1), "anneal"),

@@ -38,7 +38,8 @@ def head_params(orc, wl, l, h):
     budgets = orc.budgets(wl.n_layers, wl.avg_budget, wl.n_sink, wl.beta)
     return orc.HeadParams(D=wl.head_dim, budget=budgets[l], n_sink=wl.n_sink, layer=l, head=h,
                           tau_init=wl.tau_init, tau_end=wl.tau_end, anneal_steps=wl.anneal_steps,
-                          theta=wl.rope_theta, seed=wl.gumbel_seed)
+                          theta=wl.rope_theta, seed=wl.gumbel_seed, recent=wl.recent,
+                          mode=wl.score_mode)
 
 
 def run_gpu(kvx, wgpu, wl, rows, segments=None, mode="graph"):
@@ -125,6 +126,16 @@ SMALL = [
              rope_theta=500000.0, gumbel_seed=3, key_seed=9, prefill=0, decode=300,
              late_riser=True),
     workloads.TINY_H2O,
+    Workload("recent_window", batch=1, n_layers=2, n_kv_heads=2, head_dim=128, avg_budget=24,
+             beta=1.0, n_sink=4, tau_init=1.0, tau_end=2.0, anneal_steps=60, rope_theta=500000.0,
+             gumbel_seed=5, key_seed=10, prefill=40, decode=60, recent=5),
+    Workload("tova_prompt", batch=2, n_layers=2, n_kv_heads=2, head_dim=64, avg_budget=16,
+             beta=1.0, n_sink=2, tau_init=0.0, tau_end=0.0, anneal_steps=0, rope_theta=10000.0,
+             gumbel_seed=0, key_seed=11, prefill=30, decode=50, score_mode=1),
+    Workload("tova_recent_gumbel", batch=1, n_layers=1, n_kv_heads=3, head_dim=128,
+             avg_budget=20, beta=1.0, n_sink=4, tau_init=0.5, tau_end=0.5, anneal_steps=0,
+             rope_theta=500000.0, gumbel_seed=12, key_seed=12, prefill=0, decode=80, recent=3,
+             score_mode=1),
 ]
 
 

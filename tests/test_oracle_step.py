@@ -15,9 +15,10 @@ from scipy.special import softmax
 
 
 def _params(orc, D=64, budget=12, n_sink=4, tau_init=0.0, tau_end=0.0, A=0, theta=1e4, seed=0,
-            layer=0, head=0):
+            layer=0, head=0, recent=0, mode=0):
     return orc.HeadParams(D=D, budget=budget, n_sink=n_sink, layer=layer, head=head,
-                          tau_init=tau_init, tau_end=tau_end, anneal_steps=A, theta=theta, seed=seed)
+                          tau_init=tau_init, tau_end=tau_end, anneal_steps=A, theta=theta, seed=seed,
+                          recent=recent, mode=mode)
 
 
 def _keys(rng, T, D, scale=1.0):
@@ -51,14 +52,15 @@ class Brute:
         K = np.stack([r[0] for r in self.rows]).view(np.float16).astype(np.float64)
         attn = softmax(K @ k.view(np.float16).astype(np.float64) / math.sqrt(prm.D))
         for r, a in zip(self.rows, attn):
-            r[1] += a
+            r[1] = a if prm.mode == 1 else r[1] + a
         if len(self.rows) <= prm.budget:
             return -1
         if prm.anneal_steps > 0 and prm.tau_init != prm.tau_end:
             tau = prm.tau_init + min(p, prm.anneal_steps) * (prm.tau_end - prm.tau_init) / prm.anneal_steps
         else:
             tau = prm.tau_init
-        cand = [(r[1] + tau * r[2], j) for j, r in enumerate(self.rows) if j >= prm.n_sink]
+        cand = [(r[1] + tau * r[2], j) for j, r in enumerate(self.rows)
+                if prm.n_sink <= j < len(self.rows) - prm.recent]
         e = min(cand)[1]
         del self.rows[e]
         for r in self.rows[e:]:
@@ -66,17 +68,21 @@ class Brute:
         return e
 
 
-@pytest.mark.parametrize("D,budget,n_sink,tau_init,tau_end,A,theta", [
-    (64, 12, 4, 0.0, 0.0, 0, 1e4),
-    (64, 5, 4, 0.0, 0.0, 0, 1e4),        # budget = n_sink + 1
-    (64, 8, 0, 0.0, 0.0, 0, 1e4),        # no sinks
-    (128, 16, 4, 1.0, 2.0, 30, 5e5),     # annealed Gumbel regulariser
-    (128, 9, 2, 0.5, 0.5, 0, 5e5),       # constant tau
+@pytest.mark.parametrize("D,budget,n_sink,tau_init,tau_end,A,theta,recent,mode", [
+    (64, 12, 4, 0.0, 0.0, 0, 1e4, 0, 0),
+    (64, 5, 4, 0.0, 0.0, 0, 1e4, 0, 0),        # budget = n_sink + 1
+    (64, 8, 0, 0.0, 0.0, 0, 1e4, 0, 0),        # no sinks
+    (128, 16, 4, 1.0, 2.0, 30, 5e5, 0, 0),     # annealed Gumbel regulariser
+    (128, 9, 2, 0.5, 0.5, 0, 5e5, 0, 0),       # constant tau
+    (64, 12, 4, 0.0, 0.0, 0, 1e4, 3, 0),       # trailing protected window
+    (64, 8, 2, 0.0, 0.0, 0, 1e4, 5, 0),        # budget = n_sink + recent + 1
+    (64, 12, 4, 0.0, 0.0, 0, 1e4, 0, 1),       # TOVA-adapted (current-step scores)
+    (128, 10, 2, 1.0, 2.0, 30, 5e5, 2, 1),     # TOVA + Gumbel + recent window
 ])
-def test_brute_force_tiny(orc, D, budget, n_sink, tau_init, tau_end, A, theta):
-    rng = np.random.default_rng(budget * 7 + n_sink)
+def test_brute_force_tiny(orc, D, budget, n_sink, tau_init, tau_end, A, theta, recent, mode):
+    rng = np.random.default_rng(budget * 7 + n_sink + 13 * recent + 101 * mode)
     prm = _params(orc, D=D, budget=budget, n_sink=n_sink, tau_init=tau_init, tau_end=tau_end, A=A,
-                  theta=theta, seed=42, layer=1, head=3)
+                  theta=theta, seed=42, layer=1, head=3, recent=recent, mode=mode)
     head, brute = orc.OracleHead(prm), Brute(orc, prm)
     keys = _keys(rng, 40, D)
     for p in range(40):
@@ -274,3 +280,79 @@ def test_c_driver_matches_stepwise(orc):
         assert n[i] == head.n
         assert np.array_equal(K[i, : head.n], Kh) and np.array_equal(pos[i, : head.n], posh)
         assert np.array_equal(sc[i, : head.n], sch) and np.array_equal(g[i, : head.n], gh)
+
+
+# ---------------------------------------------------------------- recent window / TOVA
+def test_recent_window_protects_the_newest_rows(orc):
+    # keyformer page, KeyformerState.recent: a trailing protected window
+    rng = np.random.default_rng(11)
+    for recent, n_sink, budget in [(3, 4, 12), (5, 0, 7), (1, 2, 4)]:
+        head = orc.OracleHead(_params(orc, budget=budget, n_sink=n_sink, recent=recent,
+                                      tau_init=1.0, tau_end=1.0, seed=3))
+        keys = _keys(rng, 80, 64)
+        for p in range(80):
+            n_before = head.n
+            e = head.step(keys[p])
+            if e >= 0:
+                assert n_sink <= e < n_before + 1 - recent
+            K, sc, g, pos = head.state()
+            newest = list(range(max(0, p + 1 - recent), p + 1))
+            assert set(newest) <= set(pos.tolist())
+            assert head.n <= budget
+
+
+def test_recent_zero_is_the_plain_rule(orc):
+    rng = np.random.default_rng(12)
+    keys = _keys(rng, 60, 64)
+    a = orc.OracleHead(_params(orc, budget=10, tau_init=1.0, tau_end=1.0, seed=9))
+    b = orc.OracleHead(_params(orc, budget=10, tau_init=1.0, tau_end=1.0, seed=9, recent=0))
+    assert [a.step(k) for k in keys] == [b.step(k) for k in keys]
+
+
+def test_tova_closed_form_orthogonal_keys(orc):
+    # PyramidKV page, method table: TOVA-adapted scores each row by the current
+    # step's attention weight. With one-hot keys the step over i+1 rows gives
+    # the newest row E/(E+i) and every older row 1/(E+i).
+    D, c = 64, 2.0
+    head = orc.OracleHead(_params(orc, D=D, budget=40, mode=1))
+    E = math.exp(c * c / math.sqrt(D))
+    for i in range(30):
+        k = np.zeros(D, np.float16)
+        k[i] = c
+        head.step(k.view(np.uint16))
+        sc = head.state()[1]
+        np.testing.assert_allclose(sc[:-1], 1.0 / (E + i), rtol=1e-13)
+        np.testing.assert_allclose(sc[-1], E / (E + i), rtol=1e-13)
+
+
+def test_tova_scores_are_one_distribution(orc):
+    rng = np.random.default_rng(13)
+    head = orc.OracleHead(_params(orc, budget=10, mode=1))
+    for k in _keys(rng, 50, 64):
+        head.accumulate(k)
+        assert abs(head.score[: head.n].sum() - 1.0) < 1e-12
+        assert np.all(head.score[: head.n] >= 0)
+        if head.over_budget():
+            head.evict(head.select())
+
+
+def test_tova_prompt_scores_are_the_last_softmax_row(orc):
+    rng = np.random.default_rng(14)
+    for D, S in [(64, 1), (64, 33), (128, 130)]:
+        keys = _keys(rng, S, D)
+        Kf = keys.view(np.float16).astype(np.float64)
+        want = softmax(Kf @ Kf[-1] / math.sqrt(D))
+        np.testing.assert_allclose(orc.prefill_lastrow(keys), want, rtol=1e-12)
+        # and equal to one decode step over the first S-1 rows
+        head = orc.OracleHead(_params(orc, D=D, budget=S + 1, mode=1))
+        for k in keys:
+            head.step(k)
+        np.testing.assert_allclose(head.state()[1], want, rtol=1e-12)
+
+
+def test_prefill_select_respects_recent(orc):
+    head = orc.OracleHead(_params(orc, budget=6, n_sink=2, recent=2))
+    r = np.array([0.0, 0.0, 0.5, 0.2, 0.2, 0.9, 0.1, 0.8, 0.0, 0.0])  # last two lowest but protected
+    mask = head.prefill_select(r)
+    # 4 of the rows 2..7 go: 0.1 (6), 0.2 (3), 0.2 (4), 0.5 (2); rows 8, 9 are protected
+    assert list(np.nonzero(mask)[0]) == [2, 3, 4, 6]

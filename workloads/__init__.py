@@ -76,6 +76,8 @@ class Workload:
     prefill: int
     decode: int
     late_riser: bool = False
+    recent: int = 0          # trailing protected window (0 = off)
+    score_mode: int = 0      # 0 cumulative attention mass, 1 current-step attention
 
     @property
     def n_heads(self) -> int:
