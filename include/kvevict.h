@@ -71,7 +71,16 @@ typedef struct kvevict_config {
   int32_t recent;         /* trailing protected window, >= 0; 0 = off (keyformer page,
                              KeyformerState.recent); every budget >= n_sink + recent + 1 */
   int32_t score_mode;     /* KVEVICT_SCORE_CUMULATIVE (H2O rule) or KVEVICT_SCORE_CURRENT */
+  int32_t prefill_mode;   /* KVEVICT_PREFILL_BULK or KVEVICT_PREFILL_SEQUENTIAL */
 } kvevict_config;
+
+/* Prompt modes. BULK: score the whole prompt, then a row over budget evicts its
+ * lowest (score + tau(S-1) * g, slot) rows at once. SEQUENTIAL: every prompt
+ * token is absorbed as one step (page "veloxquant_mlx.quantizers.keyformer
+ * module", keyformer_update: "For each of the S incoming tokens", steps 1-3),
+ * so evictions happen inside the prompt, each with tau at its own position. */
+#define KVEVICT_PREFILL_BULK 0
+#define KVEVICT_PREFILL_SEQUENTIAL 1
 
 /* Score modes (page "PyramidKV ...", method table): cumulative attention mass
  * (H2O-adapted, Keyformer-adapted, PyramidKV-adapted) or the current step's
@@ -116,6 +125,17 @@ int kvevict_reset(kvevict_t* h, void* stream);
  * Errors: INVALID_ARG (null keys, S < 0 or S > max_prefill), BAD_STATE (state
  * not empty), CUDA. */
 int kvevict_prefill(kvevict_t* h, const uint16_t* keys, int32_t S, void* stream);
+
+/* kvevict_prefill with an optional log of the prompt's evictions: evicted is
+ * device int32 [S, B, L, H] or NULL; in SEQUENTIAL mode entry [t] is the slot
+ * the token at position t evicted (index into the rows after its append) or
+ * -1; in BULK mode every entry is -1 (the bulk choice shows in the kept
+ * positions). SEQUENTIAL mode runs the first min(S, smallest budget) tokens
+ * through the prompt scorer (no row can evict yet, so this equals as many
+ * single steps) and each further token as one decode step read straight from
+ * the prompt buffer. Errors: as kvevict_prefill. */
+int kvevict_prefill_ex(kvevict_t* h, const uint16_t* keys, int32_t S, int32_t* evicted,
+                       void* stream);
 
 /* One decode step for every row at position p = kvevict_next_pos().
  * k_new: device fp16 [B, L, H, D], RoPE-rotated at p. evicted: device int32

@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libkvevict.so")
 
 OK, ERR_INVALID_ARG, ERR_BAD_STATE, ERR_CUDA, ERR_OOM, ERR_DEVICE_CHECK = 0, -1, -2, -3, -4, -5
 SCORE_CUMULATIVE, SCORE_CURRENT = 0, 1
+PREFILL_BULK, PREFILL_SEQUENTIAL = 0, 1
 MAX_LAYERS = 256
 MAX_PREFILL = 16384
 
@@ -33,7 +34,8 @@ class Config(ctypes.Structure):
     _fields_ = [("batch", i32), ("n_layers", i32), ("n_kv_heads", i32), ("head_dim", i32),
                 ("avg_budget", i32), ("pyramid_beta", f64), ("layer_budgets", P), ("n_sink", i32),
                 ("tau_init", f32), ("tau_end", f32), ("anneal_steps", i32), ("rope_theta", f64),
-                ("seed", u64), ("max_prefill", i32), ("recent", i32), ("score_mode", i32)]
+                ("seed", u64), ("max_prefill", i32), ("recent", i32), ("score_mode", i32),
+                ("prefill_mode", i32)]
 
 
 class KVEvictError(RuntimeError):
@@ -51,6 +53,7 @@ SIGNATURES = {
     "kvevict_destroy": (ctypes.c_int, [P]),
     "kvevict_reset": (ctypes.c_int, [P, P]),
     "kvevict_prefill": (ctypes.c_int, [P, P, i32, P]),
+    "kvevict_prefill_ex": (ctypes.c_int, [P, P, i32, P, P]),
     "kvevict_step": (ctypes.c_int, [P, P, P, P]),
     "kvevict_decode": (ctypes.c_int, [P, P, i32, P, P]),
     "kvevict_run_host": (ctypes.c_int, [P, P, i32, P, i32, P, P]),
@@ -134,14 +137,14 @@ class KVEvict:
                  n_sink: int = 4, tau_init: float = 0.0, tau_end: float = 0.0,
                  anneal_steps: int = 0, rope_theta: float = 10000.0, seed: int = 0,
                  max_prefill: int = 0, recent: int = 0, score_mode: int = SCORE_CUMULATIVE,
-                 stream=None):
+                 prefill_mode: int = PREFILL_BULK, stream=None):
         self._lb = None
         if layer_budgets is not None:
             self._lb = (i32 * n_layers)(*layer_budgets)
         self.cfg = Config(batch, n_layers, n_kv_heads, head_dim, avg_budget, pyramid_beta,
                           ctypes.addressof(self._lb) if self._lb is not None else None, n_sink,
                           tau_init, tau_end, anneal_steps, rope_theta, seed & (2 ** 64 - 1),
-                          max_prefill, recent, score_mode)
+                          max_prefill, recent, score_mode, prefill_mode)
         self._h = P()
         _check(lib().kvevict_create(ctypes.addressof(self.cfg), _stream(stream),
                                     ctypes.addressof(self._h)))
@@ -170,10 +173,10 @@ class KVEvict:
         _check(lib().kvevict_reset(self._h, _stream(stream)))
 
     # ------------------------------------------------------------------ the path
-    def prefill(self, keys, stream=None):
-        """keys: device fp16 [B, L, H, S, D]."""
+    def prefill(self, keys, evicted=None, stream=None):
+        """keys: device fp16 [B, L, H, S, D]; evicted: device int32 [S, B, L, H] or None."""
         S = int(keys.shape[3]) if keys is not None else 0
-        _check(lib().kvevict_prefill(self._h, _ptr(keys), S, _stream(stream)))
+        _check(lib().kvevict_prefill_ex(self._h, _ptr(keys), S, _ptr(evicted), _stream(stream)))
 
     def step(self, k_new, evicted=None, stream=None):
         """k_new: device fp16 [B, L, H, D]; evicted: device int32 [B, L, H] or None."""
@@ -237,4 +240,5 @@ def from_workload(wl, stream=None) -> KVEvict:
                    n_sink=wl.n_sink, tau_init=wl.tau_init, tau_end=wl.tau_end,
                    anneal_steps=wl.anneal_steps, rope_theta=wl.rope_theta, seed=wl.gumbel_seed,
                    max_prefill=wl.prefill, recent=getattr(wl, "recent", 0),
-                   score_mode=getattr(wl, "score_mode", SCORE_CUMULATIVE), stream=stream)
+                   score_mode=getattr(wl, "score_mode", SCORE_CUMULATIVE),
+                   prefill_mode=getattr(wl, "prefill_mode", PREFILL_BULK), stream=stream)

@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
   float* scg = a.score + li.meta_base + (int64_t)rem * li.capm;
   float* gg = a.gum + li.meta_base + (int64_t)rem * li.capm;
   int32_t* pg = a.pos + li.meta_base + (int64_t)rem * li.capm;
-  const __half* qg = a.k_new + (((int64_t)b * a.L + l) * a.H + hh) * D;
+  const __half* qg = a.k_new + (((int64_t)b * a.L + l) * a.H + hh) * a.k_stride;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {

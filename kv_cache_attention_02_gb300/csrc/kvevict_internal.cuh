@@ -38,7 +38,8 @@ struct LayerInfo {
 };
 
 struct DecodeArgs {
-  const __half* k_new;     // [B, L, H, D] user layout
+  const __half* k_new;     // [B, L, H] rows of D, user layout, k_stride elements apart
+  int64_t k_stride;        // D for a decode step; S*D when keys come from a prompt buffer
   __half* K;
   float* score;
   float* gum;
@@ -72,18 +73,19 @@ struct FlushArgs {
 };
 
 struct PrefillScoreArgs {
-  const __half* keys;      // [heads, S, D] for the heads of this launch
+  const __half* keys;      // [heads, S_buf, D] for the heads of this launch; the first S rows used
   float* lse2;             // [heads, Sp] base-2 log-sum-exp of each causal row
   float* colsum;           // [heads, Sp]
   int S;
-  int Sp;                  // scratch row stride: S rounded up to 64
+  int S_buf;               // rows per head in the key buffer (>= S)
+  int Sp;                  // scratch row stride: S rounded up to 128
   int heads;
   float scale2;            // log2(e) / sqrt(D)
   int* err;                // error word for bounded waits, or null
 };
 
 struct PrefillSelectArgs {
-  const __half* keys;      // [heads, S, D] for the heads of this launch
+  const __half* keys;      // [heads, S_buf, D] for the heads of this launch; the first S rows used
   const float* colsum;     // [heads, S]
   float* gscr;             // [heads, S] scratch for the prompt's Gumbel values
   __half* K;
@@ -99,6 +101,7 @@ struct PrefillSelectArgs {
   int recent;              // trailing protected window
   int b0;                  // first batch index of this launch
   int S;
+  int S_buf;               // rows per head in the key buffer (>= S)
   int Sp;                  // scratch row stride
   float tau;               // tau(S - 1)
   uint64_t seed;

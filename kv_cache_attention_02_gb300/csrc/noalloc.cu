@@ -115,6 +115,7 @@ extern "C" int kvevict_prefill_scores_noalloc(const uint16_t* keys, int32_t head
   a.lse2 = scratch;
   a.colsum = scratch + (size_t)heads * Sp;
   a.S = S;
+  a.S_buf = S;
   a.Sp = (int)Sp;
   a.heads = heads;
   a.scale2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));

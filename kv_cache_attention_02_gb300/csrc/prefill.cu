@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(kSThreads) prefill_select_kernel(const Prefill
   float* scg = a.score + li.meta_base + (int64_t)slot_rem * li.capm;
   float* gg = a.gum + li.meta_base + (int64_t)slot_rem * li.capm;
   int32_t* pg = a.pos + li.meta_base + (int64_t)slot_rem * li.capm;
-  const __half* src = a.keys + (size_t)hi * S * D;
+  const __half* src = a.keys + (size_t)hi * a.S_buf * D;
   const float* col = a.colsum + (size_t)hi * a.Sp;
   float* gs = a.gscr + (size_t)hi * a.Sp;
   const int budget = li.budget;
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(256) prefill_lastrow_kernel(const PrefillScore
   __shared__ float red[64];
   const int tid = threadIdx.x, c = tid & 7, rg = tid >> 3, lane = tid & 31, w = tid >> 5;
   const int S = a.S;
-  const __half* Kh = a.keys + (size_t)blockIdx.x * S * D;
+  const __half* Kh = a.keys + (size_t)blockIdx.x * a.S_buf * D;
   const __half* q = Kh + (size_t)(S - 1) * D;
   const Chunk qlo = *reinterpret_cast<const Chunk*>(q + c * CH);
   const Chunk qhi = *reinterpret_cast<const Chunk*>(q + HALF + c * CH);

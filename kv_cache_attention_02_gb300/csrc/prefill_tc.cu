@@ -387,10 +387,11 @@ cudaError_t launch_prefill_tc(const PrefillScoreArgs& a, int D, cudaStream_t s) 
   if (a.S <= 0 || a.heads <= 0) return cudaSuccess;
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  // keys as a 3-D tensor [heads, S, D]: box = 64 elements (128 bytes) x 128 rows x 1 row
+  // keys as a 3-D tensor [heads, S, D] (rows S_buf apart): box = 64 elements (128 bytes)
+  // x 128 rows x 1 row; rows past S read as zeros
   CUtensorMap map;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.S, (cuuint64_t)a.heads};
-  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.S * D * 2};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.S_buf * D * 2};
   const cuuint32_t box[3] = {64, (cuuint32_t)kTB, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<__half*>(a.keys), dims,

@@ -122,9 +122,11 @@ namespace {
 int64_t BLHD(const kvevict* h) { return (int64_t)h->B * h->L * h->H * h->D; }
 int64_t BLH(const kvevict* h) { return (int64_t)h->B * h->L * h->H; }
 
-kvx::DecodeArgs decode_args(kvevict* h, const uint16_t* k_new, int32_t* evicted, int64_t p) {
+kvx::DecodeArgs decode_args(kvevict* h, const uint16_t* k_new, int32_t* evicted, int64_t p,
+                            int64_t k_stride) {
   kvx::DecodeArgs a{};
   a.k_new = reinterpret_cast<const __half*>(k_new);
+  a.k_stride = k_stride;
   a.K = h->K;
   a.score = h->score;
   a.gum = h->gum;
@@ -148,16 +150,17 @@ kvx::DecodeArgs decode_args(kvevict* h, const uint16_t* k_new, int32_t* evicted,
   return a;
 }
 
-int enqueue_step(kvevict* h, const uint16_t* k_new, int32_t* evicted, int64_t p, cudaStream_t s) {
-  const kvx::DecodeArgs a = decode_args(h, k_new, evicted, p);
+int enqueue_step(kvevict* h, const uint16_t* k_new, int32_t* evicted, int64_t p, cudaStream_t s,
+                 int64_t k_stride = 0) {
+  const kvx::DecodeArgs a = decode_args(h, k_new, evicted, p, k_stride > 0 ? k_stride : h->D);
   KV_CUDA(kvx::launch_decode_step(a, h->D, h->heads, h->decode_smem, s));
   return KVEVICT_OK;
 }
 
 // Score and bulk-evict the prompt for batches [b0, b0 + nb); keys point at
 // batch b0's [nb, L, H, S, D] block; lse2/colsum hold nb*L*H rows of Sp.
-int enqueue_prefill(kvevict* h, const uint16_t* keys, int32_t S, int b0, int nb, float* lse2,
-                    float* colsum, cudaStream_t s) {
+int enqueue_prompt_scores(kvevict* h, const uint16_t* keys, int32_t S, int32_t S_buf, int b0, int nb,
+                          float* lse2, float* colsum, cudaStream_t s) {
   const int heads = nb * h->L * h->H;
   const int Sp = (S + kvx::kPrefillRowPad - 1) / kvx::kPrefillRowPad * kvx::kPrefillRowPad;
   kvx::PrefillScoreArgs sa{};
@@ -165,6 +168,7 @@ int enqueue_prefill(kvevict* h, const uint16_t* keys, int32_t S, int b0, int nb,
   sa.lse2 = lse2;
   sa.colsum = colsum;
   sa.S = S;
+  sa.S_buf = S_buf;
   sa.Sp = Sp;
   sa.heads = heads;
   sa.scale2 = (float)(1.4426950408889634 / std::sqrt((double)h->D));
@@ -193,10 +197,31 @@ int enqueue_prefill(kvevict* h, const uint16_t* keys, int32_t S, int b0, int nb,
   pa.recent = h->cfg.recent;
   pa.b0 = b0;
   pa.S = S;
+  pa.S_buf = S_buf;
   pa.Sp = Sp;
   pa.tau = (float)tau_at(h->cfg, (int64_t)S - 1);
   pa.seed = h->cfg.seed;
   KV_CUDA(kvx::launch_prefill_select(pa, h->D, heads, s));
+  return KVEVICT_OK;
+}
+
+// The whole prompt of every row (keys [B, L, H, S, D] on the device). BULK: one
+// scoring pass + bulk eviction. SEQUENTIAL: the first S0 = min(S, smallest
+// budget) tokens through the scorer (no row can evict before its budget is
+// full, so this equals S0 single steps), then one decode step per further
+// token with its key read from the prompt buffer (row stride S*D).
+int enqueue_prefill(kvevict* h, const uint16_t* keys, int32_t S, int32_t* evicted, cudaStream_t s) {
+  int32_t S0 = S;
+  if (h->cfg.prefill_mode == KVEVICT_PREFILL_SEQUENTIAL)
+    for (int32_t b : h->budgets) S0 = std::min(S0, b);
+  int rc = enqueue_prompt_scores(h, keys, S0, S, 0, h->B, h->lse2, h->colsum, s);
+  if (rc != KVEVICT_OK) return rc;
+  if (evicted) KV_CUDA(cudaMemsetAsync(evicted, 0xFF, (size_t)S0 * BLH(h) * 4, s));
+  for (int32_t t = S0; t < S; ++t) {
+    rc = enqueue_step(h, keys + (size_t)t * h->D, evicted ? evicted + (size_t)t * BLH(h) : nullptr, t, s,
+                      (int64_t)S * h->D);
+    if (rc != KVEVICT_OK) return rc;
+  }
   return KVEVICT_OK;
 }
 
@@ -281,6 +306,8 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
   if (c.max_prefill < 0 || c.max_prefill > KVEVICT_MAX_PREFILL)
     return fail(KVEVICT_ERR_INVALID_ARG, "max_prefill must be in [0, KVEVICT_MAX_PREFILL]");
   if (c.recent < 0) return fail(KVEVICT_ERR_INVALID_ARG, "recent must be >= 0");
+  if (c.prefill_mode != KVEVICT_PREFILL_BULK && c.prefill_mode != KVEVICT_PREFILL_SEQUENTIAL)
+    return fail(KVEVICT_ERR_INVALID_ARG, "prefill_mode must be KVEVICT_PREFILL_BULK or KVEVICT_PREFILL_SEQUENTIAL");
   if (c.score_mode != KVEVICT_SCORE_CUMULATIVE && c.score_mode != KVEVICT_SCORE_CURRENT)
     return fail(KVEVICT_ERR_INVALID_ARG, "score_mode must be KVEVICT_SCORE_CUMULATIVE or KVEVICT_SCORE_CURRENT");
 
@@ -415,16 +442,20 @@ int kvevict_reset(kvevict_t* h, void* stream) {
   return KVEVICT_OK;
 }
 
-int kvevict_prefill(kvevict_t* h, const uint16_t* keys, int32_t S, void* stream) {
+int kvevict_prefill_ex(kvevict_t* h, const uint16_t* keys, int32_t S, int32_t* evicted, void* stream) {
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   if (S < 0 || S > h->cfg.max_prefill) return fail(KVEVICT_ERR_INVALID_ARG, "S must be in [0, max_prefill]");
   if (S > 0 && !keys) return fail(KVEVICT_ERR_INVALID_ARG, "keys is null");
   if (h->next_pos != 0 || h->stepped) return fail(KVEVICT_ERR_BAD_STATE, "prefill needs an empty state");
   if (S == 0) return KVEVICT_OK;
-  const int rc = enqueue_prefill(h, keys, S, 0, h->B, h->lse2, h->colsum, (cudaStream_t)stream);
+  const int rc = enqueue_prefill(h, keys, S, evicted, (cudaStream_t)stream);
   if (rc != KVEVICT_OK) return rc;
   h->next_pos = S;
   return KVEVICT_OK;
+}
+
+int kvevict_prefill(kvevict_t* h, const uint16_t* keys, int32_t S, void* stream) {
+  return kvevict_prefill_ex(h, keys, S, nullptr, stream);
 }
 
 int kvevict_step(kvevict_t* h, const uint16_t* k_new, int32_t* evicted, void* stream) {
@@ -490,7 +521,10 @@ int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, cons
   const size_t per_batch = (size_t)h->L * h->H * (size_t)S * h->D;
   const size_t per_step = (size_t)BLHD(h);
   const size_t budget_elems = (size_t)128 << 20;  // 256 MiB of fp16
-  const int bc = S > 0 ? (int)std::max<size_t>(1, std::min<size_t>(h->B, budget_elems / std::max<size_t>(per_batch, 1))) : 0;
+  const bool seq = h->cfg.prefill_mode == KVEVICT_PREFILL_SEQUENTIAL;
+  const int bc = S <= 0 ? 0
+                 : seq ? h->B   // sequential steps run over every row: stage the whole prompt
+                       : (int)std::max<size_t>(1, std::min<size_t>(h->B, budget_elems / std::max<size_t>(per_batch, 1)));
   const int tc = T > 0 ? (int)std::max<size_t>(1, std::min<size_t>((size_t)T, budget_elems / per_step)) : 0;
   const size_t need = std::max((size_t)bc * per_batch, (size_t)tc * per_step);
   if (!h->copy_stream) {
@@ -528,7 +562,8 @@ int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, cons
                             cudaMemcpyHostToDevice, h->copy_stream));
     KV_CUDA(cudaEventRecord(h->ev_ready[buf], h->copy_stream));
     KV_CUDA(cudaStreamWaitEvent(s, h->ev_ready[buf], 0));
-    const int rc = enqueue_prefill(h, h->stage[buf], S, b0, nb, h->lse2, h->colsum, s);
+    const int rc = seq ? enqueue_prefill(h, h->stage[buf], S, nullptr, s)
+                       : enqueue_prompt_scores(h, h->stage[buf], S, S, b0, nb, h->lse2, h->colsum, s);
     if (rc != KVEVICT_OK) return rc;
     KV_CUDA(cudaEventRecord(h->ev_free[buf], s));
   }

@@ -43,7 +43,8 @@ i32, i64, u64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_d
 class HeadCfg(ctypes.Structure):
     _fields_ = [("D", i32), ("budget", i32), ("n_sink", i32), ("layer", i32), ("head", i32),
                 ("tau_init", f64), ("tau_end", f64), ("anneal_steps", i64),
-                ("theta", f64), ("seed", u64), ("recent", i32), ("mode", i32)]
+                ("theta", f64), ("seed", u64), ("recent", i32), ("mode", i32),
+                ("prefill_mode", i32)]
 
 
 def lib():
@@ -175,11 +176,12 @@ class HeadParams:
     seed: int
     recent: int = 0
     mode: int = SCORE_CUMULATIVE
+    prefill_mode: int = 0     # 0 bulk, 1 one step per prompt token
 
     def cstruct(self) -> HeadCfg:
         return HeadCfg(self.D, self.budget, self.n_sink, self.layer, self.head, self.tau_init,
                        self.tau_end, self.anneal_steps, self.theta, self.seed, self.recent,
-                       self.mode)
+                       self.mode, self.prefill_mode)
 
 
 class OracleHead:
@@ -233,6 +235,8 @@ class OracleHead:
         self.next_pos = S
 
     def prefill(self, keys: np.ndarray) -> np.ndarray:
+        if self.prm.prefill_mode == 1:     # one step per prompt token
+            return np.array([self.step(k) for k in keys], dtype=np.int32)
         colsum, g, r = self.prefill_scores(keys)
         mask = self.prefill_select(r)
         self.prefill_apply(keys, colsum, g, mask)

@@ -389,8 +389,15 @@ int32_t orc_run_head(const orc_head_cfg* cfg, int32_t S, const uint16_t* prefill
                      int32_t T, const uint16_t* decode_keys, int32_t* evicted,
                      uint16_t* K, double* score, float* g, int32_t* pos) {
   int32_t D = cfg->D, budget = cfg->budget;
+  const uint16_t* decode_keys_all = decode_keys;
   int32_t n = 0;
-  if (S > 0) {
+  if (S > 0 && cfg->prefill_mode == 1) {
+    /* keyformer page, keyformer_update: "For each of the S incoming tokens" --
+     * every prompt token is one step, evicting inside the prompt */
+    T += S;
+    decode_keys = NULL;   /* handled below: the prompt comes first */
+  }
+  if (S > 0 && cfg->prefill_mode != 1) {
     double* colsum = (double*)malloc(sizeof(double) * (size_t)S);
     float* gp = (float*)malloc(sizeof(float) * (size_t)S);
     double* r = (double*)malloc(sizeof(double) * (size_t)S);
@@ -408,19 +415,22 @@ int32_t orc_run_head(const orc_head_cfg* cfg, int32_t S, const uint16_t* prefill
   float* s = c + D / 2;
   orc_rope_consts(cfg->theta, D, -1, c, s);
   double* r = (double*)malloc(sizeof(double) * (size_t)(budget + 2));
+  const int32_t seq = (S > 0 && cfg->prefill_mode == 1);
+  const int64_t p0 = seq ? 0 : (int64_t)S;
   for (int32_t t = 0; t < T; ++t) {
-    int64_t p = (int64_t)S + t;
+    int64_t p = p0 + t;
+    const uint16_t* k = (seq && t < S) ? prefill_keys + (size_t)t * D
+                                       : decode_keys_all + (size_t)(seq ? t - S : t) * D;
     float gn = orc_gumbel(cfg->seed, cfg->layer, cfg->head, p);
-    int32_t n1 = orc_step_accumulate(D, n, K, score, g, pos, decode_keys + (size_t)t * D, p, gn,
-                                     cfg->mode);
+    int32_t n1 = orc_step_accumulate(D, n, K, score, g, pos, k, p, gn, cfg->mode);
     if (n1 > budget) {
       double tau = orc_tau(cfg->tau_init, cfg->tau_end, cfg->anneal_steps, p);
       orc_regularised(n1, score, g, tau, r);
       int32_t e = orc_argmin(n1, r, cfg->n_sink, cfg->recent);
-      if (evicted) evicted[t] = e;
+      if (evicted && !(seq && t < S)) evicted[seq ? t - S : t] = e;
       n = evict_with_consts(D, n1, K, score, g, pos, e, c, s);
     } else {
-      if (evicted) evicted[t] = -1;
+      if (evicted && !(seq && t < S)) evicted[seq ? t - S : t] = -1;
       n = n1;
     }
   }

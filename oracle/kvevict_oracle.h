@@ -104,6 +104,7 @@ typedef struct orc_head_cfg {
   double tau_init, tau_end; int64_t anneal_steps;
   double theta; uint64_t seed;
   int32_t recent, mode;
+  int32_t prefill_mode;   /* 0: score the whole prompt then bulk-evict; 1: one step per token */
 } orc_head_cfg;
 int32_t orc_run_head(const orc_head_cfg* cfg, int32_t S, const uint16_t* prefill_keys,
                      int32_t T, const uint16_t* decode_keys, int32_t* evicted,

@@ -110,8 +110,42 @@ def compare_state(rep: RowReport, where: str, orc_state, gpu_state):
             rep.failures.append(f"{where}: gumbel values differ by more than 1 ULP")
 
 
+def _replay_steps(orc, prm, head, keys, gpu_ev, rep, what, checkpoints=None):
+    for t in range(int(keys.shape[0])):
+        head.accumulate(keys[t])
+        rep.steps += 1
+        eg = int(gpu_ev[t])
+        if not head.over_budget():
+            if eg != -1:
+                rep.failures.append(f"{what} {t}: gpu evicted {eg} within budget")
+                return
+            continue
+        rep.evictions += 1
+        tau = orc.tau(prm.tau_init, prm.tau_end, prm.anneal_steps, head.next_pos - 1)
+        head.regularised()
+        ties, gap = _tie_set(head, tau, prm.n_sink, prm.recent)
+        if len(ties) > 1:
+            rep.ties += 1
+        e = ties[0]
+        if eg != e:
+            if eg in ties:
+                rep.tie_divergences += 1
+                e = eg
+            else:
+                rep.failures.append(
+                    f"{what} {t} (pos {head.next_pos - 1}): gpu evicted {eg} "
+                    f"(r={head.r[eg] if 0 <= eg < head.n else None}), oracle {e} (r={head.r[e]}), "
+                    f"ties {ties}")
+                return
+        head.evict(e)
+        if checkpoints and (t + 1) in checkpoints:
+            compare_state(rep, f"after step {t + 1}", head.state(), checkpoints[t + 1])
+            if rep.failures:
+                return
+
+
 def run_row(orc, prm, prefill_keys, decode_keys, gpu_ev, gpu_after_prefill=None,
-            gpu_final=None, checkpoints=None) -> RowReport:
+            gpu_final=None, checkpoints=None, gpu_prompt_ev=None) -> RowReport:
     """Replay one cache row on the oracle and compare it with the CUDA path.
 
     gpu_ev: int32 [T] evicted slots the CUDA path reported per decode step.
@@ -122,6 +156,20 @@ def run_row(orc, prm, prefill_keys, decode_keys, gpu_ev, gpu_after_prefill=None,
     rep = RowReport()
     head = orc.OracleHead(prm)
     S = 0 if prefill_keys is None else int(prefill_keys.shape[0])
+    if S > 0 and getattr(prm, "prefill_mode", 0) == 1:
+        # one step per prompt token: replay them like decode steps against the
+        # CUDA path's prompt eviction log, then compare the state
+        if gpu_prompt_ev is None:
+            rep.failures.append("sequential prompt needs the CUDA path's prompt eviction log")
+            return rep
+        _replay_steps(orc, prm, head, prefill_keys, gpu_prompt_ev, rep, "prompt step")
+        if rep.failures:
+            return rep
+        if gpu_after_prefill is not None:
+            compare_state(rep, "after prefill", head.state(), gpu_after_prefill)
+            if rep.failures:
+                return rep
+        S = 0   # the prompt is done
     if S > 0:
         colsum, g, r = head.prefill_scores(prefill_keys)
         mask = head.prefill_select(r)
@@ -153,37 +201,9 @@ def run_row(orc, prm, prefill_keys, decode_keys, gpu_ev, gpu_after_prefill=None,
             compare_state(rep, "after prefill", head.state(), gpu_after_prefill)
             if rep.failures:
                 return rep
-    T = int(decode_keys.shape[0])
-    for t in range(T):
-        head.accumulate(decode_keys[t])
-        rep.steps += 1
-        eg = int(gpu_ev[t])
-        if not head.over_budget():
-            if eg != -1:
-                rep.failures.append(f"step {t}: gpu evicted {eg} within budget")
-                return rep
-            continue
-        rep.evictions += 1
-        tau = orc.tau(prm.tau_init, prm.tau_end, prm.anneal_steps, head.next_pos - 1)
-        head.regularised()
-        ties, gap = _tie_set(head, tau, prm.n_sink, prm.recent)
-        if len(ties) > 1:
-            rep.ties += 1
-        e = ties[0]
-        if eg != e:
-            if eg in ties:
-                rep.tie_divergences += 1
-                e = eg
-            else:
-                rep.failures.append(
-                    f"step {t} (pos {head.next_pos - 1}): gpu evicted {eg} (r={head.r[eg] if 0 <= eg < head.n else None}), "
-                    f"oracle {e} (r={head.r[e]}), ties {ties}")
-                return rep
-        head.evict(e)
-        if checkpoints and (t + 1) in checkpoints:
-            compare_state(rep, f"after step {t + 1}", head.state(), checkpoints[t + 1])
-            if rep.failures:
-                return rep
+    _replay_steps(orc, prm, head, decode_keys, gpu_ev, rep, "step", checkpoints)
+    if rep.failures:
+        return rep
     if gpu_final is not None:
         compare_state(rep, "final", head.state(), gpu_final)
     return rep

@@ -39,7 +39,7 @@ def head_params(orc, wl, l, h):
     return orc.HeadParams(D=wl.head_dim, budget=budgets[l], n_sink=wl.n_sink, layer=l, head=h,
                           tau_init=wl.tau_init, tau_end=wl.tau_end, anneal_steps=wl.anneal_steps,
                           theta=wl.rope_theta, seed=wl.gumbel_seed, recent=wl.recent,
-                          mode=wl.score_mode)
+                          mode=wl.score_mode, prefill_mode=wl.prefill_mode)
 
 
 def run_gpu(kvx, wgpu, wl, rows, segments=None, mode="graph"):
@@ -47,8 +47,12 @@ def run_gpu(kvx, wgpu, wl, rows, segments=None, mode="graph"):
     h = kvx.from_workload(wl)
     pre, dec = wgpu.device_inputs(wl)
     after_prefill = {}
+    pev = None
     if pre is not None:
-        h.prefill(pre)
+        if wl.prefill_mode == 1:
+            pev = torch.full((wl.prefill, wl.batch, wl.n_layers, wl.n_kv_heads), -7,
+                             dtype=torch.int32, device="cuda")
+        h.prefill(pre, pev)
         after_prefill = {r: h.read_state(*r) for r in rows}
     T = wl.decode
     ev = torch.full((T, wl.batch, wl.n_layers, wl.n_kv_heads), -7, dtype=torch.int32, device="cuda")
@@ -66,13 +70,14 @@ def run_gpu(kvx, wgpu, wl, rows, segments=None, mode="graph"):
     final = {r: h.read_state(*r) for r in rows}
     h.check()
     evh = ev.cpu().numpy()
+    pevh = pev.cpu().numpy() if pev is not None else None
     h.close()
     del pre, dec, ev
     torch.cuda.empty_cache()
-    return after_prefill, evh, final, checkpoints
+    return after_prefill, evh, final, checkpoints, pevh
 
 
-def compare_rows(orc, wl, rows, after_prefill, evh, final, checkpoints, threads=8):
+def compare_rows(orc, wl, rows, after_prefill, evh, final, checkpoints, pevh=None, threads=8):
     import parity
 
     def one(r):
@@ -81,7 +86,8 @@ def compare_rows(orc, wl, rows, after_prefill, evh, final, checkpoints, threads=
         prm = head_params(orc, wl, l, hh)
         return r, parity.run_row(orc, prm, keys[: wl.prefill] if wl.prefill else None,
                                  keys[wl.prefill:], evh[:, b, l, hh], after_prefill.get(r), final[r],
-                                 checkpoints.get(r))
+                                 checkpoints.get(r),
+                                 pevh[:, b, l, hh] if pevh is not None else None)
 
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
         reports = dict(ex.map(one, rows))
@@ -136,6 +142,14 @@ SMALL = [
              avg_budget=20, beta=1.0, n_sink=4, tau_init=0.5, tau_end=0.5, anneal_steps=0,
              rope_theta=500000.0, gumbel_seed=12, key_seed=12, prefill=0, decode=80, recent=3,
              score_mode=1),
+    Workload("sequential_prompt_pyramid", batch=2, n_layers=3, n_kv_heads=2, head_dim=128,
+             avg_budget=40, beta=1.8, n_sink=4, tau_init=1.0, tau_end=2.0, anneal_steps=100,
+             rope_theta=500000.0, gumbel_seed=13, key_seed=13, prefill=90, decode=40,
+             prefill_mode=1),
+    Workload("sequential_prompt_tova_recent", batch=1, n_layers=2, n_kv_heads=2, head_dim=64,
+             avg_budget=20, beta=1.0, n_sink=2, tau_init=0.0, tau_end=0.0, anneal_steps=0,
+             rope_theta=10000.0, gumbel_seed=0, key_seed=14, prefill=50, decode=30, recent=2,
+             score_mode=1, prefill_mode=1),
 ]
 
 

@@ -356,3 +356,44 @@ def test_prefill_select_respects_recent(orc):
     mask = head.prefill_select(r)
     # 4 of the rows 2..7 go: 0.1 (6), 0.2 (3), 0.2 (4), 0.5 (2); rows 8, 9 are protected
     assert list(np.nonzero(mask)[0]) == [2, 3, 4, 6]
+
+
+# ---------------------------------------------------------------- sequential prompt
+def test_sequential_prompt_c_driver_matches_stepwise(orc):
+    # keyformer page, keyformer_update: "For each of the S incoming tokens" the
+    # three steps run in turn, so a prompt longer than the budget evicts inside it
+    rng = np.random.default_rng(21)
+    prms = [_params(orc, D=64, budget=b, n_sink=ns, tau_init=ti, tau_end=te, A=A, seed=7,
+                    layer=l, head=h, recent=rc, mode=m)
+            for b, ns, ti, te, A, l, h, rc, m in [(10, 4, 0.0, 0.0, 0, 0, 0, 0, 0),
+                                                   (8, 2, 1.0, 2.0, 40, 1, 1, 2, 0),
+                                                   (12, 4, 0.5, 0.5, 0, 2, 3, 0, 1)]]
+    for p in prms:
+        p.prefill_mode = 1
+    S, T = 30, 25
+    pk = np.stack([_keys(rng, S, 64) for _ in prms])
+    dk = np.stack([_keys(rng, T, 64) for _ in prms])
+    ev, n, K, sc, g, pos, used = orc.run_heads(prms, pk, dk, n_threads=2)
+    for i, prm in enumerate(prms):
+        head = orc.OracleHead(prm)
+        prompt_ev = head.prefill(pk[i])
+        assert (prompt_ev >= 0).sum() == S - prm.budget     # one eviction per token past the budget
+        evs = [head.step(k) for k in dk[i]]
+        assert evs == list(ev[i])
+        Kh, sch, gh, posh = head.state()
+        assert np.array_equal(K[i, : head.n], Kh) and np.array_equal(pos[i, : head.n], posh)
+        assert np.array_equal(sc[i, : head.n], sch)
+
+
+def test_sequential_equals_bulk_when_the_prompt_fits(orc):
+    rng = np.random.default_rng(22)
+    keys = _keys(rng, 20, 64)
+    a = orc.OracleHead(_params(orc, budget=24, tau_init=1.0, tau_end=1.0, seed=2))
+    b = orc.OracleHead(_params(orc, budget=24, tau_init=1.0, tau_end=1.0, seed=2))
+    b.prm.prefill_mode = 1
+    a.prefill(keys)
+    b.prefill(keys)
+    sa, sb = a.state(), b.state()
+    for x, y in ((sa[0], sb[0]), (sa[3], sb[3]), (sa[2], sb[2])):
+        assert np.array_equal(x, y)
+    np.testing.assert_allclose(sa[1], sb[1], rtol=1e-12)

@@ -78,6 +78,7 @@ class Workload:
     late_riser: bool = False
     recent: int = 0          # trailing protected window (0 = off)
     score_mode: int = 0      # 0 cumulative attention mass, 1 current-step attention
+    prefill_mode: int = 0    # 0 bulk prompt eviction, 1 one step per prompt token
 
     @property
     def n_heads(self) -> int:
