@@ -261,13 +261,13 @@ def main():
         e2 = torch.cuda.Event(enable_timing=True)
         e3 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        h.reset(stream)
+        h.reset(stream=stream)
         if pre is not None:
-            h.prefill(pre, stream)
+            h.prefill(pre, stream=stream)
         e1.record(stream)
-        h.decode(dec, ev, stream)
+        h.decode(dec, ev, stream=stream)
         e2.record(stream)
-        h.flush(stream)
+        h.flush(stream=stream)
         e3.record(stream)
         if mark:
             ev_marks.append((e0, e1, e2, e3))
@@ -275,7 +275,7 @@ def main():
     for _ in range(args.warmup):
         one_pass()
     torch.cuda.synchronize()
-    h.check(stream)
+    h.check(stream=stream)
     step_bytes = algorithmic_bytes(wl, budgets, ev)
 
     # L2 is flushed between timed passes (outside the timed events) so every
@@ -292,7 +292,7 @@ def main():
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    h.check(stream)
+    h.check(stream=stream)
 
     pass_ms = [a.elapsed_time(d) for a, _, _, d in ev_marks]
     ms_per_step = sum(pass_ms) / len(pass_ms)
@@ -324,12 +324,12 @@ def main():
         ev_h = torch.empty(ev.shape, dtype=torch.int32, pin_memory=True)
         torch.cuda.synchronize()
         for _ in range(args.warmup):
-            h.reset(stream)
-            h.run_host(pre_h, dec_h, ev_h, stream)
+            h.reset(stream=stream)
+            h.run_host(pre_h, dec_h, ev_h, stream=stream)
         t0 = time.perf_counter()
         for _ in range(args.steps):
-            h.reset(stream)
-            h.run_host(pre_h, dec_h, ev_h, stream)
+            h.reset(stream=stream)
+            h.run_host(pre_h, dec_h, ev_h, stream=stream)
         dt = (time.perf_counter() - t0) / args.steps
         if not np.array_equal(ev_h.numpy(), ev.cpu().numpy()):
             raise SystemExit("end-to-end run disagrees with the device-resident run")

@@ -72,6 +72,9 @@ typedef struct kvevict_config {
                              KeyformerState.recent); every budget >= n_sink + recent + 1 */
   int32_t score_mode;     /* KVEVICT_SCORE_CUMULATIVE (H2O rule) or KVEVICT_SCORE_CURRENT */
   int32_t prefill_mode;   /* KVEVICT_PREFILL_BULK or KVEVICT_PREFILL_SEQUENTIAL */
+  int32_t with_values;    /* 1: the cache also holds value rows (fp16 [.., D]); they move with
+                             their keys and are never rotated (keyformer page,
+                             KeyformerState.values); 0: keys only */
 } kvevict_config;
 
 /* Prompt modes. BULK: score the whole prompt, then a row over budget evicts its
@@ -137,6 +140,24 @@ int kvevict_prefill(kvevict_t* h, const uint16_t* keys, int32_t S, void* stream)
 int kvevict_prefill_ex(kvevict_t* h, const uint16_t* keys, int32_t S, int32_t* evicted,
                        void* stream);
 
+/* The value-carrying forms (handles created with with_values = 1; the
+ * key-only calls above return INVALID_ARG on such a handle). values /
+ * v_new have the layouts of keys / k_new: device fp16 [B, L, H, S, D],
+ * [B, L, H, D] and [T, B, L, H, D]. A value row is stored, moved and evicted
+ * with its key; it is never rotated. Errors: as the key-only forms. */
+int kvevict_prefill_kv(kvevict_t* h, const uint16_t* keys, const uint16_t* values, int32_t S,
+                       int32_t* evicted, void* stream);
+int kvevict_step_kv(kvevict_t* h, const uint16_t* k_new, const uint16_t* v_new, int32_t* evicted,
+                    void* stream);
+int kvevict_decode_kv(kvevict_t* h, const uint16_t* keys, const uint16_t* values, int32_t T,
+                      int32_t* evicted, void* stream);
+
+/* Copy one row's value rows to host memory (synchronises the stream):
+ * values [n, D] fp16 bits in slot order, n = *n_kept. Errors: INVALID_ARG
+ * (indices out of range, or a key-only handle), CUDA, DEVICE_CHECK. */
+int kvevict_read_values(kvevict_t* h, int32_t b, int32_t l, int32_t head, uint16_t* values,
+                        int32_t* n_kept, void* stream);
+
 /* One decode step for every row at position p = kvevict_next_pos().
  * k_new: device fp16 [B, L, H, D], RoPE-rotated at p. evicted: device int32
  * [B, L, H] or NULL; receives the evicted slot (index into the rows after the
@@ -160,6 +181,7 @@ int kvevict_decode(kvevict_t* h, const uint16_t* keys, int32_t T, int32_t* evict
  * Errors: INVALID_ARG, BAD_STATE, OOM, CUDA, DEVICE_CHECK. */
 int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S,
                      const uint16_t* decode_keys, int32_t T, int32_t* evicted, void* stream);
+/* (key-only handles; a with_values handle returns INVALID_ARG) */
 
 /* Apply the compaction the last decode step decided (the step kernel leaves
  * the evicted row in place and the next step or this call removes it while

@@ -35,7 +35,7 @@ class Config(ctypes.Structure):
                 ("avg_budget", i32), ("pyramid_beta", f64), ("layer_budgets", P), ("n_sink", i32),
                 ("tau_init", f32), ("tau_end", f32), ("anneal_steps", i32), ("rope_theta", f64),
                 ("seed", u64), ("max_prefill", i32), ("recent", i32), ("score_mode", i32),
-                ("prefill_mode", i32)]
+                ("prefill_mode", i32), ("with_values", i32)]
 
 
 class KVEvictError(RuntimeError):
@@ -54,6 +54,10 @@ SIGNATURES = {
     "kvevict_reset": (ctypes.c_int, [P, P]),
     "kvevict_prefill": (ctypes.c_int, [P, P, i32, P]),
     "kvevict_prefill_ex": (ctypes.c_int, [P, P, i32, P, P]),
+    "kvevict_prefill_kv": (ctypes.c_int, [P, P, P, i32, P, P]),
+    "kvevict_step_kv": (ctypes.c_int, [P, P, P, P, P]),
+    "kvevict_decode_kv": (ctypes.c_int, [P, P, P, i32, P, P]),
+    "kvevict_read_values": (ctypes.c_int, [P, i32, i32, i32, P, P, P]),
     "kvevict_step": (ctypes.c_int, [P, P, P, P]),
     "kvevict_decode": (ctypes.c_int, [P, P, i32, P, P]),
     "kvevict_run_host": (ctypes.c_int, [P, P, i32, P, i32, P, P]),
@@ -137,18 +141,19 @@ class KVEvict:
                  n_sink: int = 4, tau_init: float = 0.0, tau_end: float = 0.0,
                  anneal_steps: int = 0, rope_theta: float = 10000.0, seed: int = 0,
                  max_prefill: int = 0, recent: int = 0, score_mode: int = SCORE_CUMULATIVE,
-                 prefill_mode: int = PREFILL_BULK, stream=None):
+                 prefill_mode: int = PREFILL_BULK, with_values: bool = False, stream=None):
         self._lb = None
         if layer_budgets is not None:
             self._lb = (i32 * n_layers)(*layer_budgets)
         self.cfg = Config(batch, n_layers, n_kv_heads, head_dim, avg_budget, pyramid_beta,
                           ctypes.addressof(self._lb) if self._lb is not None else None, n_sink,
                           tau_init, tau_end, anneal_steps, rope_theta, seed & (2 ** 64 - 1),
-                          max_prefill, recent, score_mode, prefill_mode)
+                          max_prefill, recent, score_mode, prefill_mode, int(bool(with_values)))
         self._h = P()
         _check(lib().kvevict_create(ctypes.addressof(self.cfg), _stream(stream),
                                     ctypes.addressof(self._h)))
         self.B, self.L, self.H, self.D = batch, n_layers, n_kv_heads, head_dim
+        self.with_values = bool(with_values)
         self.budgets = [self.layer_budget(l) for l in range(n_layers)]
 
     # ------------------------------------------------------------------ lifecycle
@@ -173,19 +178,31 @@ class KVEvict:
         _check(lib().kvevict_reset(self._h, _stream(stream)))
 
     # ------------------------------------------------------------------ the path
-    def prefill(self, keys, evicted=None, stream=None):
-        """keys: device fp16 [B, L, H, S, D]; evicted: device int32 [S, B, L, H] or None."""
+    def prefill(self, keys, evicted=None, stream=None, values=None):
+        """keys (values): device fp16 [B, L, H, S, D]; evicted: device int32 [S, B, L, H] or None."""
         S = int(keys.shape[3]) if keys is not None else 0
-        _check(lib().kvevict_prefill_ex(self._h, _ptr(keys), S, _ptr(evicted), _stream(stream)))
+        if self.with_values:
+            _check(lib().kvevict_prefill_kv(self._h, _ptr(keys), _ptr(values), S, _ptr(evicted),
+                                            _stream(stream)))
+        else:
+            _check(lib().kvevict_prefill_ex(self._h, _ptr(keys), S, _ptr(evicted), _stream(stream)))
 
-    def step(self, k_new, evicted=None, stream=None):
-        """k_new: device fp16 [B, L, H, D]; evicted: device int32 [B, L, H] or None."""
-        _check(lib().kvevict_step(self._h, _ptr(k_new), _ptr(evicted), _stream(stream)))
+    def step(self, k_new, evicted=None, stream=None, v_new=None):
+        """k_new (v_new): device fp16 [B, L, H, D]; evicted: device int32 [B, L, H] or None."""
+        if self.with_values:
+            _check(lib().kvevict_step_kv(self._h, _ptr(k_new), _ptr(v_new), _ptr(evicted),
+                                         _stream(stream)))
+        else:
+            _check(lib().kvevict_step(self._h, _ptr(k_new), _ptr(evicted), _stream(stream)))
 
-    def decode(self, keys, evicted=None, stream=None):
-        """keys: device fp16 [T, B, L, H, D]; evicted: device int32 [T, B, L, H] or None."""
-        _check(lib().kvevict_decode(self._h, _ptr(keys), int(keys.shape[0]), _ptr(evicted),
-                                    _stream(stream)))
+    def decode(self, keys, evicted=None, stream=None, values=None):
+        """keys (values): device fp16 [T, B, L, H, D]; evicted: device int32 [T, B, L, H] or None."""
+        if self.with_values:
+            _check(lib().kvevict_decode_kv(self._h, _ptr(keys), _ptr(values), int(keys.shape[0]),
+                                           _ptr(evicted), _stream(stream)))
+        else:
+            _check(lib().kvevict_decode(self._h, _ptr(keys), int(keys.shape[0]), _ptr(evicted),
+                                        _stream(stream)))
 
     def run_host(self, prefill_keys, decode_keys, evicted=None, stream=None):
         """End to end from host memory (pinned tensors or numpy uint16 arrays)."""
@@ -208,6 +225,15 @@ class KVEvict:
                                         _stream(stream)))
         k = n.value
         return keys[:k], sc[:k], g[:k], pos[:k]
+
+    def read_values(self, b: int, l: int, h: int, stream=None):
+        """Value rows of one cache row, fp16 bits [n, D], in slot order."""
+        cap = self.budgets[l] + 1 if 0 <= l < self.L else 1
+        vals = np.zeros((cap, self.D), np.uint16)
+        n = i32(0)
+        _check(lib().kvevict_read_values(self._h, b, l, h, vals.ctypes.data, ctypes.addressof(n),
+                                         _stream(stream)))
+        return vals[: n.value]
 
     def flush(self, stream=None):
         """Apply the last step's pending compaction (one kernel launch)."""
@@ -233,7 +259,7 @@ class KVEvict:
         return v.value
 
 
-def from_workload(wl, stream=None) -> KVEvict:
+def from_workload(wl, stream=None, with_values=False) -> KVEvict:
     """Handle for a ``workloads.Workload`` configuration."""
     return KVEvict(batch=wl.batch, n_layers=wl.n_layers, n_kv_heads=wl.n_kv_heads,
                    head_dim=wl.head_dim, avg_budget=wl.avg_budget, pyramid_beta=wl.beta,
@@ -241,4 +267,5 @@ def from_workload(wl, stream=None) -> KVEvict:
                    anneal_steps=wl.anneal_steps, rope_theta=wl.rope_theta, seed=wl.gumbel_seed,
                    max_prefill=wl.prefill, recent=getattr(wl, "recent", 0),
                    score_mode=getattr(wl, "score_mode", SCORE_CUMULATIVE),
-                   prefill_mode=getattr(wl, "prefill_mode", PREFILL_BULK), stream=stream)
+                   prefill_mode=getattr(wl, "prefill_mode", PREFILL_BULK),
+                   with_values=with_values, stream=stream)

@@ -267,6 +267,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
   float* gg = a.gum + li.meta_base + (int64_t)rem * li.capm;
   int32_t* pg = a.pos + li.meta_base + (int64_t)rem * li.capm;
   const __half* qg = a.k_new + (((int64_t)b * a.L + l) * a.H + hh) * a.k_stride;
+  __half* Vg = a.V ? a.V + (li.row_base + (int64_t)rem * li.cap) * D : nullptr;
+  const __half* vg = a.V ? a.v_new + (((int64_t)b * a.L + l) * a.H + hh) * a.k_stride : nullptr;
+  // value rows after the dead row move down one slot; they stream through the
+  // ring after the key tiles (no rotation, no scoring)
+  const int vstart = e_prev + 1;
+  const int nvt = (a.V && shift && vstart < nphys) ? (nphys - vstart + kTile - 1) / kTile : 0;
+  const int ntot = ntiles + nvt;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -281,21 +288,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
   volatile int* abort_flag = &s_abort;
 
   float run_m = -INFINITY, run_l = 0.f;   // this thread's share of the softmax statistics
-  Chunk q_lo{}, q_hi{};
+  Chunk q_lo{}, q_hi{}, v_lo{}, v_hi{};
   float gnew = 0.f;
 
   if (warp == kConsumerWarps) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
       int t = 0;
-      for (; t < ntiles; ++t) {
+      for (; t < ntot; ++t) {
         const int s = t % kStages;
         if (t >= kStages && !wait_watch(empty(s), (uint32_t)((t / kStages - 1) & 1), abort_flag, a.err))
           break;
-        const int rows = min(kTile, nphys - t * kTile);
+        const int r0 = t < ntiles ? t * kTile : vstart + (t - ntiles) * kTile;
+        const int rows = min(kTile, nphys - r0);
         const uint32_t bytes = (uint32_t)rows * G::ROWB;
+        const __half* src = (t < ntiles ? Kg : Vg) + (size_t)r0 * D;
         mbar_expect_tx(full(s), bytes);
-        bulk_g2s(smem_addr(ring + (size_t)s * G::TILEB), Kg + (size_t)t * kTile * D, bytes, full(s));
+        bulk_g2s(smem_addr(ring + (size_t)s * G::TILEB), src, bytes, full(s));
       }
       const int issued = t;
       bool drained = true;   // every issued tile consumed, so the ring is free
@@ -321,6 +330,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
     // thread's pair indices stay in registers for the whole pass.
     q_lo = *reinterpret_cast<const Chunk*>(qg + c * CH);
     q_hi = *reinterpret_cast<const Chunk*>(qg + HALF + c * CH);
+    if (vg && tid < kTPR) {
+      v_lo = *reinterpret_cast<const Chunk*>(vg + c * CH);
+      v_hi = *reinterpret_cast<const Chunk*>(vg + HALF + c * CH);
+    }
     float2 rc[CH / 2], rs[CH / 2];
 #pragma unroll
     for (int k = 0; k < CH / 2; ++k) {
@@ -393,6 +406,26 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
       __syncwarp();
       if (lane == 0) mbar_arrive_cta(empty(st));
     }
+    for (int t = ntiles; t < ntot && !*abort_flag; ++t) {   // value rows: move down one slot
+      const int st = t % kStages;
+      if (!wait_watch(full(st), (uint32_t)((t / kStages) & 1), abort_flag, a.err)) break;
+      const unsigned char* tile = ring + (size_t)st * G::TILEB;
+      const int r0 = vstart + (t - ntiles) * kTile;
+#pragma unroll
+      for (int pass = 0; pass < kTile / kRowsPerPass; ++pass) {
+        const int rr = pass * kRowsPerPass + rg;
+        const int R = r0 + rr;
+        if (R < nphys) {
+          const unsigned char* row = tile + (size_t)rr * G::ROWB;
+          __half* dst = Vg + (size_t)(R - 1) * D;
+          *reinterpret_cast<Chunk*>(dst + c * CH) = *reinterpret_cast<const Chunk*>(row + c * CH * 2);
+          *reinterpret_cast<Chunk*>(dst + HALF + c * CH) =
+              *reinterpret_cast<const Chunk*>(row + (HALF + c * CH) * 2);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(empty(st));
+    }
   }
 
   // every consumer is done with the stream (and s_log); wait for the metadata
@@ -437,10 +470,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
       pg[R - 1] = s_pos[R - pos0];
     }
   }
-  if (R_e != nphys && tid < kTPR) {   // the new key, unless it was evicted itself
+  if (R_e != nphys && tid < kTPR) {   // the new key (and value), unless it was evicted itself
     __half* dst = Kg + (size_t)n * D;
     *reinterpret_cast<Chunk*>(dst + c * CH) = q_lo;
     *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = q_hi;
+    if (Vg) {
+      __half* vd = Vg + (size_t)n * D;
+      *reinterpret_cast<Chunk*>(vd + c * CH) = v_lo;
+      *reinterpret_cast<Chunk*>(vd + HALF + c * CH) = v_hi;
+    }
   }
   if (tid == 0) {
     gg[n] = gnew;
@@ -471,6 +509,7 @@ __global__ void __launch_bounds__(kConsumers) flush_kernel(const FlushArgs a) {
   const int n = (int)(a.p < (int64_t)li.budget ? a.p : (int64_t)li.budget);
   const int nphys = n + 1;
   __half* Kg = a.K + (li.row_base + (int64_t)rem * li.cap) * D;
+  __half* Vg = a.V ? a.V + (li.row_base + (int64_t)rem * li.cap) * D : nullptr;
   float* scg = a.score + li.meta_base + (int64_t)rem * li.capm;
   float* gg = a.gum + li.meta_base + (int64_t)rem * li.capm;
   int32_t* pg = a.pos + li.meta_base + (int64_t)rem * li.capm;
@@ -483,12 +522,16 @@ __global__ void __launch_bounds__(kConsumers) flush_kernel(const FlushArgs a) {
   for (int base = e + 1; base < nphys; base += kRowsPerPass) {
     const int R = base + rg;
     const bool live = R < nphys;
-    Chunk lo{}, hi{};
+    Chunk lo{}, hi{}, vlo{}, vhi{};
     float sv = 0.f, gv = 0.f;
     int pv = 0;
     if (live) {
       lo = *reinterpret_cast<const Chunk*>(Kg + (size_t)R * D + c * CH);
       hi = *reinterpret_cast<const Chunk*>(Kg + (size_t)R * D + HALF + c * CH);
+      if (Vg) {
+        vlo = *reinterpret_cast<const Chunk*>(Vg + (size_t)R * D + c * CH);
+        vhi = *reinterpret_cast<const Chunk*>(Vg + (size_t)R * D + HALF + c * CH);
+      }
       if (c == 0) { sv = scg[R]; gv = gg[R]; pv = pg[R]; }
     }
     __syncthreads();
@@ -501,6 +544,11 @@ __global__ void __launch_bounds__(kConsumers) flush_kernel(const FlushArgs a) {
       *reinterpret_cast<Chunk*>(dst + c * CH) = pack2<CH>(fa);
       *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = pack2<CH>(fb);
       if (c == 0) { scg[R - 1] = sv; gg[R - 1] = gv; pg[R - 1] = pv; }
+      if (Vg) {
+        __half* vd = Vg + (size_t)(R - 1) * D;
+        *reinterpret_cast<Chunk*>(vd + c * CH) = vlo;
+        *reinterpret_cast<Chunk*>(vd + HALF + c * CH) = vhi;
+      }
     }
     __syncthreads();
   }

@@ -40,7 +40,9 @@ struct LayerInfo {
 struct DecodeArgs {
   const __half* k_new;     // [B, L, H] rows of D, user layout, k_stride elements apart
   int64_t k_stride;        // D for a decode step; S*D when keys come from a prompt buffer
+  const __half* v_new;     // value rows, same layout and stride as k_new (null: keys only)
   __half* K;
+  __half* V;               // value arena, same layout as K (null: keys only)
   float* score;
   float* gum;
   int32_t* pos;
@@ -61,6 +63,7 @@ struct DecodeArgs {
 
 struct FlushArgs {
   __half* K;
+  __half* V;               // null: keys only
   float* score;
   float* gum;
   int32_t* pos;
@@ -86,6 +89,8 @@ struct PrefillScoreArgs {
 
 struct PrefillSelectArgs {
   const __half* keys;      // [heads, S_buf, D] for the heads of this launch; the first S rows used
+  const __half* values;    // same layout as keys (null: keys only)
+  __half* V;               // value arena (null: keys only)
   const float* colsum;     // [heads, S]
   float* gscr;             // [heads, S] scratch for the prompt's Gumbel values
   __half* K;

@@ -42,6 +42,8 @@ __global__ void __launch_bounds__(kSThreads) prefill_select_kernel(const Prefill
   float* gg = a.gum + li.meta_base + (int64_t)slot_rem * li.capm;
   int32_t* pg = a.pos + li.meta_base + (int64_t)slot_rem * li.capm;
   const __half* src = a.keys + (size_t)hi * a.S_buf * D;
+  const __half* vsrc = a.V ? a.values + (size_t)hi * a.S_buf * D : nullptr;
+  __half* Vg = a.V ? a.V + (li.row_base + (int64_t)slot_rem * li.cap) * D : nullptr;
   const float* col = a.colsum + (size_t)hi * a.Sp;
   float* gs = a.gscr + (size_t)hi * a.Sp;
   const int budget = li.budget;
@@ -59,6 +61,12 @@ __global__ void __launch_bounds__(kSThreads) prefill_select_kernel(const Prefill
         *reinterpret_cast<Chunk*>(Kg + (size_t)j * D + c * CH) = lo;
         *reinterpret_cast<Chunk*>(Kg + (size_t)j * D + HALF + c * CH) = hi2;
         if (c == 0) { scg[j] = col[j]; gg[j] = gs[j]; pg[j] = j; }
+        if (Vg) {
+          *reinterpret_cast<Chunk*>(Vg + (size_t)j * D + c * CH) =
+              *reinterpret_cast<const Chunk*>(vsrc + (size_t)j * D + c * CH);
+          *reinterpret_cast<Chunk*>(Vg + (size_t)j * D + HALF + c * CH) =
+              *reinterpret_cast<const Chunk*>(vsrc + (size_t)j * D + HALF + c * CH);
+        }
       }
     }
     if (tid == 0) a.pend[slot] = -1;
@@ -163,6 +171,12 @@ __global__ void __launch_bounds__(kSThreads) prefill_select_kernel(const Prefill
       *reinterpret_cast<Chunk*>(Kg + (size_t)ns * D + c * CH) = lo;
       *reinterpret_cast<Chunk*>(Kg + (size_t)ns * D + HALF + c * CH) = hi2;
       if (c == 0) { scg[ns] = col[j]; gg[ns] = gs[j]; pg[ns] = j; }
+      if (Vg) {   // value rows move with their keys, never rotated
+        *reinterpret_cast<Chunk*>(Vg + (size_t)ns * D + c * CH) =
+            *reinterpret_cast<const Chunk*>(vsrc + (size_t)j * D + c * CH);
+        *reinterpret_cast<Chunk*>(Vg + (size_t)ns * D + HALF + c * CH) =
+            *reinterpret_cast<const Chunk*>(vsrc + (size_t)j * D + HALF + c * CH);
+      }
     }
   }
   if (tid == 0) a.pend[slot] = -1;

@@ -85,6 +85,7 @@ struct kvevict {
   int capm_max = 0;
   LayerInfo* d_layers = nullptr;
   __half* K = nullptr;
+  __half* V = nullptr;      // value rows (with_values handles only)
   float* score = nullptr;
   float* gum = nullptr;
   int32_t* pos = nullptr;
@@ -104,6 +105,7 @@ struct kvevict {
   cudaStream_t cap_stream = nullptr;
   cudaGraphExec_t gexec = nullptr;
   const void* g_keys = nullptr;
+  const void* g_vals = nullptr;
   const void* g_ev = nullptr;
   int g_T = -1;
   int64_t g_p0 = -1;
@@ -122,12 +124,14 @@ namespace {
 int64_t BLHD(const kvevict* h) { return (int64_t)h->B * h->L * h->H * h->D; }
 int64_t BLH(const kvevict* h) { return (int64_t)h->B * h->L * h->H; }
 
-kvx::DecodeArgs decode_args(kvevict* h, const uint16_t* k_new, int32_t* evicted, int64_t p,
-                            int64_t k_stride) {
+kvx::DecodeArgs decode_args(kvevict* h, const uint16_t* k_new, const uint16_t* v_new,
+                            int32_t* evicted, int64_t p, int64_t k_stride) {
   kvx::DecodeArgs a{};
   a.k_new = reinterpret_cast<const __half*>(k_new);
   a.k_stride = k_stride;
+  a.v_new = reinterpret_cast<const __half*>(v_new);
   a.K = h->K;
+  a.V = h->V;
   a.score = h->score;
   a.gum = h->gum;
   a.pos = h->pos;
@@ -150,17 +154,17 @@ kvx::DecodeArgs decode_args(kvevict* h, const uint16_t* k_new, int32_t* evicted,
   return a;
 }
 
-int enqueue_step(kvevict* h, const uint16_t* k_new, int32_t* evicted, int64_t p, cudaStream_t s,
-                 int64_t k_stride = 0) {
-  const kvx::DecodeArgs a = decode_args(h, k_new, evicted, p, k_stride > 0 ? k_stride : h->D);
+int enqueue_step(kvevict* h, const uint16_t* k_new, const uint16_t* v_new, int32_t* evicted, int64_t p,
+                 cudaStream_t s, int64_t k_stride = 0) {
+  const kvx::DecodeArgs a = decode_args(h, k_new, v_new, evicted, p, k_stride > 0 ? k_stride : h->D);
   KV_CUDA(kvx::launch_decode_step(a, h->D, h->heads, h->decode_smem, s));
   return KVEVICT_OK;
 }
 
 // Score and bulk-evict the prompt for batches [b0, b0 + nb); keys point at
 // batch b0's [nb, L, H, S, D] block; lse2/colsum hold nb*L*H rows of Sp.
-int enqueue_prompt_scores(kvevict* h, const uint16_t* keys, int32_t S, int32_t S_buf, int b0, int nb,
-                          float* lse2, float* colsum, cudaStream_t s) {
+int enqueue_prompt_scores(kvevict* h, const uint16_t* keys, const uint16_t* values, int32_t S,
+                          int32_t S_buf, int b0, int nb, float* lse2, float* colsum, cudaStream_t s) {
   const int heads = nb * h->L * h->H;
   const int Sp = (S + kvx::kPrefillRowPad - 1) / kvx::kPrefillRowPad * kvx::kPrefillRowPad;
   kvx::PrefillScoreArgs sa{};
@@ -179,6 +183,8 @@ int enqueue_prompt_scores(kvevict* h, const uint16_t* keys, int32_t S, int32_t S
     KV_CUDA(kvx::launch_prefill_tc(sa, h->D, s));
   kvx::PrefillSelectArgs pa{};
   pa.keys = sa.keys;
+  pa.values = reinterpret_cast<const __half*>(values);
+  pa.V = h->V;
   pa.colsum = colsum;
   pa.gscr = lse2;  // pass 1's output is dead once the column sums exist
   pa.K = h->K;
@@ -210,16 +216,17 @@ int enqueue_prompt_scores(kvevict* h, const uint16_t* keys, int32_t S, int32_t S
 // budget) tokens through the scorer (no row can evict before its budget is
 // full, so this equals S0 single steps), then one decode step per further
 // token with its key read from the prompt buffer (row stride S*D).
-int enqueue_prefill(kvevict* h, const uint16_t* keys, int32_t S, int32_t* evicted, cudaStream_t s) {
+int enqueue_prefill(kvevict* h, const uint16_t* keys, const uint16_t* values, int32_t S, int32_t* evicted,
+                    cudaStream_t s) {
   int32_t S0 = S;
   if (h->cfg.prefill_mode == KVEVICT_PREFILL_SEQUENTIAL)
     for (int32_t b : h->budgets) S0 = std::min(S0, b);
-  int rc = enqueue_prompt_scores(h, keys, S0, S, 0, h->B, h->lse2, h->colsum, s);
+  int rc = enqueue_prompt_scores(h, keys, values, S0, S, 0, h->B, h->lse2, h->colsum, s);
   if (rc != KVEVICT_OK) return rc;
   if (evicted) KV_CUDA(cudaMemsetAsync(evicted, 0xFF, (size_t)S0 * BLH(h) * 4, s));
   for (int32_t t = S0; t < S; ++t) {
-    rc = enqueue_step(h, keys + (size_t)t * h->D, evicted ? evicted + (size_t)t * BLH(h) : nullptr, t, s,
-                      (int64_t)S * h->D);
+    rc = enqueue_step(h, keys + (size_t)t * h->D, values ? values + (size_t)t * h->D : nullptr,
+                      evicted ? evicted + (size_t)t * BLH(h) : nullptr, t, s, (int64_t)S * h->D);
     if (rc != KVEVICT_OK) return rc;
   }
   return KVEVICT_OK;
@@ -228,6 +235,7 @@ int enqueue_prefill(kvevict* h, const uint16_t* keys, int32_t S, int32_t* evicte
 int enqueue_flush(kvevict* h, cudaStream_t s) {
   kvx::FlushArgs f{};
   f.K = h->K;
+  f.V = h->V;
   f.score = h->score;
   f.gum = h->gum;
   f.pos = h->pos;
@@ -268,6 +276,7 @@ void free_all(kvevict* h) {
   }
   cudaFree(h->d_layers);
   cudaFree(h->K);
+  cudaFree(h->V);
   cudaFree(h->score);
   cudaFree(h->gum);
   cudaFree(h->pos);
@@ -306,6 +315,7 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
   if (c.max_prefill < 0 || c.max_prefill > KVEVICT_MAX_PREFILL)
     return fail(KVEVICT_ERR_INVALID_ARG, "max_prefill must be in [0, KVEVICT_MAX_PREFILL]");
   if (c.recent < 0) return fail(KVEVICT_ERR_INVALID_ARG, "recent must be >= 0");
+  if (c.with_values != 0 && c.with_values != 1) return fail(KVEVICT_ERR_INVALID_ARG, "with_values must be 0 or 1");
   if (c.prefill_mode != KVEVICT_PREFILL_BULK && c.prefill_mode != KVEVICT_PREFILL_SEQUENTIAL)
     return fail(KVEVICT_ERR_INVALID_ARG, "prefill_mode must be KVEVICT_PREFILL_BULK or KVEVICT_PREFILL_SEQUENTIAL");
   if (c.score_mode != KVEVICT_SCORE_CUMULATIVE && c.score_mode != KVEVICT_SCORE_CURRENT)
@@ -386,6 +396,7 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
   KV_CUDA_CREATE(kvx::prefill_tc_setup(h->D));
   KV_CUDA_CREATE(dalloc(&h->d_layers, (size_t)c.n_layers));
   KV_CUDA_CREATE(dalloc(&h->K, (size_t)rows * h->D));
+  if (c.with_values) KV_CUDA_CREATE(dalloc(&h->V, (size_t)rows * h->D));
   KV_CUDA_CREATE(dalloc(&h->score, (size_t)meta));
   KV_CUDA_CREATE(dalloc(&h->gum, (size_t)meta));
   KV_CUDA_CREATE(dalloc(&h->pos, (size_t)meta));
@@ -398,7 +409,7 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
     KV_CUDA_CREATE(dalloc(&h->lse2, (size_t)h->heads * h->Sp_max));
     KV_CUDA_CREATE(dalloc(&h->colsum, (size_t)h->heads * h->Sp_max));
   }
-  h->bytes = (size_t)rows * h->D * 2 + (size_t)meta * 12 + (size_t)h->heads * 4 +
+  h->bytes = (size_t)rows * h->D * 2 * (c.with_values ? 2 : 1) + (size_t)meta * 12 + (size_t)h->heads * 4 +
              2 * (size_t)(h->max_delta + 1) * half * 4 + 2 * (size_t)h->heads * h->Sp_max * 4;
 
   // RoPE constants for a shift back by d positions: c = f32(cos(-d w_i)),
@@ -442,39 +453,38 @@ int kvevict_reset(kvevict_t* h, void* stream) {
   return KVEVICT_OK;
 }
 
-int kvevict_prefill_ex(kvevict_t* h, const uint16_t* keys, int32_t S, int32_t* evicted, void* stream) {
-  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+}  // extern "C"
+
+namespace {
+
+int prefill_impl(kvevict* h, const uint16_t* keys, const uint16_t* values, int32_t S, int32_t* evicted,
+                 void* stream) {
   if (S < 0 || S > h->cfg.max_prefill) return fail(KVEVICT_ERR_INVALID_ARG, "S must be in [0, max_prefill]");
-  if (S > 0 && !keys) return fail(KVEVICT_ERR_INVALID_ARG, "keys is null");
+  if (S > 0 && (!keys || (h->V && !values))) return fail(KVEVICT_ERR_INVALID_ARG, "keys or values is null");
   if (h->next_pos != 0 || h->stepped) return fail(KVEVICT_ERR_BAD_STATE, "prefill needs an empty state");
   if (S == 0) return KVEVICT_OK;
-  const int rc = enqueue_prefill(h, keys, S, evicted, (cudaStream_t)stream);
+  const int rc = enqueue_prefill(h, keys, values, S, evicted, (cudaStream_t)stream);
   if (rc != KVEVICT_OK) return rc;
   h->next_pos = S;
   return KVEVICT_OK;
 }
 
-int kvevict_prefill(kvevict_t* h, const uint16_t* keys, int32_t S, void* stream) {
-  return kvevict_prefill_ex(h, keys, S, nullptr, stream);
-}
-
-int kvevict_step(kvevict_t* h, const uint16_t* k_new, int32_t* evicted, void* stream) {
-  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
-  if (!k_new) return fail(KVEVICT_ERR_INVALID_ARG, "k_new is null");
-  const int rc = enqueue_step(h, k_new, evicted, h->next_pos, (cudaStream_t)stream);
+int step_impl(kvevict* h, const uint16_t* k_new, const uint16_t* v_new, int32_t* evicted, void* stream) {
+  if (!k_new || (h->V && !v_new)) return fail(KVEVICT_ERR_INVALID_ARG, "k_new or v_new is null");
+  const int rc = enqueue_step(h, k_new, v_new, evicted, h->next_pos, (cudaStream_t)stream);
   if (rc != KVEVICT_OK) return rc;
   h->next_pos += 1;
   h->stepped = true;
   return KVEVICT_OK;
 }
 
-int kvevict_decode(kvevict_t* h, const uint16_t* keys, int32_t T, int32_t* evicted, void* stream) {
-  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+int decode_impl(kvevict* h, const uint16_t* keys, const uint16_t* values, int32_t T, int32_t* evicted,
+                void* stream) {
   if (T < 0) return fail(KVEVICT_ERR_INVALID_ARG, "T must be >= 0");
   if (T == 0) return KVEVICT_OK;
-  if (!keys) return fail(KVEVICT_ERR_INVALID_ARG, "keys is null");
-  const bool hit = h->gexec && h->g_keys == keys && h->g_ev == evicted && h->g_T == T &&
-                   h->g_p0 == h->next_pos;
+  if (!keys || (h->V && !values)) return fail(KVEVICT_ERR_INVALID_ARG, "keys or values is null");
+  const bool hit = h->gexec && h->g_keys == keys && h->g_vals == values && h->g_ev == evicted &&
+                   h->g_T == T && h->g_p0 == h->next_pos;
   if (!hit) {
     if (h->gexec) {
       cudaGraphExecDestroy(h->gexec);
@@ -483,8 +493,8 @@ int kvevict_decode(kvevict_t* h, const uint16_t* keys, int32_t T, int32_t* evict
     KV_CUDA(cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
     int rc = KVEVICT_OK;
     for (int32_t t = 0; t < T && rc == KVEVICT_OK; ++t)
-      rc = enqueue_step(h, keys + (size_t)t * BLHD(h), evicted ? evicted + (size_t)t * BLH(h) : nullptr,
-                        h->next_pos + t, h->cap_stream);
+      rc = enqueue_step(h, keys + (size_t)t * BLHD(h), values ? values + (size_t)t * BLHD(h) : nullptr,
+                        evicted ? evicted + (size_t)t * BLH(h) : nullptr, h->next_pos + t, h->cap_stream);
     cudaGraph_t graph = nullptr;
     const cudaError_t ce = cudaStreamEndCapture(h->cap_stream, &graph);
     if (rc != KVEVICT_OK) {
@@ -499,6 +509,7 @@ int kvevict_decode(kvevict_t* h, const uint16_t* keys, int32_t T, int32_t* evict
       return fail(KVEVICT_ERR_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(ie));
     }
     h->g_keys = keys;
+    h->g_vals = values;
     h->g_ev = evicted;
     h->g_T = T;
     h->g_p0 = h->next_pos;
@@ -509,12 +520,68 @@ int kvevict_decode(kvevict_t* h, const uint16_t* keys, int32_t T, int32_t* evict
   return KVEVICT_OK;
 }
 
+int keys_only(const kvevict* h) {
+  return h->V ? fail(KVEVICT_ERR_INVALID_ARG, "this handle carries values: use the _kv entry points")
+              : KVEVICT_OK;
+}
+int with_values(const kvevict* h) {
+  return h->V ? KVEVICT_OK : fail(KVEVICT_ERR_INVALID_ARG, "this handle was created without values");
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvevict_prefill_ex(kvevict_t* h, const uint16_t* keys, int32_t S, int32_t* evicted, void* stream) {
+  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  if (int rc = keys_only(h)) return rc;
+  return prefill_impl(h, keys, nullptr, S, evicted, stream);
+}
+
+int kvevict_prefill(kvevict_t* h, const uint16_t* keys, int32_t S, void* stream) {
+  return kvevict_prefill_ex(h, keys, S, nullptr, stream);
+}
+
+int kvevict_prefill_kv(kvevict_t* h, const uint16_t* keys, const uint16_t* values, int32_t S,
+                       int32_t* evicted, void* stream) {
+  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  if (int rc = with_values(h)) return rc;
+  return prefill_impl(h, keys, values, S, evicted, stream);
+}
+
+int kvevict_step(kvevict_t* h, const uint16_t* k_new, int32_t* evicted, void* stream) {
+  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  if (int rc = keys_only(h)) return rc;
+  return step_impl(h, k_new, nullptr, evicted, stream);
+}
+
+int kvevict_step_kv(kvevict_t* h, const uint16_t* k_new, const uint16_t* v_new, int32_t* evicted,
+                    void* stream) {
+  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  if (int rc = with_values(h)) return rc;
+  return step_impl(h, k_new, v_new, evicted, stream);
+}
+
+int kvevict_decode(kvevict_t* h, const uint16_t* keys, int32_t T, int32_t* evicted, void* stream) {
+  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  if (int rc = keys_only(h)) return rc;
+  return decode_impl(h, keys, nullptr, T, evicted, stream);
+}
+
+int kvevict_decode_kv(kvevict_t* h, const uint16_t* keys, const uint16_t* values, int32_t T,
+                      int32_t* evicted, void* stream) {
+  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  if (int rc = with_values(h)) return rc;
+  return decode_impl(h, keys, values, T, evicted, stream);
+}
+
 int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, const uint16_t* decode_keys,
                      int32_t T, int32_t* evicted, void* stream) {
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   if (S < 0 || S > h->cfg.max_prefill || T < 0) return fail(KVEVICT_ERR_INVALID_ARG, "bad S or T");
   if ((S > 0 && !prefill_keys) || (T > 0 && !decode_keys)) return fail(KVEVICT_ERR_INVALID_ARG, "null keys");
   if (h->next_pos != 0 || h->stepped) return fail(KVEVICT_ERR_BAD_STATE, "run_host needs an empty state");
+  if (int rc = keys_only(h)) return rc;
   cudaStream_t s = (cudaStream_t)stream;
   // Staging: two buffers of up to 256 MiB (or one batch's prompt / one step,
   // whichever is larger), so copies of chunk k+1 overlap compute on chunk k.
@@ -562,8 +629,8 @@ int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, cons
                             cudaMemcpyHostToDevice, h->copy_stream));
     KV_CUDA(cudaEventRecord(h->ev_ready[buf], h->copy_stream));
     KV_CUDA(cudaStreamWaitEvent(s, h->ev_ready[buf], 0));
-    const int rc = seq ? enqueue_prefill(h, h->stage[buf], S, nullptr, s)
-                       : enqueue_prompt_scores(h, h->stage[buf], S, S, b0, nb, h->lse2, h->colsum, s);
+    const int rc = seq ? enqueue_prefill(h, h->stage[buf], nullptr, S, nullptr, s)
+                       : enqueue_prompt_scores(h, h->stage[buf], nullptr, S, S, b0, nb, h->lse2, h->colsum, s);
     if (rc != KVEVICT_OK) return rc;
     KV_CUDA(cudaEventRecord(h->ev_free[buf], s));
   }
@@ -578,7 +645,7 @@ int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, cons
     KV_CUDA(cudaEventRecord(h->ev_ready[buf], h->copy_stream));
     KV_CUDA(cudaStreamWaitEvent(s, h->ev_ready[buf], 0));
     for (int t = 0; t < nt; ++t) {
-      const int rc = enqueue_step(h, h->stage[buf] + (size_t)t * per_step,
+      const int rc = enqueue_step(h, h->stage[buf] + (size_t)t * per_step, nullptr,
                                   evicted ? h->ev_stage[buf] + (size_t)t * BLH(h) : nullptr,
                                   h->next_pos, s);
       if (rc != KVEVICT_OK) return rc;
@@ -620,6 +687,26 @@ int kvevict_read_state(kvevict_t* h, int32_t b, int32_t l, int32_t head, uint16_
 int kvevict_flush(kvevict_t* h, void* stream) {
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   return enqueue_flush(h, (cudaStream_t)stream);
+}
+
+int kvevict_read_values(kvevict_t* h, int32_t b, int32_t l, int32_t head, uint16_t* values,
+                        int32_t* n_kept, void* stream) {
+  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  if (int rc = with_values(h)) return rc;
+  if (b < 0 || b >= h->B || l < 0 || l >= h->L || head < 0 || head >= h->H)
+    return fail(KVEVICT_ERR_INVALID_ARG, "row index out of range");
+  cudaStream_t s = (cudaStream_t)stream;
+  int rc = enqueue_flush(h, s);
+  if (rc != KVEVICT_OK) return rc;
+  const LayerInfo& li = h->layers[l];
+  const int n = (int)std::min<int64_t>(h->next_pos, li.budget);
+  const int64_t rem = (int64_t)b * h->H + head;
+  if (values && n > 0)
+    KV_CUDA(cudaMemcpyAsync(values, h->V + (li.row_base + rem * li.cap) * h->D, (size_t)n * h->D * 2,
+                            cudaMemcpyDeviceToHost, s));
+  rc = check_error_word(h, s);
+  if (n_kept) *n_kept = n;
+  return rc;
 }
 
 int kvevict_check(kvevict_t* h, void* stream) {
