@@ -326,16 +326,21 @@ def main():
         for _ in range(args.warmup):
             h.reset(stream=stream)
             h.run_host(pre_h, dec_h, ev_h, stream=stream)
-        t0 = time.perf_counter()
+        e2e_clocks = ClockSampler(device_id())
+        e2e_ms = []
         for _ in range(args.steps):
+            t0 = time.perf_counter()
             h.reset(stream=stream)
             h.run_host(pre_h, dec_h, ev_h, stream=stream)
-        dt = (time.perf_counter() - t0) / args.steps
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+        e2e_clk = e2e_clocks.stop()
+        dt = sum(e2e_ms) / len(e2e_ms) / 1e3
         if not np.array_equal(ev_h.numpy(), ev.cpu().numpy()):
             raise SystemExit("end-to-end run disagrees with the device-resident run")
         h2d = (pre_h.numel() * 2 if pre_h is not None else 0) + dec_h.numel() * 2
         e2e = {"value": world * heads * T / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": ev_h.numel() * 4, "ms_per_step": dt * 1e3}
+               "d2h_bytes_per_step": ev_h.numel() * 4, "ms_per_step": dt * 1e3,
+               "pass_ms": [round(x, 1) for x in e2e_ms], "clocks": e2e_clk}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
