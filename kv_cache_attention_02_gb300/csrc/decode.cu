@@ -241,9 +241,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
   unsigned char* ring = smem + SL.ring;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SL.bars);   // full[kStages], empty[kStages], meta
   float* s_log = reinterpret_cast<float*>(smem + SL.slog);
-  float* s_sc = reinterpret_cast<float*>(smem + SL.msc);          // valid after the stream
-  float* s_g = reinterpret_cast<float*>(smem + SL.mg);
-  int32_t* s_pos = reinterpret_cast<int32_t*>(smem + SL.mpos);
+
   float* redf = reinterpret_cast<float*>(smem + SL.redf);
   int* redi = reinterpret_cast<int*>(smem + SL.redi);
   __shared__ float s_gnew;
@@ -274,6 +272,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
   const int vstart = e_prev + 1;
   const int nvt = (a.V && shift && vstart < nphys) ? (nphys - vstart + kTile - 1) / kTile : 0;
   const int ntot = ntiles + nvt;
+  // With rows short enough for one ring stage per array, scores / Gumbel values /
+  // moving positions travel as three extra ring tiles right behind the keys, so
+  // they are in shared memory by the time the last key tile is done.
+  const bool meta_staged = (size_t)(li.capm + 4) * 4 <= (size_t)G::TILEB;
+  const int n_meta = move_pos ? 3 : 2;
+  float* s_sc = reinterpret_cast<float*>(meta_staged ? ring + (size_t)(ntot % kStages) * G::TILEB
+                                                     : smem + SL.msc);
+  float* s_g = reinterpret_cast<float*>(meta_staged ? ring + (size_t)((ntot + 1) % kStages) * G::TILEB
+                                                    : smem + SL.mg);
+  int32_t* s_pos = reinterpret_cast<int32_t*>(meta_staged ? ring + (size_t)((ntot + 2) % kStages) * G::TILEB
+                                                          : smem + SL.mpos);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -306,19 +315,36 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
         mbar_expect_tx(full(s), bytes);
         bulk_g2s(smem_addr(ring + (size_t)s * G::TILEB), src, bytes, full(s));
       }
-      const int issued = t;
-      bool drained = true;   // every issued tile consumed, so the ring is free
-      for (int u = issued > kStages ? issued - kStages : 0; u < issued && drained; ++u)
-        drained = wait_watch(empty(u % kStages), (uint32_t)((u / kStages) & 1), abort_flag, a.err);
-      if (drained && !*abort_flag && nphys > 0) {
-        // metadata (scores, Gumbel values, moving positions) into the freed ring
+      int issued = t;
+      if (meta_staged && issued == ntot && nphys > 0) {
+        // metadata as three more ring tiles, each landing as soon as a stage frees
         const uint32_t mbytes = (uint32_t)(((nphys + 3) & ~3) * 4);
         const uint32_t pbytes = move_pos ? (uint32_t)(((nphys - pos0 + 3) & ~3) * 4) : 0u;
-        mbar_expect_tx(meta_bar, 2 * mbytes + pbytes);
-        bulk_g2s(smem_addr(s_sc), scg, mbytes, meta_bar);
-        bulk_g2s(smem_addr(s_g), gg, mbytes, meta_bar);
-        if (pbytes) bulk_g2s(smem_addr(s_pos), pg + pos0, pbytes, meta_bar);
-      } else if (!drained) {
+        for (int k = 0; k < n_meta; ++k, ++t) {
+          const int s = t % kStages;
+          if (t >= kStages && !wait_watch(empty(s), (uint32_t)((t / kStages - 1) & 1), abort_flag, a.err))
+            break;
+          const void* src = k == 0 ? (const void*)scg : k == 1 ? (const void*)gg : (const void*)(pg + pos0);
+          const uint32_t bytes = k < 2 ? mbytes : pbytes;
+          mbar_expect_tx(full(s), bytes);
+          bulk_g2s(smem_addr(ring + (size_t)s * G::TILEB), src, bytes, full(s));
+        }
+        issued = t;
+      }
+      bool drained = true;
+      if (!meta_staged) {   // every issued tile consumed, so the ring is free for the metadata
+        for (int u = issued > kStages ? issued - kStages : 0; u < issued && drained; ++u)
+          drained = wait_watch(empty(u % kStages), (uint32_t)((u / kStages) & 1), abort_flag, a.err);
+        if (drained && !*abort_flag && nphys > 0) {
+          const uint32_t mbytes = (uint32_t)(((nphys + 3) & ~3) * 4);
+          const uint32_t pbytes = move_pos ? (uint32_t)(((nphys - pos0 + 3) & ~3) * 4) : 0u;
+          mbar_expect_tx(meta_bar, 2 * mbytes + pbytes);
+          bulk_g2s(smem_addr(s_sc), scg, mbytes, meta_bar);
+          bulk_g2s(smem_addr(s_g), gg, mbytes, meta_bar);
+          if (pbytes) bulk_g2s(smem_addr(s_pos), pg + pos0, pbytes, meta_bar);
+        }
+      }
+      if (!drained || *abort_flag) {
         // give copies still in flight a moment to land before the CTA leaves
         for (int u = issued > kStages ? issued - kStages : 0; u < issued; ++u)
           (void)mbar_wait_bounded(full(u % kStages), (uint32_t)((u / kStages) & 1), 10000000ull);
@@ -430,10 +456,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
 
   // every consumer is done with the stream (and s_log); wait for the metadata
   if (__syncthreads_or(*abort_flag)) return;
-  if (nphys > 0 && warp < kConsumerWarps &&
-      !wait_watch(meta_bar, 0, abort_flag, a.err)) { /* abort flagged */ }
+  if (nphys > 0 && warp < kConsumerWarps) {
+    if (meta_staged) {
+      for (int u = ntot; u < ntot + n_meta; ++u)
+        if (!wait_watch(full(u % kStages), (uint32_t)((u / kStages) & 1), abort_flag, a.err)) break;
+    } else {
+      (void)wait_watch(meta_bar, 0, abort_flag, a.err);
+    }
+  }
   if (__syncthreads_or(*abort_flag)) {
-    if (tid == kConsumers) (void)mbar_wait_bounded(meta_bar, 0, 10000000ull);
+    if (tid == kConsumers && !meta_staged) (void)mbar_wait_bounded(meta_bar, 0, 10000000ull);
     return;
   }
   if (warp == kConsumerWarps) return;   // the producer warp is done
