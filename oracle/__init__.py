@@ -47,39 +47,64 @@ class HeadCfg(ctypes.Structure):
                 ("prefill_mode", i32)]
 
 
-def lib():
+def use_library(path: str | None):
+    """Point this module at another build of the oracle (None: the default).
+
+    Used by the mutation tests, which compile copies of the oracle with a
+    planted mistake and check that the pins catch it. Returns the previous
+    library handle.
+    """
     global _lib
+    prev = _lib
+    _lib = None
+    if path is not None:
+        _bind(ctypes.CDLL(path))
+    return prev
+
+
+def _restore(handle):
+    global _lib
+    _lib = handle
+
+
+def lib():
     if _lib is None:
-        _lib = ctypes.CDLL(build())
-        sig = {
-            "orc_budgets": (ctypes.c_int, [i32, i32, i32, f64, P]),
-            "orc_splitmix64": (u64, [u64]),
-            "orc_gumbel_hash": (u64, [u64, i64, i64, i64]),
-            "orc_gumbel": (ctypes.c_float, [u64, i64, i64, i64]),
-            "orc_gumbel_many": (None, [u64, i64, i64, i64, i64, P]),
-            "orc_tau": (f64, [f64, f64, i64, i64]),
-            "orc_f32_to_f16": (ctypes.c_uint16, [ctypes.c_float]),
-            "orc_f16_to_f64": (f64, [ctypes.c_uint16]),
-            "orc_f32_to_f16_array": (None, [i64, P, P]),
-            "orc_f16_to_f64_array": (None, [i64, P, P]),
-            "orc_rope_consts": (None, [f64, i32, i64, P, P]),
-            "orc_rotate_row": (None, [i32, P, P, P]),
-            "orc_step_accumulate": (i32, [i32, i32, P, P, P, P, P, i64, ctypes.c_float, i32]),
-            "orc_regularised": (None, [i32, P, P, f64, P]),
-            "orc_argmin": (i32, [i32, P, i32, i32]),
-            "orc_evict": (i32, [i32, i32, P, P, P, P, i32, f64]),
-            "orc_prefill_colsum": (None, [i32, i32, P, P]),
-            "orc_prefill_select": (i32, [i32, i32, i32, i32, P, P]),
-            "orc_prefill_lastrow": (None, [i32, i32, P, P]),
-            "orc_prefill_apply": (i32, [i32, i32, P, P, P, P, f64, P, P, P, P]),
-            "orc_run_head": (i32, [P, i32, P, i32, P, P, P, P, P, P]),
-            "orc_run_heads": (i32, [i32, P, i32, P, i32, P, P, i32, P, P, P, P, P, i32]),
-        }
-        for name, (res, args) in sig.items():
-            fn = getattr(_lib, name)
-            fn.restype = res
-            fn.argtypes = args
+        # KVEVICT_ORACLE_LIB: a separately built oracle (the mutation tests use it)
+        _bind(ctypes.CDLL(os.environ.get("KVEVICT_ORACLE_LIB") or build()))
     return _lib
+
+
+def _bind(handle):
+    global _lib
+    _lib = handle
+    sig = {
+        "orc_budgets": (ctypes.c_int, [i32, i32, i32, f64, P]),
+        "orc_splitmix64": (u64, [u64]),
+        "orc_gumbel_hash": (u64, [u64, i64, i64, i64]),
+        "orc_gumbel": (ctypes.c_float, [u64, i64, i64, i64]),
+        "orc_gumbel_many": (None, [u64, i64, i64, i64, i64, P]),
+        "orc_tau": (f64, [f64, f64, i64, i64]),
+        "orc_f32_to_f16": (ctypes.c_uint16, [ctypes.c_float]),
+        "orc_f16_to_f64": (f64, [ctypes.c_uint16]),
+        "orc_f32_to_f16_array": (None, [i64, P, P]),
+        "orc_f16_to_f64_array": (None, [i64, P, P]),
+        "orc_rope_consts": (None, [f64, i32, i64, P, P]),
+        "orc_rotate_row": (None, [i32, P, P, P]),
+        "orc_step_accumulate": (i32, [i32, i32, P, P, P, P, P, i64, ctypes.c_float, i32]),
+        "orc_regularised": (None, [i32, P, P, f64, P]),
+        "orc_argmin": (i32, [i32, P, i32, i32]),
+        "orc_evict": (i32, [i32, i32, P, P, P, P, i32, f64]),
+        "orc_prefill_colsum": (None, [i32, i32, P, P]),
+        "orc_prefill_select": (i32, [i32, i32, i32, i32, P, P]),
+        "orc_prefill_lastrow": (None, [i32, i32, P, P]),
+        "orc_prefill_apply": (i32, [i32, i32, P, P, P, P, f64, P, P, P, P]),
+        "orc_run_head": (i32, [P, i32, P, i32, P, P, P, P, P, P]),
+        "orc_run_heads": (i32, [i32, P, i32, P, i32, P, P, i32, P, P, P, P, P, i32]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(_lib, name)
+        fn.restype = res
+        fn.argtypes = args
 
 
 def _p(a: np.ndarray):
