@@ -148,11 +148,11 @@ __device__ __forceinline__ void warp_argmin(float& r, int& i) {
   }
 }
 
-// Combine two (max, sum of exp(x - max)) pairs.
+// Combine two (max, sum of 2^(x - max)) pairs (logits are kept in base-2 units).
 __device__ __forceinline__ void lse_combine(float& m, float& l, float m2, float l2) {
   const float mn = fmaxf(m, m2);
   if (mn == -INFINITY) return;
-  l = (m == -INFINITY ? 0.f : l * expf(m - mn)) + (m2 == -INFINITY ? 0.f : l2 * expf(m2 - mn));
+  l = (m == -INFINITY ? 0.f : l * exp2f(m - mn)) + (m2 == -INFINITY ? 0.f : l2 * exp2f(m2 - mn));
   m = mn;
 }
 
@@ -373,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
       d += __shfl_xor_sync(0xffffffffu, d, 2);
       d += __shfl_xor_sync(0xffffffffu, d, 4);
       if (tid == 0) {
-        s_log[nphys] = d * a.scale;
-        run_m = d * a.scale;
+        s_log[nphys] = d * a.scale2;
+        run_m = d * a.scale2;
         run_l = 1.f;
       }
     }
@@ -419,13 +419,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
 #pragma unroll
       for (int pass = 0; pass < P; ++pass) {
         if (live[pass] && c == 0) {
-          const float sv = dot[pass] * a.scale;
+          const float sv = dot[pass] * a.scale2;   // base-2 logit
           s_log[Rr[pass]] = sv;
           if (sv > run_m) {
-            run_l = run_l * expf(run_m - sv) + 1.f;
+            run_l = run_l * exp2f(run_m - sv) + 1.f;
             run_m = sv;
           } else {
-            run_l += expf(sv - run_m);
+            run_l += exp2f(sv - run_m);
           }
         }
       }
@@ -474,16 +474,24 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
   block_lse(run_m, run_l, redf);
   const float m = run_m, lsum = run_l;
 
-  // ------------------------------------------------- accumulate + select
+  // ------------------------------- accumulate, write back, select (one pass)
+  // Every source is in shared memory, so each row's new score, its moved
+  // Gumbel value and position go straight to their (compacted) global slots.
   gnew = s_gnew;
+  const float inv_l = 1.f / lsum;
   float best_r = INFINITY;
   int best_R = INT_MAX;
   for (int R = tid; R < NR; R += kConsumers) {
     if (R == e_prev) continue;
-    const float attn = expf(s_log[R] - m) / lsum;
+    const float attn = exp2f(s_log[R] - m) * inv_l;
     const float ns = a.mode ? attn : (R < nphys ? s_sc[R] : 0.f) + attn;   // current-step or cumulative
-    s_log[R] = ns;
-    const int j = R - ((shift && R > e_prev) ? 1 : 0);                    // slot after the append
+    const bool moved = shift && R > e_prev;
+    const int j = R - (moved ? 1 : 0);                                     // slot after compaction
+    scg[j] = ns;
+    if (moved && R < nphys) {
+      gg[j] = s_g[R];
+      pg[j] = s_pos[R - pos0];
+    }
     if (evict && R >= a.n_sink && j < n + 1 - a.recent) {
       const float gv = R < nphys ? s_g[R] : gnew;
       const float r = fmaf(a.tau, gv, ns);
@@ -493,15 +501,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
   int R_e = -1;
   if (evict) R_e = block_argmin(best_r, best_R, redf, redi);
 
-  // ---------------------------------------------------------------- write back
-  for (int R = tid; R < NR; R += kConsumers)
-    if (R != e_prev) scg[R - ((shift && R > e_prev) ? 1 : 0)] = s_log[R];
-  if (move_pos) {
-    for (int R = e_prev + 1 + tid; R < nphys; R += kConsumers) {
-      gg[R - 1] = s_g[R];
-      pg[R - 1] = s_pos[R - pos0];
-    }
-  }
   if (R_e != nphys && tid < kTPR) {   // the new key (and value), unless it was evicted itself
     __half* dst = Kg + (size_t)n * D;
     *reinterpret_cast<Chunk*>(dst + c * CH) = q_lo;

@@ -57,7 +57,7 @@ struct DecodeArgs {
   int mode;                // 0 cumulative scores, 1 current-step scores
   int64_t p;               // absolute position of the incoming key
   float tau;               // tau(p)
-  float scale;             // 1/sqrt(D)
+  float scale2;            // log2(e)/sqrt(D): logits in base-2 units
   uint64_t seed;
 };
 

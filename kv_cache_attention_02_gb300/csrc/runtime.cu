@@ -149,7 +149,7 @@ kvx::DecodeArgs decode_args(kvevict* h, const uint16_t* k_new, const uint16_t* v
   a.mode = h->cfg.score_mode;
   a.p = p;
   a.tau = (float)tau_at(h->cfg, p);
-  a.scale = (float)(1.0 / std::sqrt((double)h->D));
+  a.scale2 = (float)(1.4426950408889634 / std::sqrt((double)h->D));
   a.seed = h->cfg.seed;
   return a;
 }
