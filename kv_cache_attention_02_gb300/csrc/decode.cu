@@ -10,9 +10,13 @@
 // after the evicted one move down one slot, keys re-rotated by -1 RoPE
 // position in fp32 (FUSED METAL KERNEL note) and stored as fp16.
 //
-// Design (GB300): one CTA per cache row. The row's keys stream through a
-// 4-stage shared-memory ring filled by 1-D TMA bulk copies (16 KB tiles),
-// completion tracked by mbarriers. 8 threads share a key row (two 16-byte
+// Design (GB300): persistent CTAs (as many as fit, at most one per row) claim
+// rows from a launch-wide counter, heaviest layers first. In each CTA a
+// scheduler warp claims the next row and stages its header, new key and
+// Gumbel value in shared memory; a producer warp streams the row's keys
+// through a 6-stage shared-memory ring with 1-D TMA bulk copies (16 KB tiles,
+// mbarrier completion) and runs on into the next row while eight consumer
+// warps finish the current one. 8 threads share a key row (two 16-byte
 // chunks each: the pair halves (i, i + D/2) a RoPE rotation needs), so bank
 // access is conflict-free without a swizzle and the dot product reduces with
 // three shuffles. The compaction decided by the previous step is applied to
@@ -30,11 +34,29 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;   // 256 threads work on key rows
-constexpr int kThreads = kConsumers + 32;         // + one TMA producer warp
+constexpr int kProducerWarp = kConsumerWarps;     // issues the TMA copies
+constexpr int kSchedulerWarp = kConsumerWarps + 1;  // claims rows and stages their inputs
+constexpr int kThreads = kConsumers + 64;
 constexpr int kTPR = 8;                           // threads per key row
 constexpr int kRowsPerPass = kConsumers / kTPR;   // 32
 constexpr int kTile = 64;                         // rows per TMA tile
 constexpr int kStages = 6;
+constexpr int kRowQ = 2;                          // the row in work + the one claimed next
+
+// A claimed cache row as the scheduler warp leaves it in shared memory; the
+// new key row (and value row) follow the header.
+struct RowHdr {
+  int64_t kbase;   // first key row of this head in the arena
+  int64_t mbase;   // first metadata entry of this head
+  int head;        // row index (layer-major), or -1: nothing left to claim
+  int n;           // rows kept before the append
+  int e_prev;      // row the previous step evicted but left in place, or -1
+  int budget;
+  int capm;
+  float gnew;      // Gumbel value of the incoming key
+  int pad[2];
+};
+static_assert(sizeof(RowHdr) == 48, "row header layout");
 
 template <int D>
 struct Geo {
@@ -42,29 +64,60 @@ struct Geo {
   static constexpr int HALF = D / 2;
   static constexpr int ROWB = D * 2;
   static constexpr int TILEB = kTile * ROWB;
+  static constexpr int SLOTB = (int)sizeof(RowHdr) + 2 * ROWB;   // header + new key + new value
   using Chunk = typename std::conditional<CH == 8, uint4, uint2>::type;
+  using Word = typename std::conditional<D == 128, uint2, uint32_t>::type;   // a row over 32 lanes
 };
+static_assert(Geo<128>::SLOTB % 16 == 0 && Geo<64>::SLOTB % 16 == 0, "16-byte aligned rows in a slot");
 
 struct SmemLayout {
-  size_t ring, bars, slog, redf, redi, total;
-  size_t msc, mg, mpos;   // score / Gumbel / position copies, placed in the ring after the stream
+  size_t ring, bars, rowq, redf, redi, slog, total;
 };
 
+__host__ __device__ inline size_t meta_stride(int capm) { return ((size_t)(capm + 4) * 4 + 127) / 128 * 128; }
+
 template <int D>
-__host__ __device__ inline SmemLayout decode_layout(int capm) {
+__host__ __device__ inline SmemLayout decode_layout(int capm_max) {
   SmemLayout L{};
   size_t o = 0;
   L.ring = o;  o += (size_t)kStages * Geo<D>::TILEB;
-  L.bars = o;  o += 2 * 8 * (kStages + 1);
-  const size_t arr = ((size_t)(capm + 4) * 4 + 127) / 128 * 128;
-  L.slog = o;  o += arr;
+  L.bars = o;  o += (size_t)8 * (2 * kStages + 2 * kRowQ);
+  o = (o + 127) / 128 * 128;
+  L.rowq = o;  o += (size_t)kRowQ * Geo<D>::SLOTB;
+  o = (o + 127) / 128 * 128;
   L.redf = o;  o += 64 * 4;
   L.redi = o;  o += 64 * 4;
+  L.slog = o;  o += meta_stride(capm_max);
   L.total = o;
-  L.msc = L.ring;
-  L.mg = L.msc + arr;
-  L.mpos = L.mg + arr;
   return L;
+}
+
+// Tile accounting of one row, computed alike by the producer and the consumers.
+struct RowPlan {
+  int nphys;     // stored rows (kept rows + the dead one still in place)
+  int ntiles;    // key tiles
+  int vstart;    // first value row that moves
+  int ntot;      // key + value tiles
+  int nm;        // metadata tiles (the whole ring when the row is too long to stage)
+  int pos0;      // 16-byte aligned start of the moving positions
+  bool move_pos;
+  bool staged;   // metadata as one ring tile per array
+};
+
+template <int D>
+__device__ __forceinline__ RowPlan row_plan(const RowHdr& h, bool values) {
+  RowPlan P;
+  const bool shift = h.e_prev >= 0;
+  P.nphys = h.n + (shift ? 1 : 0);
+  P.ntiles = (P.nphys + kTile - 1) / kTile;
+  P.vstart = h.e_prev + 1;
+  const int nvt = (values && shift && P.vstart < P.nphys) ? (P.nphys - P.vstart + kTile - 1) / kTile : 0;
+  P.ntot = P.ntiles + nvt;
+  P.pos0 = (h.e_prev + 1) & ~3;
+  P.move_pos = shift && h.e_prev + 1 < P.nphys;
+  P.staged = (size_t)(h.capm + 4) * 4 <= (size_t)Geo<D>::TILEB;
+  P.nm = P.nphys == 0 ? 0 : P.staged ? (P.move_pos ? 3 : 2) : kStages;
+  return P;
 }
 
 // Largest metadata stride the ring can host after the stream (scores, Gumbel
@@ -202,6 +255,24 @@ __device__ __forceinline__ void mbar_arrive_cta(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Named barrier 1 over the consumer warps only (the producer and scheduler
+// warps run ahead on their own): a plain sync, and one that ORs a predicate.
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+__device__ __forceinline__ bool consumers_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "n"(kConsumers)
+      : "memory");
+  return r != 0;
+}
+
 // Bounded wait that also gives up as soon as another thread raised the abort flag.
 __device__ __forceinline__ bool wait_watch(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            int* err) {
@@ -227,297 +298,351 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int c = tid & (kTPR - 1);   // chunk index within a row (consumers)
-  const int rg = tid >> 3;          // row within a pass (consumers)
-
-  const int head = blockIdx.x;
-  const int BH = a.B * a.H;
-  const int l = head / BH;
-  const int rem = head - l * BH;
-  const int b = rem / a.H;
-  const int hh = rem - b * a.H;
-  const LayerInfo li = a.layers[l];
-  const SmemLayout SL = decode_layout<D>(li.capm);
+  const SmemLayout SL = decode_layout<D>(a.capm_max);
   unsigned char* ring = smem + SL.ring;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SL.bars);   // full[kStages], empty[kStages], meta
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SL.bars);
+  unsigned char* rowq = smem + SL.rowq;
   float* s_log = reinterpret_cast<float*>(smem + SL.slog);
-
   float* redf = reinterpret_cast<float*>(smem + SL.redf);
   int* redi = reinterpret_cast<int*>(smem + SL.redi);
-  __shared__ float s_gnew;
   __shared__ int s_abort;
   auto full = [&](int s) { return smem_addr(&bars[s]); };
   auto empty = [&](int s) { return smem_addr(&bars[kStages + s]); };
-  const uint32_t meta_bar = smem_addr(&bars[2 * kStages]);
-
-  const int n = (int)(a.p < (int64_t)li.budget ? a.p : (int64_t)li.budget);  // rows before append
-  const int e_prev = a.pend[head];                                          // dead row or -1
-  const int shift = e_prev >= 0 ? 1 : 0;
-  const int nphys = n + shift;                                              // stored rows
-  const int NR = nphys + 1;                                                 // + the new row
-  const bool evict = (n + 1) > li.budget;
-  const int ntiles = (nphys + kTile - 1) / kTile;
-  const int pos0 = (e_prev + 1) & ~3;          // 16-byte aligned start of the moving positions
-  const bool move_pos = shift && e_prev + 1 < nphys;
-
-  __half* Kg = a.K + (li.row_base + (int64_t)rem * li.cap) * D;
-  float* scg = a.score + li.meta_base + (int64_t)rem * li.capm;
-  float* gg = a.gum + li.meta_base + (int64_t)rem * li.capm;
-  int32_t* pg = a.pos + li.meta_base + (int64_t)rem * li.capm;
-  const __half* qg = a.k_new + (((int64_t)b * a.L + l) * a.H + hh) * a.k_stride;
-  __half* Vg = a.V ? a.V + (li.row_base + (int64_t)rem * li.cap) * D : nullptr;
-  const __half* vg = a.V ? a.v_new + (((int64_t)b * a.L + l) * a.H + hh) * a.k_stride : nullptr;
-  // value rows after the dead row move down one slot; they stream through the
-  // ring after the key tiles (no rotation, no scoring)
-  const int vstart = e_prev + 1;
-  const int nvt = (a.V && shift && vstart < nphys) ? (nphys - vstart + kTile - 1) / kTile : 0;
-  const int ntot = ntiles + nvt;
-  // With rows short enough for one ring stage per array, scores / Gumbel values /
-  // moving positions travel as three extra ring tiles right behind the keys, so
-  // they are in shared memory by the time the last key tile is done.
-  const bool meta_staged = (size_t)(li.capm + 4) * 4 <= (size_t)G::TILEB;
-  const int n_meta = move_pos ? 3 : 2;
-  float* s_sc = reinterpret_cast<float*>(meta_staged ? ring + (size_t)(ntot % kStages) * G::TILEB
-                                                     : smem + SL.msc);
-  float* s_g = reinterpret_cast<float*>(meta_staged ? ring + (size_t)((ntot + 1) % kStages) * G::TILEB
-                                                    : smem + SL.mg);
-  int32_t* s_pos = reinterpret_cast<int32_t*>(meta_staged ? ring + (size_t)((ntot + 2) % kStages) * G::TILEB
-                                                          : smem + SL.mpos);
+  auto rfull = [&](int q) { return smem_addr(&bars[2 * kStages + q]); };
+  auto rempty = [&](int q) { return smem_addr(&bars[2 * kStages + kRowQ + q]); };
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), kConsumerWarps);
     }
-    mbar_init(meta_bar, 1);
+    for (int q = 0; q < kRowQ; ++q) {
+      mbar_init(rfull(q), 32);                    // every scheduler lane
+      mbar_init(rempty(q), 1 + kConsumerWarps);   // the producer + each consumer warp
+    }
     fence_mbar_init();
     s_abort = 0;
   }
   __syncthreads();
   volatile int* abort_flag = &s_abort;
+  const bool values = a.V != nullptr;
+  const int BH = a.B * a.H;
 
-  float run_m = -INFINITY, run_l = 0.f;   // this thread's share of the softmax statistics
-  Chunk q_lo{}, q_hi{}, v_lo{}, v_hi{};
-  float gnew = 0.f;
-
-  if (warp == kConsumerWarps) {
+  if (warp == kSchedulerWarp) {
+    // ------------------------------------------------------- row scheduler
+    // Claims rows from the launch-wide counter (heaviest layers first) and
+    // stages each one's header, new key and new value one row ahead.
+    for (int seq = 0;; ++seq) {
+      const int q = seq % kRowQ;
+      if (seq >= kRowQ && !wait_watch(rempty(q), (uint32_t)((seq / kRowQ - 1) & 1), abort_flag, a.err)) break;
+      int row = 0;
+      if (lane == 0) {
+        row = atomicAdd(a.ticket, 1);
+        if (row == a.rows + (int)gridDim.x - 1) atomicExch(a.ticket, 0);   // the launch's last claim
+      }
+      row = __shfl_sync(0xffffffffu, row, 0);
+      unsigned char* slot = rowq + (size_t)q * G::SLOTB;
+      RowHdr* hd = reinterpret_cast<RowHdr*>(slot);
+      if (row < a.rows) {
+        const int l = row / BH;
+        const int rem = row - l * BH;
+        const int b = rem / a.H;
+        const int hh = rem - b * a.H;
+        const int64_t src = (((int64_t)b * a.L + l) * a.H + hh) * a.k_stride;
+        using Word = typename G::Word;   // this lane's share of a new row
+        reinterpret_cast<Word*>(slot + sizeof(RowHdr))[lane] = reinterpret_cast<const Word*>(a.k_new + src)[lane];
+        if (values)
+          reinterpret_cast<Word*>(slot + sizeof(RowHdr) + G::ROWB)[lane] =
+              reinterpret_cast<const Word*>(a.v_new + src)[lane];
+        if (lane == 0) {
+          const LayerInfo li = a.layers[l];
+          hd->kbase = li.row_base + (int64_t)rem * li.cap;
+          hd->mbase = li.meta_base + (int64_t)rem * li.capm;
+          hd->head = row;
+          hd->n = (int)(a.p < (int64_t)li.budget ? a.p : (int64_t)li.budget);
+          hd->e_prev = a.pend[row];
+          hd->budget = li.budget;
+          hd->capm = li.capm;
+          hd->gnew = gumbel_at(a.seed, l, hh, a.p);
+        }
+      } else if (lane == 0) {
+        hd->head = -1;
+      }
+      __syncwarp();
+      mbar_arrive_cta(rfull(q));
+      if (row >= a.rows) break;
+    }
+  } else if (warp == kProducerWarp) {
     // ---------------------------------------------------------- TMA producer
+    // Tile sequence tg runs across rows: a row's key tiles, its value tiles,
+    // then its metadata (scores, Gumbel values, moving positions) as up to
+    // three more tiles, or, for rows too long for that, the whole ring.
     if (lane == 0) {
-      int t = 0;
-      for (; t < ntot; ++t) {
-        const int s = t % kStages;
-        if (t >= kStages && !wait_watch(empty(s), (uint32_t)((t / kStages - 1) & 1), abort_flag, a.err))
-          break;
-        const int r0 = t < ntiles ? t * kTile : vstart + (t - ntiles) * kTile;
-        const int rows = min(kTile, nphys - r0);
-        const uint32_t bytes = (uint32_t)rows * G::ROWB;
-        const __half* src = (t < ntiles ? Kg : Vg) + (size_t)r0 * D;
-        mbar_expect_tx(full(s), bytes);
-        bulk_g2s(smem_addr(ring + (size_t)s * G::TILEB), src, bytes, full(s));
-      }
-      int issued = t;
-      if (meta_staged && issued == ntot && nphys > 0) {
-        // metadata as three more ring tiles, each landing as soon as a stage frees
-        const uint32_t mbytes = (uint32_t)(((nphys + 3) & ~3) * 4);
-        const uint32_t pbytes = move_pos ? (uint32_t)(((nphys - pos0 + 3) & ~3) * 4) : 0u;
-        for (int k = 0; k < n_meta; ++k, ++t) {
-          const int s = t % kStages;
-          if (t >= kStages && !wait_watch(empty(s), (uint32_t)((t / kStages - 1) & 1), abort_flag, a.err))
+      int tg = 0;
+      for (int seq = 0;; ++seq) {
+        const int q = seq % kRowQ;
+        if (!wait_watch(rfull(q), (uint32_t)((seq / kRowQ) & 1), abort_flag, a.err)) break;
+        const RowHdr hd = *reinterpret_cast<const RowHdr*>(rowq + (size_t)q * G::SLOTB);
+        mbar_arrive_cta(rempty(q));
+        if (hd.head < 0) break;
+        const RowPlan P = row_plan<D>(hd, values);
+        const __half* Kg = a.K + hd.kbase * D;
+        const __half* Vg = values ? a.V + hd.kbase * D : nullptr;
+        bool ok = true;
+        for (int t = 0; t < P.ntot; ++t) {
+          const int s = tg % kStages;
+          if (tg >= kStages && !(ok = wait_watch(empty(s), (uint32_t)((tg / kStages - 1) & 1), abort_flag, a.err)))
             break;
-          const void* src = k == 0 ? (const void*)scg : k == 1 ? (const void*)gg : (const void*)(pg + pos0);
-          const uint32_t bytes = k < 2 ? mbytes : pbytes;
+          const int r0 = t < P.ntiles ? t * kTile : P.vstart + (t - P.ntiles) * kTile;
+          const int rows = min(kTile, P.nphys - r0);
+          const uint32_t bytes = (uint32_t)rows * G::ROWB;
           mbar_expect_tx(full(s), bytes);
-          bulk_g2s(smem_addr(ring + (size_t)s * G::TILEB), src, bytes, full(s));
+          bulk_g2s(smem_addr(ring + (size_t)s * G::TILEB), (t < P.ntiles ? Kg : Vg) + (size_t)r0 * D, bytes,
+                   full(s));
+          ++tg;
         }
-        issued = t;
-      }
-      bool drained = true;
-      if (!meta_staged) {   // every issued tile consumed, so the ring is free for the metadata
-        for (int u = issued > kStages ? issued - kStages : 0; u < issued && drained; ++u)
-          drained = wait_watch(empty(u % kStages), (uint32_t)((u / kStages) & 1), abort_flag, a.err);
-        if (drained && !*abort_flag && nphys > 0) {
-          const uint32_t mbytes = (uint32_t)(((nphys + 3) & ~3) * 4);
-          const uint32_t pbytes = move_pos ? (uint32_t)(((nphys - pos0 + 3) & ~3) * 4) : 0u;
-          mbar_expect_tx(meta_bar, 2 * mbytes + pbytes);
-          bulk_g2s(smem_addr(s_sc), scg, mbytes, meta_bar);
-          bulk_g2s(smem_addr(s_g), gg, mbytes, meta_bar);
-          if (pbytes) bulk_g2s(smem_addr(s_pos), pg + pos0, pbytes, meta_bar);
+        if (!ok) break;
+        if (P.nm == 0) continue;
+        const float* scg = a.score + hd.mbase;
+        const float* gg = a.gum + hd.mbase;
+        const int32_t* pg = a.pos + hd.mbase;
+        const uint32_t mbytes = (uint32_t)(((P.nphys + 3) & ~3) * 4);
+        const uint32_t pbytes = P.move_pos ? (uint32_t)(((P.nphys - P.pos0 + 3) & ~3) * 4) : 0u;
+        if (P.staged) {
+          for (int k = 0; k < P.nm; ++k) {
+            const int s = tg % kStages;
+            if (tg >= kStages && !(ok = wait_watch(empty(s), (uint32_t)((tg / kStages - 1) & 1), abort_flag, a.err)))
+              break;
+            const void* src = k == 0 ? (const void*)scg : k == 1 ? (const void*)gg : (const void*)(pg + P.pos0);
+            const uint32_t bytes = k < 2 ? mbytes : pbytes;
+            mbar_expect_tx(full(s), bytes);
+            bulk_g2s(smem_addr(ring + (size_t)s * G::TILEB), src, bytes, full(s));
+            ++tg;
+          }
+        } else {
+          for (int k = 0; k < kStages && ok; ++k) {   // wait until every stage is free
+            const int u = tg + k;
+            if (u >= kStages)
+              ok = wait_watch(empty(u % kStages), (uint32_t)((u / kStages - 1) & 1), abort_flag, a.err);
+          }
+          if (ok) {
+            const size_t arr = meta_stride(hd.capm);
+            const int s0 = tg % kStages;
+            mbar_expect_tx(full(s0), 2 * mbytes + pbytes);
+            bulk_g2s(smem_addr(ring), scg, mbytes, full(s0));
+            bulk_g2s(smem_addr(ring + arr), gg, mbytes, full(s0));
+            if (pbytes) bulk_g2s(smem_addr(ring + 2 * arr), pg + P.pos0, pbytes, full(s0));
+            for (int k = 1; k < kStages; ++k) mbar_arrive_cta(full((tg + k) % kStages));
+            tg += kStages;
+          }
         }
+        if (!ok) break;
       }
-      if (!drained || *abort_flag) {
-        // give copies still in flight a moment to land before the CTA leaves
-        for (int u = issued > kStages ? issued - kStages : 0; u < issued; ++u)
-          (void)mbar_wait_bounded(full(u % kStages), (uint32_t)((u / kStages) & 1), 10000000ull);
-      }
+      // no copy may still be landing in shared memory when the CTA leaves
+      for (int u = tg > kStages ? tg - kStages : 0; u < tg; ++u)
+        (void)mbar_wait_bounded(full(u % kStages), (uint32_t)((u / kStages) & 1), 10000000ull);
     }
   } else {
     // ---------------------------------------------------------- consumers
-    // The proxy query (the new key) and the shift-by-one RoPE constants of this
-    // thread's pair indices stay in registers for the whole pass.
-    q_lo = *reinterpret_cast<const Chunk*>(qg + c * CH);
-    q_hi = *reinterpret_cast<const Chunk*>(qg + HALF + c * CH);
-    if (vg && tid < kTPR) {
-      v_lo = *reinterpret_cast<const Chunk*>(vg + c * CH);
-      v_hi = *reinterpret_cast<const Chunk*>(vg + HALF + c * CH);
-    }
+    const int c = tid & (kTPR - 1);   // chunk index within a row
+    const int rg = tid >> 3;          // row within a pass
+    // shift-by-one RoPE constants of this thread's pair indices, for every row
     float2 rc[CH / 2], rs[CH / 2];
 #pragma unroll
     for (int k = 0; k < CH / 2; ++k) {
       rc[k] = make_float2(a.rope_c[c * CH + 2 * k], a.rope_c[c * CH + 2 * k + 1]);
       rs[k] = make_float2(a.rope_s[c * CH + 2 * k], a.rope_s[c * CH + 2 * k + 1]);
     }
-    if (tid == 32) s_gnew = gumbel_at(a.seed, l, hh, a.p);
-    if (tid < 32) {  // logit of the new row against itself
-      float d = dot_chunks<CH>(q_lo, q_hi, q_lo, q_hi);
-      d += __shfl_xor_sync(0xffffffffu, d, 1);
-      d += __shfl_xor_sync(0xffffffffu, d, 2);
-      d += __shfl_xor_sync(0xffffffffu, d, 4);
-      if (tid == 0) {
-        s_log[nphys] = d * a.scale2;
-        run_m = d * a.scale2;
-        run_l = 1.f;
+    int tg = 0;
+    for (int seq = 0;; ++seq) {
+      const int q = seq % kRowQ;
+      const bool got = wait_watch(rfull(q), (uint32_t)((seq / kRowQ) & 1), abort_flag, a.err);
+      if (consumers_any(!got || *abort_flag)) break;
+      const unsigned char* slot = rowq + (size_t)q * G::SLOTB;
+      const RowHdr hd = *reinterpret_cast<const RowHdr*>(slot);
+      if (hd.head < 0) break;
+      const RowPlan P = row_plan<D>(hd, values);
+      // the proxy query (the new key) stays in registers for the whole row
+      const unsigned char* qs = slot + sizeof(RowHdr);
+      const Chunk q_lo = *reinterpret_cast<const Chunk*>(qs + c * CH * 2);
+      const Chunk q_hi = *reinterpret_cast<const Chunk*>(qs + (HALF + c * CH) * 2);
+      Chunk v_lo{}, v_hi{};
+      if (values && tid < kTPR) {
+        v_lo = *reinterpret_cast<const Chunk*>(qs + G::ROWB + c * CH * 2);
+        v_hi = *reinterpret_cast<const Chunk*>(qs + G::ROWB + (HALF + c * CH) * 2);
       }
-    }
-    for (int t = 0; t < ntiles; ++t) {
-      const int st = t % kStages;
-      if (!wait_watch(full(st), (uint32_t)((t / kStages) & 1), abort_flag, a.err)) break;
-      const unsigned char* tile = ring + (size_t)st * G::TILEB;
-      const int r0 = t * kTile;
-      constexpr int P = kTile / kRowsPerPass;   // rows per thread in this tile
-      Chunk lo[P], hi[P];
-      bool live[P];
-      int Rr[P];
-#pragma unroll
-      for (int pass = 0; pass < P; ++pass) {     // both rows' loads first
-        const int rr = pass * kRowsPerPass + rg;
-        Rr[pass] = r0 + rr;
-        live[pass] = (Rr[pass] < nphys) && (Rr[pass] != e_prev);
-        const unsigned char* row = tile + (size_t)rr * G::ROWB;
-        lo[pass] = *reinterpret_cast<const Chunk*>(row + c * CH * 2);
-        hi[pass] = *reinterpret_cast<const Chunk*>(row + (HALF + c * CH) * 2);
-      }
-      float dot[P];
-#pragma unroll
-      for (int pass = 0; pass < P; ++pass) {
-        if (live[pass] && shift && Rr[pass] > e_prev) {   // apply last step's compaction
-          float2 fa[CH / 2], fb[CH / 2];
-          unpack2<CH>(lo[pass], fa);
-          unpack2<CH>(hi[pass], fb);
-          rotate2<CH>(fa, fb, rc, rs);
-          lo[pass] = pack2<CH>(fa);                      // the stored fp16 values are scored
-          hi[pass] = pack2<CH>(fb);
-          __half* dst = Kg + (size_t)(Rr[pass] - 1) * D;
-          *reinterpret_cast<Chunk*>(dst + c * CH) = lo[pass];
-          *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = hi[pass];
+      const int n = hd.n, e_prev = hd.e_prev, nphys = P.nphys, NR = nphys + 1;
+      const bool shift = e_prev >= 0;
+      const bool evict = (n + 1) > hd.budget;
+      __half* Kg = a.K + hd.kbase * D;
+      __half* Vg = values ? a.V + hd.kbase * D : nullptr;
+      float* scg = a.score + hd.mbase;
+      float* gg = a.gum + hd.mbase;
+      int32_t* pg = a.pos + hd.mbase;
+      const size_t arr = meta_stride(hd.capm);
+      const int um = tg + P.ntot;   // first metadata tile
+      const float* s_sc = reinterpret_cast<const float*>(P.staged ? ring + (size_t)(um % kStages) * G::TILEB : ring);
+      const float* s_g =
+          reinterpret_cast<const float*>(P.staged ? ring + (size_t)((um + 1) % kStages) * G::TILEB : ring + arr);
+      const int32_t* s_pos =
+          reinterpret_cast<const int32_t*>(P.staged ? ring + (size_t)((um + 2) % kStages) * G::TILEB : ring + 2 * arr);
+
+      float run_m = -INFINITY, run_l = 0.f;   // this thread's share of the softmax statistics
+      if (tid < 32) {   // logit of the new row against itself
+        float d = dot_chunks<CH>(q_lo, q_hi, q_lo, q_hi);
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        d += __shfl_xor_sync(0xffffffffu, d, 2);
+        d += __shfl_xor_sync(0xffffffffu, d, 4);
+        if (tid == 0) {
+          s_log[nphys] = d * a.scale2;
+          run_m = d * a.scale2;
+          run_l = 1.f;
         }
-        dot[pass] = live[pass] ? dot_chunks<CH>(lo[pass], hi[pass], q_lo, q_hi) : 0.f;
       }
+      for (int t = 0; t < P.ntiles; ++t) {
+        const int u = tg + t;
+        const int st = u % kStages;
+        if (!wait_watch(full(st), (uint32_t)((u / kStages) & 1), abort_flag, a.err)) break;
+        const unsigned char* tile = ring + (size_t)st * G::TILEB;
+        const int r0 = t * kTile;
+        constexpr int PR = kTile / kRowsPerPass;   // rows per thread in this tile
+        Chunk lo[PR], hi[PR];
+        bool live[PR];
+        int Rr[PR];
 #pragma unroll
-      for (int o = 1; o < kTPR; o <<= 1)
+        for (int pass = 0; pass < PR; ++pass) {     // both rows' loads first
+          const int rr = pass * kRowsPerPass + rg;
+          Rr[pass] = r0 + rr;
+          live[pass] = (Rr[pass] < nphys) && (Rr[pass] != e_prev);
+          const unsigned char* row = tile + (size_t)rr * G::ROWB;
+          lo[pass] = *reinterpret_cast<const Chunk*>(row + c * CH * 2);
+          hi[pass] = *reinterpret_cast<const Chunk*>(row + (HALF + c * CH) * 2);
+        }
+        float dot[PR];
 #pragma unroll
-        for (int pass = 0; pass < P; ++pass) dot[pass] += __shfl_xor_sync(0xffffffffu, dot[pass], o);
+        for (int pass = 0; pass < PR; ++pass) {
+          if (live[pass] && shift && Rr[pass] > e_prev) {   // apply last step's compaction
+            float2 fa[CH / 2], fb[CH / 2];
+            unpack2<CH>(lo[pass], fa);
+            unpack2<CH>(hi[pass], fb);
+            rotate2<CH>(fa, fb, rc, rs);
+            lo[pass] = pack2<CH>(fa);                      // the stored fp16 values are scored
+            hi[pass] = pack2<CH>(fb);
+            __half* dst = Kg + (size_t)(Rr[pass] - 1) * D;
+            *reinterpret_cast<Chunk*>(dst + c * CH) = lo[pass];
+            *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = hi[pass];
+          }
+          dot[pass] = live[pass] ? dot_chunks<CH>(lo[pass], hi[pass], q_lo, q_hi) : 0.f;
+        }
 #pragma unroll
-      for (int pass = 0; pass < P; ++pass) {
-        if (live[pass] && c == 0) {
-          const float sv = dot[pass] * a.scale2;   // base-2 logit
-          s_log[Rr[pass]] = sv;
-          if (sv > run_m) {
-            run_l = run_l * exp2f(run_m - sv) + 1.f;
-            run_m = sv;
-          } else {
-            run_l += exp2f(sv - run_m);
+        for (int o = 1; o < kTPR; o <<= 1)
+#pragma unroll
+          for (int pass = 0; pass < PR; ++pass) dot[pass] += __shfl_xor_sync(0xffffffffu, dot[pass], o);
+#pragma unroll
+        for (int pass = 0; pass < PR; ++pass) {
+          if (live[pass] && c == 0) {
+            const float sv = dot[pass] * a.scale2;   // base-2 logit
+            s_log[Rr[pass]] = sv;
+            if (sv > run_m) {
+              run_l = run_l * exp2f(run_m - sv) + 1.f;
+              run_m = sv;
+            } else {
+              run_l += exp2f(sv - run_m);
+            }
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cta(empty(st));
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cta(empty(st));
-    }
-    for (int t = ntiles; t < ntot && !*abort_flag; ++t) {   // value rows: move down one slot
-      const int st = t % kStages;
-      if (!wait_watch(full(st), (uint32_t)((t / kStages) & 1), abort_flag, a.err)) break;
-      const unsigned char* tile = ring + (size_t)st * G::TILEB;
-      const int r0 = vstart + (t - ntiles) * kTile;
+      for (int t = P.ntiles; t < P.ntot && !*abort_flag; ++t) {   // value rows: move down one slot
+        const int u = tg + t;
+        const int st = u % kStages;
+        if (!wait_watch(full(st), (uint32_t)((u / kStages) & 1), abort_flag, a.err)) break;
+        const unsigned char* tile = ring + (size_t)st * G::TILEB;
+        const int r0 = P.vstart + (t - P.ntiles) * kTile;
 #pragma unroll
-      for (int pass = 0; pass < kTile / kRowsPerPass; ++pass) {
-        const int rr = pass * kRowsPerPass + rg;
-        const int R = r0 + rr;
-        if (R < nphys) {
-          const unsigned char* row = tile + (size_t)rr * G::ROWB;
-          __half* dst = Vg + (size_t)(R - 1) * D;
-          *reinterpret_cast<Chunk*>(dst + c * CH) = *reinterpret_cast<const Chunk*>(row + c * CH * 2);
-          *reinterpret_cast<Chunk*>(dst + HALF + c * CH) =
-              *reinterpret_cast<const Chunk*>(row + (HALF + c * CH) * 2);
+        for (int pass = 0; pass < kTile / kRowsPerPass; ++pass) {
+          const int rr = pass * kRowsPerPass + rg;
+          const int R = r0 + rr;
+          if (R < nphys) {
+            const unsigned char* row = tile + (size_t)rr * G::ROWB;
+            __half* dst = Vg + (size_t)(R - 1) * D;
+            *reinterpret_cast<Chunk*>(dst + c * CH) = *reinterpret_cast<const Chunk*>(row + c * CH * 2);
+            *reinterpret_cast<Chunk*>(dst + HALF + c * CH) =
+                *reinterpret_cast<const Chunk*>(row + (HALF + c * CH) * 2);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cta(empty(st));
+      }
+      for (int k = 0; k < P.nm && !*abort_flag; ++k)   // the metadata
+        if (!wait_watch(full((um + k) % kStages), (uint32_t)(((um + k) / kStages) & 1), abort_flag, a.err)) break;
+      if (consumers_any(*abort_flag)) break;
+
+      // -------------------------------------------------------------- softmax
+      block_lse(run_m, run_l, redf);
+      const float m = run_m;
+      const float inv_l = 1.f / run_l;
+
+      // --------------------------- accumulate, write back, select (one pass)
+      // Every source is in shared memory, so each row's new score, its moved
+      // Gumbel value and position go straight to their (compacted) global slots.
+      const float gnew = hd.gnew;
+      float best_r = INFINITY;
+      int best_R = INT_MAX;
+      for (int R = tid; R < NR; R += kConsumers) {
+        if (R == e_prev) continue;
+        const float attn = exp2f(s_log[R] - m) * inv_l;
+        const float ns = a.mode ? attn : (R < nphys ? s_sc[R] : 0.f) + attn;   // current-step or cumulative
+        const bool moved = shift && R > e_prev;
+        const int j = R - (moved ? 1 : 0);                                     // slot after compaction
+        scg[j] = ns;
+        if (moved && R < nphys) {
+          gg[j] = s_g[R];
+          pg[j] = s_pos[R - P.pos0];
+        }
+        if (evict && R >= a.n_sink && j < n + 1 - a.recent) {
+          const float gv = R < nphys ? s_g[R] : gnew;
+          const float r = fmaf(a.tau, gv, ns);
+          if (r < best_r) { best_r = r; best_R = R; }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cta(empty(st));
-    }
-  }
+      int R_e = -1;
+      if (evict) R_e = block_argmin(best_r, best_R, redf, redi);
 
-  // every consumer is done with the stream (and s_log); wait for the metadata
-  if (__syncthreads_or(*abort_flag)) return;
-  if (nphys > 0 && warp < kConsumerWarps) {
-    if (meta_staged) {
-      for (int u = ntot; u < ntot + n_meta; ++u)
-        if (!wait_watch(full(u % kStages), (uint32_t)((u / kStages) & 1), abort_flag, a.err)) break;
-    } else {
-      (void)wait_watch(meta_bar, 0, abort_flag, a.err);
+      if (R_e != nphys && tid < kTPR) {   // the new key (and value), unless it was evicted itself
+        __half* dst = Kg + (size_t)n * D;
+        *reinterpret_cast<Chunk*>(dst + c * CH) = q_lo;
+        *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = q_hi;
+        if (Vg) {
+          __half* vd = Vg + (size_t)n * D;
+          *reinterpret_cast<Chunk*>(vd + c * CH) = v_lo;
+          *reinterpret_cast<Chunk*>(vd + HALF + c * CH) = v_hi;
+        }
+      }
+      if (tid == 0) {
+        const int head = hd.head;
+        gg[n] = gnew;
+        pg[n] = (int32_t)a.p;
+        const int e_log = evict ? R_e - ((shift && R_e > e_prev) ? 1 : 0) : -1;
+        a.pend[head] = e_log;
+        if (a.evicted) {
+          const int l = head / BH;
+          const int rem = head - l * BH;
+          const int b = rem / a.H;
+          a.evicted[((int64_t)b * a.L + l) * a.H + (rem - b * a.H)] = e_log;
+        }
+        if (evict && (R_e < a.n_sink || R_e > nphys || e_log >= n + 1 - a.recent)) atomicOr(a.err, kErrBadIndex);
+      }
+      // every consumer is done with s_log, the metadata and the reduction
+      // scratch: free the metadata stages and the row's slot
+      consumers_sync();
+      if (lane == 0) {
+        for (int k = 0; k < P.nm; ++k) mbar_arrive_cta(empty((um + k) % kStages));
+        mbar_arrive_cta(rempty(q));
+      }
+      tg = um + P.nm;
     }
-  }
-  if (__syncthreads_or(*abort_flag)) {
-    if (tid == kConsumers && !meta_staged) (void)mbar_wait_bounded(meta_bar, 0, 10000000ull);
-    return;
-  }
-  if (warp == kConsumerWarps) return;   // the producer warp is done
-
-  // ---------------------------------------------------------------- softmax
-  block_lse(run_m, run_l, redf);
-  const float m = run_m, lsum = run_l;
-
-  // ------------------------------- accumulate, write back, select (one pass)
-  // Every source is in shared memory, so each row's new score, its moved
-  // Gumbel value and position go straight to their (compacted) global slots.
-  gnew = s_gnew;
-  const float inv_l = 1.f / lsum;
-  float best_r = INFINITY;
-  int best_R = INT_MAX;
-  for (int R = tid; R < NR; R += kConsumers) {
-    if (R == e_prev) continue;
-    const float attn = exp2f(s_log[R] - m) * inv_l;
-    const float ns = a.mode ? attn : (R < nphys ? s_sc[R] : 0.f) + attn;   // current-step or cumulative
-    const bool moved = shift && R > e_prev;
-    const int j = R - (moved ? 1 : 0);                                     // slot after compaction
-    scg[j] = ns;
-    if (moved && R < nphys) {
-      gg[j] = s_g[R];
-      pg[j] = s_pos[R - pos0];
-    }
-    if (evict && R >= a.n_sink && j < n + 1 - a.recent) {
-      const float gv = R < nphys ? s_g[R] : gnew;
-      const float r = fmaf(a.tau, gv, ns);
-      if (r < best_r) { best_r = r; best_R = R; }
-    }
-  }
-  int R_e = -1;
-  if (evict) R_e = block_argmin(best_r, best_R, redf, redi);
-
-  if (R_e != nphys && tid < kTPR) {   // the new key (and value), unless it was evicted itself
-    __half* dst = Kg + (size_t)n * D;
-    *reinterpret_cast<Chunk*>(dst + c * CH) = q_lo;
-    *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = q_hi;
-    if (Vg) {
-      __half* vd = Vg + (size_t)n * D;
-      *reinterpret_cast<Chunk*>(vd + c * CH) = v_lo;
-      *reinterpret_cast<Chunk*>(vd + HALF + c * CH) = v_hi;
-    }
-  }
-  if (tid == 0) {
-    gg[n] = gnew;
-    pg[n] = (int32_t)a.p;
-    const int e_log = evict ? R_e - ((shift && R_e > e_prev) ? 1 : 0) : -1;
-    a.pend[head] = e_log;
-    if (a.evicted) a.evicted[((int64_t)b * a.L + l) * a.H + hh] = e_log;
-    if (evict && (R_e < a.n_sink || R_e > nphys || e_log >= n + 1 - a.recent)) atomicOr(a.err, kErrBadIndex);
   }
 }
 
@@ -600,12 +725,18 @@ cudaError_t decode_step_setup(int D, size_t smem) {
   return cudaFuncSetAttribute(decode_step_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
-cudaError_t launch_decode_step(const DecodeArgs& a, int D, int heads, size_t smem, cudaStream_t s) {
-  if (heads <= 0) return cudaSuccess;
+cudaError_t decode_step_ctas_per_sm(int D, size_t smem, int* ctas) {
   if (D == 64)
-    decode_step_kernel<64><<<heads, kThreads, smem, s>>>(a);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, decode_step_kernel<64>, kThreads, smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, decode_step_kernel<128>, kThreads, smem);
+}
+
+cudaError_t launch_decode_step(const DecodeArgs& a, int D, int grid, size_t smem, cudaStream_t s) {
+  if (a.rows <= 0 || grid <= 0) return cudaSuccess;
+  if (D == 64)
+    decode_step_kernel<64><<<grid, kThreads, smem, s>>>(a);
   else
-    decode_step_kernel<128><<<heads, kThreads, smem, s>>>(a);
+    decode_step_kernel<128><<<grid, kThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -52,6 +52,9 @@ struct DecodeArgs {
   const float* rope_c;     // [D/2] cos(-w_i) as f32 (shift by -1)
   const float* rope_s;     // [D/2] sin(-w_i)
   int* err;
+  int* ticket;             // row counter CTAs claim rows from; 0 between launches
+  int rows;                // B * L * H
+  int capm_max;            // largest metadata stride (sizes the shared-memory logits)
   int B, L, H, n_sink;
   int recent;              // trailing protected window
   int mode;                // 0 cumulative scores, 1 current-step scores
@@ -115,7 +118,10 @@ struct PrefillSelectArgs {
 // ---------------------------------------------------------------- launchers
 cudaError_t decode_step_setup(int D, size_t smem);
 size_t decode_step_smem(int D, int capm_max);
-cudaError_t launch_decode_step(const DecodeArgs& a, int D, int heads, size_t smem, cudaStream_t s);
+// The decode step runs persistent CTAs (grid = CTAs per SM x SMs, at most one
+// per row) that claim rows from a.ticket until none is left.
+cudaError_t decode_step_ctas_per_sm(int D, size_t smem, int* ctas);
+cudaError_t launch_decode_step(const DecodeArgs& a, int D, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_flush(const FlushArgs& a, int D, int heads, cudaStream_t s);
 
 cudaError_t prefill_setup(int D, int max_prefill);  // bulk-eviction kernel's shared memory

@@ -90,7 +90,7 @@ struct kvevict {
   float* gum = nullptr;
   int32_t* pos = nullptr;
   int32_t* pend = nullptr;
-  int* err = nullptr;
+  int* err = nullptr;       // [0] error word, [1] the decode step's row counter
   float* rope_c = nullptr;  // [max_delta + 1, D/2]; row d = f32(cos(-d * w_i))
   float* rope_s = nullptr;
   int max_delta = 1;
@@ -98,6 +98,7 @@ struct kvevict {
   float* colsum = nullptr;
   int64_t Sp_max = 0;
   size_t decode_smem = 0;
+  int decode_grid = 0;      // persistent decode CTAs
   int64_t next_pos = 0;
   bool stepped = false;
   size_t bytes = 0;
@@ -141,6 +142,9 @@ kvx::DecodeArgs decode_args(kvevict* h, const uint16_t* k_new, const uint16_t* v
   a.rope_c = h->rope_c + (size_t)(h->D / 2);  // row d = 1: shift by -1
   a.rope_s = h->rope_s + (size_t)(h->D / 2);
   a.err = h->err;
+  a.ticket = h->err + 1;
+  a.rows = h->heads;
+  a.capm_max = h->capm_max;
   a.B = h->B;
   a.L = h->L;
   a.H = h->H;
@@ -157,7 +161,7 @@ kvx::DecodeArgs decode_args(kvevict* h, const uint16_t* k_new, const uint16_t* v
 int enqueue_step(kvevict* h, const uint16_t* k_new, const uint16_t* v_new, int32_t* evicted, int64_t p,
                  cudaStream_t s, int64_t k_stride = 0) {
   const kvx::DecodeArgs a = decode_args(h, k_new, v_new, evicted, p, k_stride > 0 ? k_stride : h->D);
-  KV_CUDA(kvx::launch_decode_step(a, h->D, h->heads, h->decode_smem, s));
+  KV_CUDA(kvx::launch_decode_step(a, h->D, h->decode_grid, h->decode_smem, s));
   return KVEVICT_OK;
 }
 
@@ -392,6 +396,13 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
       return bail(fail(KVEVICT_ERR_INVALID_ARG, "layer budget or max_prefill too large for shared memory"));
   }
   KV_CUDA_CREATE(kvx::decode_step_setup(h->D, h->decode_smem));
+  {
+    int per_sm = 0, sms = 0;
+    KV_CUDA_CREATE(kvx::decode_step_ctas_per_sm(h->D, h->decode_smem, &per_sm));
+    KV_CUDA_CREATE(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device));
+    if (per_sm < 1) return bail(fail(KVEVICT_ERR_INVALID_ARG, "decode step does not fit on an SM"));
+    h->decode_grid = (int)std::min<int64_t>((int64_t)per_sm * sms, h->heads);
+  }
   KV_CUDA_CREATE(kvx::prefill_setup(h->D, c.max_prefill));
   KV_CUDA_CREATE(kvx::prefill_tc_setup(h->D));
   KV_CUDA_CREATE(dalloc(&h->d_layers, (size_t)c.n_layers));
@@ -401,7 +412,7 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
   KV_CUDA_CREATE(dalloc(&h->gum, (size_t)meta));
   KV_CUDA_CREATE(dalloc(&h->pos, (size_t)meta));
   KV_CUDA_CREATE(dalloc(&h->pend, (size_t)h->heads));
-  KV_CUDA_CREATE(dalloc(&h->err, 1));
+  KV_CUDA_CREATE(dalloc(&h->err, 2));
   const size_t half = (size_t)h->D / 2;
   KV_CUDA_CREATE(dalloc(&h->rope_c, (size_t)(h->max_delta + 1) * half));
   KV_CUDA_CREATE(dalloc(&h->rope_s, (size_t)(h->max_delta + 1) * half));
@@ -427,7 +438,7 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
   KV_CUDA_CREATE(cudaMemcpy(h->d_layers, h->layers.data(), h->layers.size() * sizeof(LayerInfo),
                             cudaMemcpyHostToDevice));
   KV_CUDA_CREATE(cudaMemsetAsync(h->pend, 0xFF, (size_t)h->heads * 4, s));
-  KV_CUDA_CREATE(cudaMemsetAsync(h->err, 0, sizeof(int), s));
+  KV_CUDA_CREATE(cudaMemsetAsync(h->err, 0, 2 * sizeof(int), s));
   KV_CUDA_CREATE(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
   KV_CUDA_CREATE(cudaStreamSynchronize(s));
 #undef KV_CUDA_CREATE
@@ -447,7 +458,7 @@ int kvevict_reset(kvevict_t* h, void* stream) {
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   cudaStream_t s = (cudaStream_t)stream;
   KV_CUDA(cudaMemsetAsync(h->pend, 0xFF, (size_t)h->heads * 4, s));
-  KV_CUDA(cudaMemsetAsync(h->err, 0, sizeof(int), s));
+  KV_CUDA(cudaMemsetAsync(h->err, 0, 2 * sizeof(int), s));   // error word and row counter
   h->next_pos = 0;
   h->stepped = false;
   return KVEVICT_OK;

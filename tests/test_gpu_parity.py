@@ -272,6 +272,32 @@ def test_gpu_keygen_matches_host(wgpu, wl):
     torch.cuda.empty_cache()
 
 
+# More rows than the decode step runs CTAs (two per SM at most), so every CTA
+# claims several rows in turn; rows of one CTA differ in budget and so in tile
+# count. Rows longer than one ring stage per metadata array (budget above 2044
+# at head_dim 64, above 4092 at head_dim 128) take the whole ring for their
+# metadata, and the mixed case alternates the two layouts within a launch.
+MANY_ROWS = [
+    Workload("many_rows_per_cta", batch=4, n_layers=4, n_kv_heads=40, head_dim=64,
+             avg_budget=24, beta=2.0, n_sink=4, tau_init=1.0, tau_end=2.0, anneal_steps=50,
+             rope_theta=10000.0, gumbel_seed=21, key_seed=21, prefill=30, decode=50),
+    Workload("long_rows_mixed_d64", batch=8, n_layers=2, n_kv_heads=32, head_dim=64,
+             avg_budget=2048, beta=1.5, n_sink=4, tau_init=1.0, tau_end=2.0, anneal_steps=3200,
+             rope_theta=500000.0, gumbel_seed=22, key_seed=22, prefill=3100, decode=24),
+    Workload("long_rows_d128", batch=4, n_layers=2, n_kv_heads=40, head_dim=128,
+             avg_budget=4200, beta=1.0, n_sink=4, tau_init=1.0, tau_end=2.0, anneal_steps=4300,
+             rope_theta=500000.0, gumbel_seed=23, key_seed=23, prefill=4250, decode=16),
+]
+
+
+@pytest.mark.parametrize("wl", MANY_ROWS, ids=lambda w: w.name)
+def test_many_rows_sampled(kvx, wgpu, orc, wl):
+    rows = sampled_rows(wl, k=24 if wl.avg_budget < 1000 else 6, seed=1)
+    res = run_gpu(kvx, wgpu, wl, rows, segments=[wl.decode // 2])
+    reps = compare_rows(orc, wl, rows, *res, threads=8)
+    assert sum(r.evictions for r in reps.values()) > 0
+
+
 FULL = [workloads.KEYFORMER_3B, workloads.PYRAMIDKV, workloads.LATE_RISER_TAU0,
         workloads.LATE_RISER_ANNEAL, workloads.LARGE_CONTEXT]
 
