@@ -3,19 +3,19 @@
 
 One benchmark step is one pass of the whole path over the workload: reset the
 state, score and bulk-evict the prompt (tensor-core column sums + selection),
-run every decode step (one fused kernel launch per step, replayed from a CUDA
-graph) and apply the last step's pending compaction. Keys are seeded
-synthetic fp16 N(0,1) draws, RoPE-rotated at their positions, generated on the
-device before the timed region.
+run every decode step (one kernel launch for all of them: a row's next step
+starts as soon as its own previous step is done) and apply the last step's
+pending compaction. Keys are seeded synthetic fp16 N(0,1) draws, RoPE-rotated
+at their positions, generated on the device before the timed region.
 
 Prints one JSON line. ``value`` = decode head-steps (batch x layers x KV heads
 x decode tokens) per second of whole-pass time, inputs resident in HBM;
 ``e2e`` = the same metric through ``kvevict_run_host`` with the keys in pinned
 host memory and the evicted-slot log copied back, copies inside the timed
-region; ``roofline`` = the decode kernel's algorithmic bytes per launch (from
-the actual eviction log) over its average launch time, against the measured
-HBM copy bandwidth; ``cpu_baseline`` = the fp64 CPU oracle on a bounded sample
-of the same workload on this host's cores.
+region; ``roofline`` = the decode kernel's algorithmic bytes (from the actual
+eviction log) over its time, against the measured HBM copy bandwidth;
+``cpu_baseline`` = the fp64 CPU oracle on a bounded sample of the same
+workload on this host's cores.
 
 ``--impl reference`` times the fp64 CPU oracle itself on a bounded sample of
 the workload (the pages publish no runnable reference implementation).
@@ -356,11 +356,12 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None,
                      "kernel": "decode_step_kernel<128>" if D == 128 else "decode_step_kernel<64>",
-                     "bytes_per_launch": step_bytes / T, "launch_us": launch_ms * 1e3,
+                     "bytes_per_launch": step_bytes, "launch_us": decode_ms * 1e3,
+                     "steps_per_launch": T, "us_per_step": launch_ms * 1e3,
                      "peak_kind": f"of {peak_kind}"},
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "gpu_launches": args.steps * ((3 if wl.prefill else 0) + T + 1),
+        "gpu_launches": args.steps * ((3 if wl.prefill else 0) + 1 + 1),
         "clocks": clk,
         "decode_head_steps_per_s": world * heads * T / (decode_ms / 1e3),
         "prefill_ms": prefill_ms, "decode_ms": decode_ms, "flush_ms": flush_ms,

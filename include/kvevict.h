@@ -165,10 +165,13 @@ int kvevict_read_values(kvevict_t* h, int32_t b, int32_t l, int32_t head, uint16
  * Errors: INVALID_ARG (null k_new), CUDA. */
 int kvevict_step(kvevict_t* h, const uint16_t* k_new, int32_t* evicted, void* stream);
 
-/* T consecutive decode steps, replayed from a CUDA graph that the library
- * captures once per (keys, evicted, T, start position) and caches.
+/* T consecutive decode steps at positions p .. p + T - 1 in one kernel launch:
+ * the same result as T kvevict_step calls. Rows are independent, so a row's
+ * step t + 1 starts as soon as its own step t is done, with no wait for the
+ * rest of the cache between steps.
  * keys: device fp16 [T, B, L, H, D]; evicted: device int32 [T, B, L, H] or NULL.
- * Errors: as kvevict_step; T < 0 is INVALID_ARG, T = 0 does nothing. */
+ * Errors: as kvevict_step; T < 0 is INVALID_ARG, T = 0 does nothing,
+ * BAD_STATE once more than 2^31 - 1 decode steps follow a reset. */
 int kvevict_decode(kvevict_t* h, const uint16_t* keys, int32_t T, int32_t* evicted,
                    void* stream);
 

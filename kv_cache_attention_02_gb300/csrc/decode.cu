@@ -10,8 +10,12 @@
 // after the evicted one move down one slot, keys re-rotated by -1 RoPE
 // position in fp32 (FUSED METAL KERNEL note) and stored as fp16.
 //
-// Design (GB300): persistent CTAs (as many as fit, at most one per row) claim
-// rows from a launch-wide counter, heaviest layers first. In each CTA a
+// Design (GB300): one launch runs T decode steps. Persistent CTAs (as many as
+// fit, at most one per row) claim (step, row) pairs from a launch-wide
+// counter, heaviest layers first within a step; rows are independent, so a
+// row's next step starts as soon as its own previous step has been published
+// (a per-row release/acquire counter), never waiting for the whole cache to
+// finish a step. In each CTA a
 // scheduler warp claims the next row and stages its header, new key and
 // Gumbel value in shared memory; a producer warp streams the row's keys
 // through a 6-stage shared-memory ring with 1-D TMA bulk copies (16 KB tiles,
@@ -43,20 +47,22 @@ constexpr int kTile = 64;                         // rows per TMA tile
 constexpr int kStages = 6;
 constexpr int kRowQ = 2;                          // the row in work + the one claimed next
 
-// A claimed cache row as the scheduler warp leaves it in shared memory; the
-// new key row (and value row) follow the header.
+// A claimed (step, row) pair as the scheduler warp leaves it in shared memory;
+// the new key row (and value row) follow the header.
 struct RowHdr {
   int64_t kbase;   // first key row of this head in the arena
   int64_t mbase;   // first metadata entry of this head
+  int64_t p;       // absolute position of the incoming key
   int head;        // row index (layer-major), or -1: nothing left to claim
+  int t;           // step within the launch
   int n;           // rows kept before the append
   int e_prev;      // row the previous step evicted but left in place, or -1
   int budget;
   int capm;
   float gnew;      // Gumbel value of the incoming key
-  int pad[2];
+  float tau;       // tau(p)
 };
-static_assert(sizeof(RowHdr) == 48, "row header layout");
+static_assert(sizeof(RowHdr) == 56, "row header layout");
 
 template <int D>
 struct Geo {
@@ -64,7 +70,7 @@ struct Geo {
   static constexpr int HALF = D / 2;
   static constexpr int ROWB = D * 2;
   static constexpr int TILEB = kTile * ROWB;
-  static constexpr int SLOTB = (int)sizeof(RowHdr) + 2 * ROWB;   // header + new key + new value
+  static constexpr int SLOTB = 64 + 2 * ROWB;   // header (padded) + new key + new value
   using Chunk = typename std::conditional<CH == 8, uint4, uint2>::type;
   using Word = typename std::conditional<D == 128, uint2, uint32_t>::type;   // a row over 32 lanes
 };
@@ -255,6 +261,29 @@ __device__ __forceinline__ void mbar_arrive_cta(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int32_t* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Order this thread's later async-proxy (TMA) reads of global memory after the
+// generic-proxy writes it has synchronised with.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// tau(p) = tau_init + min(p, A) (tau_end - tau_init) / A, each operation in
+// fp64 and the result rounded to f32.
+__device__ __forceinline__ float tau_at(const DecodeArgs& a, int64_t p) {
+  if (a.anneal_steps <= 0 || a.tau_init == a.tau_end) return a.tau_init;
+  const int64_t t = p < 0 ? 0 : (p < a.anneal_steps ? p : (int64_t)a.anneal_steps);
+  const double span = __dsub_rn((double)a.tau_end, (double)a.tau_init);
+  return (float)__dadd_rn((double)a.tau_init, __ddiv_rn(__dmul_rn((double)t, span), (double)a.anneal_steps));
+}
+
 // Named barrier 1 over the consumer warps only (the producer and scheduler
 // warps run ahead on their own): a plain sync, and one that ORs a predicate.
 __device__ __forceinline__ void consumers_sync() {
@@ -330,47 +359,73 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
 
   if (warp == kSchedulerWarp) {
     // ------------------------------------------------------- row scheduler
-    // Claims rows from the launch-wide counter (heaviest layers first) and
-    // stages each one's header, new key and new value one row ahead.
+    // Claims (step, row) pairs from the launch-wide counter in order (step by
+    // step, heaviest layers first within a step) and stages each one's header,
+    // new key and new value one row ahead. A row's step t first waits until
+    // the row's step t - 1 has been published (in practice long done: the row
+    // was claimed a whole step of the cache earlier).
+    const unsigned long long total = (unsigned long long)a.T * (unsigned long long)a.rows;
     for (int seq = 0;; ++seq) {
       const int q = seq % kRowQ;
       if (seq >= kRowQ && !wait_watch(rempty(q), (uint32_t)((seq / kRowQ - 1) & 1), abort_flag, a.err)) break;
-      int row = 0;
+      unsigned long long k = 0;
       if (lane == 0) {
-        row = atomicAdd(a.ticket, 1);
-        if (row == a.rows + (int)gridDim.x - 1) atomicExch(a.ticket, 0);   // the launch's last claim
+        k = atomicAdd(a.ticket, 1ull);
+        if (k == total + gridDim.x - 1) atomicExch(a.ticket, 0ull);   // the launch's last claim
       }
-      row = __shfl_sync(0xffffffffu, row, 0);
+      k = __shfl_sync(0xffffffffu, k, 0);
       unsigned char* slot = rowq + (size_t)q * G::SLOTB;
       RowHdr* hd = reinterpret_cast<RowHdr*>(slot);
-      if (row < a.rows) {
+      const bool claimed = k < total;
+      bool ready = true;
+      if (claimed) {
+        const int t = (int)(k / (unsigned long long)a.rows);
+        const int row = (int)(k - (unsigned long long)t * a.rows);
         const int l = row / BH;
         const int rem = row - l * BH;
         const int b = rem / a.H;
         const int hh = rem - b * a.H;
-        const int64_t src = (((int64_t)b * a.L + l) * a.H + hh) * a.k_stride;
+        const int64_t src = (int64_t)t * a.k_step + (((int64_t)b * a.L + l) * a.H + hh) * a.k_stride;
         using Word = typename G::Word;   // this lane's share of a new row
-        reinterpret_cast<Word*>(slot + sizeof(RowHdr))[lane] = reinterpret_cast<const Word*>(a.k_new + src)[lane];
+        reinterpret_cast<Word*>(slot + 64)[lane] = reinterpret_cast<const Word*>(a.k_new + src)[lane];
         if (values)
-          reinterpret_cast<Word*>(slot + sizeof(RowHdr) + G::ROWB)[lane] =
-              reinterpret_cast<const Word*>(a.v_new + src)[lane];
+          reinterpret_cast<Word*>(slot + 64 + G::ROWB)[lane] = reinterpret_cast<const Word*>(a.v_new + src)[lane];
         if (lane == 0) {
+          // step t of this row needs step t - 1 applied (by whichever CTA ran it)
+          if (t > 0 && ld_acquire(a.done + row) < a.s0 + t) {
+            const uint64_t t0 = global_timer_ns();
+            while (ld_acquire(a.done + row) < a.s0 + t) {
+              if (*abort_flag) { ready = false; break; }
+              if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(a.err, kErrWaitTimeout);
+                ready = false;
+                break;
+              }
+            }
+          }
           const LayerInfo li = a.layers[l];
+          const int64_t p = a.p0 + t;
           hd->kbase = li.row_base + (int64_t)rem * li.cap;
           hd->mbase = li.meta_base + (int64_t)rem * li.capm;
+          hd->p = p;
           hd->head = row;
-          hd->n = (int)(a.p < (int64_t)li.budget ? a.p : (int64_t)li.budget);
-          hd->e_prev = a.pend[row];
+          hd->t = t;
+          hd->n = (int)(p < (int64_t)li.budget ? p : (int64_t)li.budget);
+          hd->e_prev = __ldcg(a.pend + row);
           hd->budget = li.budget;
           hd->capm = li.capm;
-          hd->gnew = gumbel_at(a.seed, l, hh, a.p);
+          hd->gnew = gumbel_at(a.seed, l, hh, p);
+          hd->tau = tau_at(a, p);
         }
+        ready = __shfl_sync(0xffffffffu, ready, 0);
       } else if (lane == 0) {
         hd->head = -1;
       }
+      if (!ready) break;   // aborted while waiting: the other roles see the flag
       __syncwarp();
       mbar_arrive_cta(rfull(q));
-      if (row >= a.rows) break;
+      if (!claimed) break;
     }
   } else if (warp == kProducerWarp) {
     // ---------------------------------------------------------- TMA producer
@@ -388,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
         const RowPlan P = row_plan<D>(hd, values);
         const __half* Kg = a.K + hd.kbase * D;
         const __half* Vg = values ? a.V + hd.kbase * D : nullptr;
+        if (hd.t > 0) fence_proxy_async_global();   // the row's previous step was written in this launch
         bool ok = true;
         for (int t = 0; t < P.ntot; ++t) {
           const int s = tg % kStages;
@@ -463,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
       if (hd.head < 0) break;
       const RowPlan P = row_plan<D>(hd, values);
       // the proxy query (the new key) stays in registers for the whole row
-      const unsigned char* qs = slot + sizeof(RowHdr);
+      const unsigned char* qs = slot + 64;
       const Chunk q_lo = *reinterpret_cast<const Chunk*>(qs + c * CH * 2);
       const Chunk q_hi = *reinterpret_cast<const Chunk*>(qs + (HALF + c * CH) * 2);
       Chunk v_lo{}, v_hi{};
@@ -603,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
         }
         if (evict && R >= a.n_sink && j < n + 1 - a.recent) {
           const float gv = R < nphys ? s_g[R] : gnew;
-          const float r = fmaf(a.tau, gv, ns);
+          const float r = fmaf(hd.tau, gv, ns);
           if (r < best_r) { best_r = r; best_R = R; }
         }
       }
@@ -623,20 +679,25 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
       if (tid == 0) {
         const int head = hd.head;
         gg[n] = gnew;
-        pg[n] = (int32_t)a.p;
+        pg[n] = (int32_t)hd.p;
         const int e_log = evict ? R_e - ((shift && R_e > e_prev) ? 1 : 0) : -1;
         a.pend[head] = e_log;
         if (a.evicted) {
           const int l = head / BH;
           const int rem = head - l * BH;
           const int b = rem / a.H;
-          a.evicted[((int64_t)b * a.L + l) * a.H + (rem - b * a.H)] = e_log;
+          a.evicted[hd.t * a.ev_step + ((int64_t)b * a.L + l) * a.H + (rem - b * a.H)] = e_log;
         }
         if (evict && (R_e < a.n_sink || R_e > nphys || e_log >= n + 1 - a.recent)) atomicOr(a.err, kErrBadIndex);
       }
       // every consumer is done with s_log, the metadata and the reduction
-      // scratch: free the metadata stages and the row's slot
+      // scratch, and every write of this row's step has been issued: publish
+      // the step, free the metadata stages and the row's slot
       consumers_sync();
+      if (tid == 0) {
+        __threadfence();
+        st_release(a.done + hd.head, a.s0 + hd.t + 1);
+      }
       if (lane == 0) {
         for (int k = 0; k < P.nm; ++k) mbar_arrive_cta(empty((um + k) % kStages));
         mbar_arrive_cta(rempty(q));

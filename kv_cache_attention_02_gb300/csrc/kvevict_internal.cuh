@@ -38,28 +38,34 @@ struct LayerInfo {
 };
 
 struct DecodeArgs {
-  const __half* k_new;     // [B, L, H] rows of D, user layout, k_stride elements apart
-  int64_t k_stride;        // D for a decode step; S*D when keys come from a prompt buffer
-  const __half* v_new;     // value rows, same layout and stride as k_new (null: keys only)
+  const __half* k_new;     // step t's key of row (b, l, h) at k_new + t*k_step + ((b*L + l)*H + h)*k_stride
+  int64_t k_stride;        // D for decode keys; S*D when keys come from a prompt buffer
+  int64_t k_step;          // elements between consecutive steps' keys (B*L*H*D, or D in a prompt buffer)
+  const __half* v_new;     // value rows, same layout and strides as k_new (null: keys only)
   __half* K;
   __half* V;               // value arena, same layout as K (null: keys only)
   float* score;
   float* gum;
   int32_t* pos;
   int32_t* pend;
-  int32_t* evicted;        // [B, L, H] user layout, or null
+  int32_t* done;           // [rows] decode steps applied to each row since reset
+  int32_t* evicted;        // [T, B, L, H] user layout (ev_step apart), or null
+  int64_t ev_step;
   const LayerInfo* layers;
   const float* rope_c;     // [D/2] cos(-w_i) as f32 (shift by -1)
   const float* rope_s;     // [D/2] sin(-w_i)
   int* err;
-  int* ticket;             // row counter CTAs claim rows from; 0 between launches
+  unsigned long long* ticket;   // (step, row) claims; 0 between launches
   int rows;                // B * L * H
+  int T;                   // decode steps in this launch
+  int s0;                  // steps already applied to every row before this launch
   int capm_max;            // largest metadata stride (sizes the shared-memory logits)
   int B, L, H, n_sink;
   int recent;              // trailing protected window
   int mode;                // 0 cumulative scores, 1 current-step scores
-  int64_t p;               // absolute position of the incoming key
-  float tau;               // tau(p)
+  int64_t p0;              // absolute position of step 0's key
+  float tau_init, tau_end; // tau(p) = tau_init + min(p, A) * (tau_end - tau_init) / A, in fp64
+  int anneal_steps;        // A (0: constant tau_init)
   float scale2;            // log2(e)/sqrt(D): logits in base-2 units
   uint64_t seed;
 };
@@ -118,8 +124,9 @@ struct PrefillSelectArgs {
 // ---------------------------------------------------------------- launchers
 cudaError_t decode_step_setup(int D, size_t smem);
 size_t decode_step_smem(int D, int capm_max);
-// The decode step runs persistent CTAs (grid = CTAs per SM x SMs, at most one
-// per row) that claim rows from a.ticket until none is left.
+// One launch runs a.T decode steps: persistent CTAs (grid = CTAs per SM x SMs,
+// at most one per row) claim (step, row) pairs in order from a.ticket; a row's
+// step t waits until a.done[row] shows step t - 1 applied.
 cudaError_t decode_step_ctas_per_sm(int D, size_t smem, int* ctas);
 cudaError_t launch_decode_step(const DecodeArgs& a, int D, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_flush(const FlushArgs& a, int D, int heads, cudaStream_t s);

@@ -5,6 +5,7 @@
 #include "kvevict.h"
 #include "kvevict_internal.cuh"
 
+#include <climits>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -90,7 +91,8 @@ struct kvevict {
   float* gum = nullptr;
   int32_t* pos = nullptr;
   int32_t* pend = nullptr;
-  int* err = nullptr;       // [0] error word, [1] the decode step's row counter
+  int* err = nullptr;
+  unsigned long long* ticket = nullptr;   // the decode step's (step, row) claim counter
   float* rope_c = nullptr;  // [max_delta + 1, D/2]; row d = f32(cos(-d * w_i))
   float* rope_s = nullptr;
   int max_delta = 1;
@@ -102,14 +104,8 @@ struct kvevict {
   int64_t next_pos = 0;
   bool stepped = false;
   size_t bytes = 0;
-  // cached CUDA graph of a run of decode steps
-  cudaStream_t cap_stream = nullptr;
-  cudaGraphExec_t gexec = nullptr;
-  const void* g_keys = nullptr;
-  const void* g_vals = nullptr;
-  const void* g_ev = nullptr;
-  int g_T = -1;
-  int64_t g_p0 = -1;
+  int32_t* done = nullptr;  // [heads] decode steps applied to each row since reset
+  int64_t dsteps = 0;       // decode steps launched since reset (every row takes each one)
   // host pipeline staging
   cudaStream_t copy_stream = nullptr;
   cudaEvent_t ev_ready[2] = {nullptr, nullptr};
@@ -125,25 +121,35 @@ namespace {
 int64_t BLHD(const kvevict* h) { return (int64_t)h->B * h->L * h->H * h->D; }
 int64_t BLH(const kvevict* h) { return (int64_t)h->B * h->L * h->H; }
 
-kvx::DecodeArgs decode_args(kvevict* h, const uint16_t* k_new, const uint16_t* v_new,
-                            int32_t* evicted, int64_t p, int64_t k_stride) {
+// T decode steps in one launch. Step t's key (value) of row (b, l, h) is at
+// keys + t*k_step + ((b*L + l)*H + h)*k_stride; its evicted slot goes to
+// evicted + t*B*L*H + (b*L + l)*H + h. The first step's position is p0.
+int enqueue_steps(kvevict* h, const uint16_t* keys, const uint16_t* values, int64_t k_stride, int64_t k_step,
+                  int32_t* evicted, int32_t T, int64_t p0, cudaStream_t s) {
+  if (T <= 0) return KVEVICT_OK;
+  if (h->dsteps + T > INT32_MAX) return fail(KVEVICT_ERR_BAD_STATE, "too many decode steps since reset");
   kvx::DecodeArgs a{};
-  a.k_new = reinterpret_cast<const __half*>(k_new);
+  a.k_new = reinterpret_cast<const __half*>(keys);
   a.k_stride = k_stride;
-  a.v_new = reinterpret_cast<const __half*>(v_new);
+  a.k_step = k_step;
+  a.v_new = reinterpret_cast<const __half*>(values);
   a.K = h->K;
   a.V = h->V;
   a.score = h->score;
   a.gum = h->gum;
   a.pos = h->pos;
   a.pend = h->pend;
+  a.done = h->done;
   a.evicted = evicted;
+  a.ev_step = BLH(h);
   a.layers = h->d_layers;
   a.rope_c = h->rope_c + (size_t)(h->D / 2);  // row d = 1: shift by -1
   a.rope_s = h->rope_s + (size_t)(h->D / 2);
   a.err = h->err;
-  a.ticket = h->err + 1;
+  a.ticket = h->ticket;
   a.rows = h->heads;
+  a.T = T;
+  a.s0 = (int)h->dsteps;
   a.capm_max = h->capm_max;
   a.B = h->B;
   a.L = h->L;
@@ -151,17 +157,14 @@ kvx::DecodeArgs decode_args(kvevict* h, const uint16_t* k_new, const uint16_t* v
   a.n_sink = h->cfg.n_sink;
   a.recent = h->cfg.recent;
   a.mode = h->cfg.score_mode;
-  a.p = p;
-  a.tau = (float)tau_at(h->cfg, p);
+  a.p0 = p0;
+  a.tau_init = h->cfg.tau_init;
+  a.tau_end = h->cfg.tau_end;
+  a.anneal_steps = h->cfg.anneal_steps;
   a.scale2 = (float)(1.4426950408889634 / std::sqrt((double)h->D));
   a.seed = h->cfg.seed;
-  return a;
-}
-
-int enqueue_step(kvevict* h, const uint16_t* k_new, const uint16_t* v_new, int32_t* evicted, int64_t p,
-                 cudaStream_t s, int64_t k_stride = 0) {
-  const kvx::DecodeArgs a = decode_args(h, k_new, v_new, evicted, p, k_stride > 0 ? k_stride : h->D);
   KV_CUDA(kvx::launch_decode_step(a, h->D, h->decode_grid, h->decode_smem, s));
+  h->dsteps += T;
   return KVEVICT_OK;
 }
 
@@ -228,11 +231,9 @@ int enqueue_prefill(kvevict* h, const uint16_t* keys, const uint16_t* values, in
   int rc = enqueue_prompt_scores(h, keys, values, S0, S, 0, h->B, h->lse2, h->colsum, s);
   if (rc != KVEVICT_OK) return rc;
   if (evicted) KV_CUDA(cudaMemsetAsync(evicted, 0xFF, (size_t)S0 * BLH(h) * 4, s));
-  for (int32_t t = S0; t < S; ++t) {
-    rc = enqueue_step(h, keys + (size_t)t * h->D, values ? values + (size_t)t * h->D : nullptr,
-                      evicted ? evicted + (size_t)t * BLH(h) : nullptr, t, s, (int64_t)S * h->D);
-    if (rc != KVEVICT_OK) return rc;
-  }
+  if (S0 < S)
+    return enqueue_steps(h, keys + (size_t)S0 * h->D, values ? values + (size_t)S0 * h->D : nullptr,
+                         (int64_t)S * h->D, h->D, evicted ? evicted + (size_t)S0 * BLH(h) : nullptr, S - S0, S0, s);
   return KVEVICT_OK;
 }
 
@@ -269,8 +270,6 @@ int check_error_word(kvevict* h, cudaStream_t s) {
 }
 
 void free_all(kvevict* h) {
-  if (h->gexec) cudaGraphExecDestroy(h->gexec);
-  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
   for (int i = 0; i < 2; ++i) {
     if (h->ev_ready[i]) cudaEventDestroy(h->ev_ready[i]);
@@ -285,7 +284,9 @@ void free_all(kvevict* h) {
   cudaFree(h->gum);
   cudaFree(h->pos);
   cudaFree(h->pend);
+  cudaFree(h->done);
   cudaFree(h->err);
+  cudaFree(h->ticket);
   cudaFree(h->rope_c);
   cudaFree(h->rope_s);
   cudaFree(h->lse2);
@@ -412,7 +413,9 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
   KV_CUDA_CREATE(dalloc(&h->gum, (size_t)meta));
   KV_CUDA_CREATE(dalloc(&h->pos, (size_t)meta));
   KV_CUDA_CREATE(dalloc(&h->pend, (size_t)h->heads));
-  KV_CUDA_CREATE(dalloc(&h->err, 2));
+  KV_CUDA_CREATE(dalloc(&h->done, (size_t)h->heads));
+  KV_CUDA_CREATE(dalloc(&h->err, 1));
+  KV_CUDA_CREATE(dalloc(&h->ticket, 1));
   const size_t half = (size_t)h->D / 2;
   KV_CUDA_CREATE(dalloc(&h->rope_c, (size_t)(h->max_delta + 1) * half));
   KV_CUDA_CREATE(dalloc(&h->rope_s, (size_t)(h->max_delta + 1) * half));
@@ -438,8 +441,9 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
   KV_CUDA_CREATE(cudaMemcpy(h->d_layers, h->layers.data(), h->layers.size() * sizeof(LayerInfo),
                             cudaMemcpyHostToDevice));
   KV_CUDA_CREATE(cudaMemsetAsync(h->pend, 0xFF, (size_t)h->heads * 4, s));
-  KV_CUDA_CREATE(cudaMemsetAsync(h->err, 0, 2 * sizeof(int), s));
-  KV_CUDA_CREATE(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
+  KV_CUDA_CREATE(cudaMemsetAsync(h->done, 0, (size_t)h->heads * 4, s));
+  KV_CUDA_CREATE(cudaMemsetAsync(h->err, 0, sizeof(int), s));
+  KV_CUDA_CREATE(cudaMemsetAsync(h->ticket, 0, sizeof(unsigned long long), s));
   KV_CUDA_CREATE(cudaStreamSynchronize(s));
 #undef KV_CUDA_CREATE
   *out = h;
@@ -458,8 +462,11 @@ int kvevict_reset(kvevict_t* h, void* stream) {
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   cudaStream_t s = (cudaStream_t)stream;
   KV_CUDA(cudaMemsetAsync(h->pend, 0xFF, (size_t)h->heads * 4, s));
-  KV_CUDA(cudaMemsetAsync(h->err, 0, 2 * sizeof(int), s));   // error word and row counter
+  KV_CUDA(cudaMemsetAsync(h->done, 0, (size_t)h->heads * 4, s));
+  KV_CUDA(cudaMemsetAsync(h->err, 0, sizeof(int), s));
+  KV_CUDA(cudaMemsetAsync(h->ticket, 0, sizeof(unsigned long long), s));   // left set by an aborted launch
   h->next_pos = 0;
+  h->dsteps = 0;
   h->stepped = false;
   return KVEVICT_OK;
 }
@@ -482,7 +489,7 @@ int prefill_impl(kvevict* h, const uint16_t* keys, const uint16_t* values, int32
 
 int step_impl(kvevict* h, const uint16_t* k_new, const uint16_t* v_new, int32_t* evicted, void* stream) {
   if (!k_new || (h->V && !v_new)) return fail(KVEVICT_ERR_INVALID_ARG, "k_new or v_new is null");
-  const int rc = enqueue_step(h, k_new, v_new, evicted, h->next_pos, (cudaStream_t)stream);
+  const int rc = enqueue_steps(h, k_new, v_new, h->D, 0, evicted, 1, h->next_pos, (cudaStream_t)stream);
   if (rc != KVEVICT_OK) return rc;
   h->next_pos += 1;
   h->stepped = true;
@@ -494,38 +501,8 @@ int decode_impl(kvevict* h, const uint16_t* keys, const uint16_t* values, int32_
   if (T < 0) return fail(KVEVICT_ERR_INVALID_ARG, "T must be >= 0");
   if (T == 0) return KVEVICT_OK;
   if (!keys || (h->V && !values)) return fail(KVEVICT_ERR_INVALID_ARG, "keys or values is null");
-  const bool hit = h->gexec && h->g_keys == keys && h->g_vals == values && h->g_ev == evicted &&
-                   h->g_T == T && h->g_p0 == h->next_pos;
-  if (!hit) {
-    if (h->gexec) {
-      cudaGraphExecDestroy(h->gexec);
-      h->gexec = nullptr;
-    }
-    KV_CUDA(cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
-    int rc = KVEVICT_OK;
-    for (int32_t t = 0; t < T && rc == KVEVICT_OK; ++t)
-      rc = enqueue_step(h, keys + (size_t)t * BLHD(h), values ? values + (size_t)t * BLHD(h) : nullptr,
-                        evicted ? evicted + (size_t)t * BLH(h) : nullptr, h->next_pos + t, h->cap_stream);
-    cudaGraph_t graph = nullptr;
-    const cudaError_t ce = cudaStreamEndCapture(h->cap_stream, &graph);
-    if (rc != KVEVICT_OK) {
-      if (graph) cudaGraphDestroy(graph);
-      return rc;
-    }
-    if (ce != cudaSuccess) return fail(KVEVICT_ERR_CUDA, std::string("stream capture: ") + cudaGetErrorString(ce));
-    const cudaError_t ie = cudaGraphInstantiate(&h->gexec, graph, 0);
-    cudaGraphDestroy(graph);
-    if (ie != cudaSuccess) {
-      h->gexec = nullptr;
-      return fail(KVEVICT_ERR_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(ie));
-    }
-    h->g_keys = keys;
-    h->g_vals = values;
-    h->g_ev = evicted;
-    h->g_T = T;
-    h->g_p0 = h->next_pos;
-  }
-  KV_CUDA(cudaGraphLaunch(h->gexec, (cudaStream_t)stream));
+  const int rc = enqueue_steps(h, keys, values, h->D, BLHD(h), evicted, T, h->next_pos, (cudaStream_t)stream);
+  if (rc != KVEVICT_OK) return rc;
   h->next_pos += T;
   h->stepped = true;
   return KVEVICT_OK;
@@ -655,14 +632,11 @@ int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, cons
                             cudaMemcpyHostToDevice, h->copy_stream));
     KV_CUDA(cudaEventRecord(h->ev_ready[buf], h->copy_stream));
     KV_CUDA(cudaStreamWaitEvent(s, h->ev_ready[buf], 0));
-    for (int t = 0; t < nt; ++t) {
-      const int rc = enqueue_step(h, h->stage[buf] + (size_t)t * per_step, nullptr,
-                                  evicted ? h->ev_stage[buf] + (size_t)t * BLH(h) : nullptr,
-                                  h->next_pos, s);
-      if (rc != KVEVICT_OK) return rc;
-      h->next_pos += 1;
-      h->stepped = true;
-    }
+    const int rc = enqueue_steps(h, h->stage[buf], nullptr, h->D, (int64_t)per_step,
+                                 evicted ? h->ev_stage[buf] : nullptr, nt, h->next_pos, s);
+    if (rc != KVEVICT_OK) return rc;
+    h->next_pos += nt;
+    h->stepped = true;
     if (evicted)
       KV_CUDA(cudaMemcpyAsync(evicted + (size_t)t0 * BLH(h), h->ev_stage[buf], (size_t)nt * BLH(h) * 4,
                               cudaMemcpyDeviceToHost, s));

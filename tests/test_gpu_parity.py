@@ -2,8 +2,8 @@
 
 Small configurations compare every cache row over the whole run (several TMA
 tiles, ragged tails, every edge case the method has); the five full-size
-workloads run exactly as the benchmark launches them (prompt, then one CUDA
-graph of all decode steps) and compare sampled rows over the whole run.
+workloads run exactly as the benchmark launches them (prompt, then one launch
+of all decode steps) and compare sampled rows over the whole run.
 """
 import concurrent.futures as cf
 
@@ -42,7 +42,7 @@ def head_params(orc, wl, l, h):
                           mode=wl.score_mode, prefill_mode=wl.prefill_mode)
 
 
-def run_gpu(kvx, wgpu, wl, rows, segments=None, mode="graph"):
+def run_gpu(kvx, wgpu, wl, rows, segments=None, mode="multi"):
     """Run the workload on the GPU; read back the sampled rows."""
     h = kvx.from_workload(wl)
     pre, dec = wgpu.device_inputs(wl)
@@ -59,7 +59,7 @@ def run_gpu(kvx, wgpu, wl, rows, segments=None, mode="graph"):
     bounds = sorted(set([0, T] + list(segments or [])))
     checkpoints = {r: {} for r in rows}
     for t0, t1 in zip(bounds, bounds[1:]):
-        if mode == "graph":
+        if mode == "multi":
             h.decode(dec[t0:t1], ev[t0:t1])
         else:
             for t in range(t0, t1):
@@ -162,10 +162,10 @@ def test_small_all_rows(kvx, wgpu, orc, wl):
     assert sum(r.evictions for r in reps.values()) > 0
 
 
-def test_step_path_equals_graph_path(kvx, wgpu):
+def test_step_path_equals_multistep_path(kvx, wgpu):
     wl = SMALL[0]
     rows = all_rows(wl)
-    a = run_gpu(kvx, wgpu, wl, rows, mode="graph")
+    a = run_gpu(kvx, wgpu, wl, rows, mode="multi")
     b = run_gpu(kvx, wgpu, wl, rows, mode="step")
     assert np.array_equal(a[1], b[1])
     for r in rows:

@@ -27,7 +27,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
-@pytest.mark.parametrize("path", ["graph", "step"])
+@pytest.mark.parametrize("path", ["multi", "step"])
 def test_values_follow_positions(wl, path):
     import kv_cache_attention_02_gb300 as kvx
     from workloads import gpu as wgpu
@@ -45,7 +45,7 @@ def test_values_follow_positions(wl, path):
         if pre is not None:
             pev = torch.full((wl.prefill,) + shape[1:], -7, dtype=torch.int32, device="cuda")
             h.prefill(pre, pev, values=vpre)
-        if path == "graph":
+        if path == "multi":
             h.decode(dec, ev, values=vdec)
         else:
             for t in range(wl.decode):
