@@ -78,6 +78,26 @@ def config_of(wl, budgets):
             "late_riser": wl.late_riser}
 
 
+def profiled_traffic(wl, kernel_src):
+    """DRAM bytes (read + write) of one decode launch on this workload, from the
+    committed ncu launch list, or None when the kernel source has changed since
+    the counters were taken or the workload differs."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "large_context_launch_list.md")) as f:
+            lines = [ln.split() for ln in f if ln.startswith("traffic ")]
+        with open(kernel_src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    for ln in lines:
+        kv = dict(x.split("=", 1) for x in ln[3:] if "=" in x)
+        if (ln[2] == wl.name and wl is workloads.ALL.get(wl.name) and int(kv.get("steps", -1)) == wl.decode
+                and kv.get("decode_cu_sha256") == sha):
+            return int(kv["bytes"])
+    return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -249,6 +269,7 @@ def main():
     B, L, H, D, T = wl.batch, wl.n_layers, wl.n_kv_heads, wl.head_dim, wl.decode
     pre, dec = wgpu.device_inputs(wl)
     h = kvx.from_workload(wl)
+    state_bytes = h.device_bytes()   # the cache arena and prompt scratch (before any host staging)
     budgets = h.budgets
     ev = torch.empty((T, B, L, H), dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
@@ -351,10 +372,12 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {**config_of(wl, budgets), "l2": "flushed (256 MB write) before every timed pass",
-                   "state_gb": round(h.device_bytes() / 1e9, 3),
+                   "state_gb": round(state_bytes / 1e9, 3),
                    "input_gb": round(heads * wl.positions * D * 2 / 1e9, 3)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": profiled_traffic(wl, os.path.join(ROOT, "kv_cache_attention_02_gb300", "csrc",
+                                                                  "decode.cu")),
                      "kernel": "decode_step_kernel<128>" if D == 128 else "decode_step_kernel<64>",
                      "bytes_per_launch": step_bytes, "launch_us": decode_ms * 1e3,
                      "steps_per_launch": T, "us_per_step": launch_ms * 1e3,
