@@ -176,6 +176,40 @@ def run_reference(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- ranks
+def init_ranks(backend="nccl"):
+    """(world, rank, dist or None) from the torchrun environment. One process
+    per GPU; every rank runs its own replica of the workload (cache rows are
+    independent, so nothing is exchanged on the data path)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend)
+    return world, rank, dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(x, dist, device="cuda"):
+    """The slowest rank's value: the job is done when every replica is."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, units_per_rank, seconds):
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -256,14 +290,8 @@ def main():
     import kv_cache_attention_02_gb300 as kvx
     from workloads import gpu as wgpu
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    world, rank, dist = init_ranks("nccl")
 
     wl = workload_of(args)
     B, L, H, D, T = wl.batch, wl.n_layers, wl.n_kv_heads, wl.head_dim, wl.decode
@@ -303,29 +331,23 @@ def main():
     # pass starts cold, whatever the size of the workload's state.
     flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     clocks = ClockSampler(device_id())
-    if dist:
-        dist.barrier()
+    barrier(dist)
     torch.cuda.synchronize()
     for _ in range(args.steps):
         flush_buf.fill_(1)
         one_pass(mark=True)
     torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
+    barrier(dist)
     clk = clocks.stop()
     h.check(stream=stream)
 
     pass_ms = [a.elapsed_time(d) for a, _, _, d in ev_marks]
-    ms_per_step = sum(pass_ms) / len(pass_ms)
-    if dist:
-        tt = torch.tensor([ms_per_step], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_per_step = float(tt.item())
+    ms_per_step = max_over_ranks(sum(pass_ms) / len(pass_ms), dist)
     prefill_ms = statistics.median(a.elapsed_time(b) for a, b, _, _ in ev_marks)
     decode_ms = statistics.median(b.elapsed_time(c) for _, b, c, _ in ev_marks)
     flush_ms = statistics.median(c.elapsed_time(d) for _, _, c, d in ev_marks)
     heads = B * L * H
-    value = world * heads * T / (ms_per_step / 1e3)
+    value = job_rate(world, heads * T, ms_per_step / 1e3)
 
     # decode kernel roofline: algorithmic bytes per launch over average launch time
     launch_ms = decode_ms / T
@@ -349,17 +371,19 @@ def main():
             h.run_host(pre_h, dec_h, ev_h, stream=stream)
         e2e_clocks = ClockSampler(device_id())
         e2e_ms = []
+        barrier(dist)
         for _ in range(args.steps):
             t0 = time.perf_counter()
             h.reset(stream=stream)
             h.run_host(pre_h, dec_h, ev_h, stream=stream)
             e2e_ms.append((time.perf_counter() - t0) * 1e3)
+        barrier(dist)
         e2e_clk = e2e_clocks.stop()
-        dt = sum(e2e_ms) / len(e2e_ms) / 1e3
+        dt = max_over_ranks(sum(e2e_ms) / len(e2e_ms) / 1e3, dist)
         if not np.array_equal(ev_h.numpy(), ev.cpu().numpy()):
             raise SystemExit("end-to-end run disagrees with the device-resident run")
         h2d = (pre_h.numel() * 2 if pre_h is not None else 0) + dec_h.numel() * 2
-        e2e = {"value": world * heads * T / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_rate(world, heads * T, dt), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": ev_h.numel() * 4, "ms_per_step": dt * 1e3,
                "pass_ms": [round(x, 1) for x in e2e_ms], "clocks": e2e_clk}
 
