@@ -122,21 +122,26 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-  uint32_t r[32];
+// 64 consecutive fp32 accumulator columns of this warp's 32 TMEM lanes (one
+// per thread), waited for before returning.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+  uint32_t r[64];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+  for (int e = 0; e < 64; ++e) v[e] = __uint_as_float(r[e]);
+}
+
+// 2^x on the MUFU (ex2.approx: relative error below 2^-22; subnormal results
+// flush to zero, which only drops terms below 2^-126 from a sum of terms <= 1).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -284,43 +289,70 @@ __global__ void __launch_bounds__(kTCThreads, 1)
     for (int k = 0; k < nblk; ++k) {
       const int b = k & 1;
       const int colB0 = (first + k) * kTB;
-      if (COLSUM) lse_s[b * kTB + et] = lse_h[colB0 + et];   // this tile's 128 query lse values
+      if (COLSUM) lse_s[b * kTB + et] = -lse_h[colB0 + et];   // this tile's 128 query -lse values
       const bool ok = wait_or_abort(acc_full(b), (uint32_t)((k / 2) & 1), abort_flag, a.err);
       if (epi_any(!ok)) break;                    // also publishes lse_s to the warpgroup
       tc_fence_after();
       const bool full_tile = COLSUM ? (colB0 > ablk * kTB + kTB - 1 && colB0 + kTB <= S)
                                     : (colB0 + kTB - 1 < ablk * kTB && ablk * kTB + kTB <= S);
+      // Interior tiles take no mask; the scale rides in one FMA per element
+      // (max over the raw dot products: scale2 > 0 keeps the order).
 #pragma unroll 1
-      for (int c = 0; c < kTB / 32; ++c) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * kTB + c * 32), v);
+      for (int c = 0; c < kTB / 64; ++c) {
+        float v[64];
+        tmem_ld64(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * kTB + c * 64), v);
+        const int c0 = colB0 + c * 64;
         if (!COLSUM) {
-          float cm = -INFINITY;
+          if (!full_tile) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int j = colB0 + c * 32 + e;
-            const float s = v[e] * a.scale2;
-            v[e] = (full_tile || (j <= rowA && j < S)) ? s : -INFINITY;
-            cm = fmaxf(cm, v[e]);
+            for (int e = 0; e < 64; ++e) {
+              const int j = c0 + e;
+              v[e] = (j <= rowA && j < S) ? v[e] : -INFINITY;
+            }
           }
-          const float mn = fmaxf(run_m, cm);
-          if (mn != -INFINITY) {
-            float sum = 0.f;
+          float cm = v[0];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) sum += exp2f(v[e] - mn);
-            run_l = run_l * exp2f(run_m - mn) + sum;
+          for (int e = 1; e < 64; ++e) cm = fmaxf(cm, v[e]);
+          if (cm != -INFINITY) {
+            const float mn = fmaxf(run_m, cm * a.scale2);
+            const float nm = -mn;
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 64; e += 2) {
+              s0 += ex2(fmaf(v[e], a.scale2, nm));
+              s1 += ex2(fmaf(v[e + 1], a.scale2, nm));
+            }
+            run_l = run_l * ex2(run_m - mn) + (s0 + s1);
             run_m = mn;
           }
         } else {
-          const float* lt = lse_s + b * kTB + c * 32;
-          float sum = 0.f;
+          float nl[64];   // -lse2 of the tile's queries (16-byte broadcast loads)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int i = colB0 + c * 32 + e;
-            const float p = exp2f(v[e] * a.scale2 - lt[e]);
-            sum += (full_tile || (i >= rowA && i < S)) ? p : 0.f;
+          for (int e = 0; e < 64; e += 4) {
+            const float4 t = *reinterpret_cast<const float4*>(lse_s + b * kTB + c * 64 + e);
+            nl[e] = t.x;
+            nl[e + 1] = t.y;
+            nl[e + 2] = t.z;
+            nl[e + 3] = t.w;
           }
-          csum += sum;
+          float s0 = 0.f, s1 = 0.f;
+          if (full_tile) {
+#pragma unroll
+            for (int e = 0; e < 64; e += 2) {
+              s0 += ex2(fmaf(v[e], a.scale2, nl[e]));
+              s1 += ex2(fmaf(v[e + 1], a.scale2, nl[e + 1]));
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 64; e += 2) {
+              const int i = c0 + e;
+              const float p0 = ex2(fmaf(v[e], a.scale2, nl[e]));
+              const float p1 = ex2(fmaf(v[e + 1], a.scale2, nl[e + 1]));
+              s0 += (i >= rowA && i < S) ? p0 : 0.f;
+              s1 += (i + 1 >= rowA && i + 1 < S) ? p1 : 0.f;
+            }
+          }
+          csum += s0 + s1;
         }
       }
       tc_fence_before();
