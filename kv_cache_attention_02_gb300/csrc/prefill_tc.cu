@@ -11,14 +11,16 @@
 //            transposed product (TMEM lanes = key j, columns = query i);
 //            colsum_j = sum_{i>=j} 2^(s_ij - lse2_i), summed per lane in registers.
 //
-// Roles in a 192-thread CTA:
+// Roles in a 320-thread CTA (two per SM):
 //   warp 0      one thread issues TMA loads (3-D tensor map [heads, S, D], 128-byte
 //               swizzle, two 64-element halves per 128-row tile) into a 2-stage ring;
 //   warp 1      allocates 256 TMEM columns (two 128x128 fp32 accumulators) and one
 //               thread issues tcgen05.mma (M=128, N=128, K=16, f16 in, f32 out);
 //               tcgen05.commit releases the smem stage and publishes the accumulator;
-//   warps 2..5  the epilogue warpgroup: tcgen05.ld 32 columns at a time, mask, exp2,
-//               online row max/sum (pass 1) or masked column sums (pass 2).
+//   warps 2..9  two epilogue warpgroups, one per accumulator (alternate tiles):
+//               tcgen05.ld, causal mask on diagonal tiles only, exp2 on the MUFU,
+//               online row max/sum (pass 1) or column sums (pass 2); the two
+//               combine their per-row results at the end.
 // Every mbarrier wait is bounded; on expiry the CTA sets the error word, drains
 // and frees its TMEM.
 #include "kvevict_internal.cuh"
@@ -32,7 +34,7 @@ namespace kvx {
 namespace {
 
 constexpr int kTB = 128;           // tile rows (M) and columns (N)
-constexpr int kTCThreads = 192;
+constexpr int kTCThreads = 320;   // TMA warp, MMA warp, two epilogue warpgroups
 constexpr int kStagesTC = 2;
 constexpr int kTmemCols = 256;     // two 128-column fp32 accumulators
 
@@ -45,7 +47,7 @@ struct TCGeo {
 };
 
 struct TCSmem {
-  size_t a, b, lse, bars, tmem, total;
+  size_t a, b, lse, comb, bars, tmem, total;
 };
 
 template <int D>
@@ -55,6 +57,7 @@ __host__ __device__ constexpr TCSmem tc_layout() {
   L.a = o;    o += TCGeo<D>::TILEB;
   L.b = o;    o += (size_t)kStagesTC * TCGeo<D>::TILEB;
   L.lse = o;  o += 2 * kTB * sizeof(float);
+  L.comb = o; o += 2 * kTB * sizeof(float);
   L.bars = o; o += 16 * 8;
   L.tmem = o; o += 16;
   L.total = o + 1024;  // slack to align the tile region to 1024 bytes
@@ -122,6 +125,19 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 
+// 32 consecutive fp32 accumulator columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]);
+}
+
 // 64 consecutive fp32 accumulator columns of this warp's 32 TMEM lanes (one
 // per thread), waited for before returning.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
@@ -148,22 +164,40 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ void epi_bar() {  // named barrier for the 128 epilogue threads
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+// Named barriers: 1 + w for the 128 threads of epilogue warpgroup w, 3 for
+// both warpgroups (256 threads).
+__device__ __forceinline__ void wg_bar(int w) {
+  if (w == 0)
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+  else
+    asm volatile("bar.sync 2, 128;" ::: "memory");
+}
+__device__ __forceinline__ void epi_all_bar() {
+  asm volatile("bar.sync 3, 256;" ::: "memory");
 }
 
-// Named barrier for the 128 epilogue threads that also ORs a predicate across
-// them, so the whole warpgroup leaves its loop together.
-__device__ __forceinline__ bool epi_any(bool pred) {
+// Barrier of warpgroup w that also ORs a predicate across it, so the whole
+// warpgroup leaves its loop together.
+__device__ __forceinline__ bool wg_any(int w, bool pred) {
   uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, 128, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)pred)
-      : "memory");
+  if (w == 0)
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 2, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
   return r != 0;
 }
 
@@ -184,7 +218,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 }
 
 template <int D, bool COLSUM>
-__global__ void __launch_bounds__(kTCThreads, 1)
+__global__ void __launch_bounds__(kTCThreads, 2)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const PrefillScoreArgs a) {
   using G = TCGeo<D>;
   constexpr TCSmem SL = tc_layout<D>();
@@ -279,92 +313,110 @@ __global__ void __launch_bounds__(kTCThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue warpgroup
-    const int q = warp & 3;                       // TMEM lane quadrant of this warp
+    // ------------------------------------------------------------ epilogue warpgroups
+    // Warpgroup wg (warps 2..5: 0, warps 6..9: 1) owns TMEM accumulator wg and
+    // the tiles k = wg, wg + 2, ...; the two combine their per-row results at
+    // the end. A warp reaches TMEM lanes 32 * (warp % 4) .. + 31.
+    const int wg = (warp - 2) >> 2;
+    const int b = wg;
+    const int q = warp & 3;
     const int r = q * 32 + lane;                  // tile row = TMEM lane
     const int rowA = ablk * kTB + r;              // query row i (pass 1) / key row j (pass 2)
-    const int et = tid - 64;                      // 0..127 within the epilogue
+    const int et = tid - 64 - wg * kTB;           // 0..127 within the warpgroup
     const float* lse_h = a.lse2 + (size_t)head * a.Sp;
+    constexpr int CW = COLSUM ? 32 : 64;          // accumulator columns per TMEM read
     float run_m = -INFINITY, run_l = 0.f, csum = 0.f;
-    for (int k = 0; k < nblk; ++k) {
-      const int b = k & 1;
+    for (int k = wg; k < nblk; k += 2) {
       const int colB0 = (first + k) * kTB;
       if (COLSUM) lse_s[b * kTB + et] = -lse_h[colB0 + et];   // this tile's 128 query -lse values
       const bool ok = wait_or_abort(acc_full(b), (uint32_t)((k / 2) & 1), abort_flag, a.err);
-      if (epi_any(!ok)) break;                    // also publishes lse_s to the warpgroup
+      if (wg_any(wg, !ok)) break;                 // also publishes lse_s to the warpgroup
       tc_fence_after();
       const bool full_tile = COLSUM ? (colB0 > ablk * kTB + kTB - 1 && colB0 + kTB <= S)
                                     : (colB0 + kTB - 1 < ablk * kTB && ablk * kTB + kTB <= S);
       // Interior tiles take no mask; the scale rides in one FMA per element
       // (max over the raw dot products: scale2 > 0 keeps the order).
 #pragma unroll 1
-      for (int c = 0; c < kTB / 64; ++c) {
-        float v[64];
-        tmem_ld64(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * kTB + c * 64), v);
-        const int c0 = colB0 + c * 64;
+      for (int c = 0; c < kTB / CW; ++c) {
+        float v[CW];
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * kTB + c * CW);
+        if (CW == 64)
+          tmem_ld64(taddr, v);
+        else
+          tmem_ld32(taddr, v);
+        const int c0 = colB0 + c * CW;
         if (!COLSUM) {
           if (!full_tile) {
 #pragma unroll
-            for (int e = 0; e < 64; ++e) {
+            for (int e = 0; e < CW; ++e) {
               const int j = c0 + e;
               v[e] = (j <= rowA && j < S) ? v[e] : -INFINITY;
             }
           }
-          float cm = v[0];
+          float m8[8];   // independent max chains
 #pragma unroll
-          for (int e = 1; e < 64; ++e) cm = fmaxf(cm, v[e]);
+          for (int e = 0; e < 8; ++e) m8[e] = v[e];
+#pragma unroll
+          for (int e = 8; e < CW; ++e) m8[e & 7] = fmaxf(m8[e & 7], v[e]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) m8[e] = fmaxf(m8[e], m8[e + 4]);
+          const float cm = fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3]));
           if (cm != -INFINITY) {
             const float mn = fmaxf(run_m, cm * a.scale2);
             const float nm = -mn;
-            float s0 = 0.f, s1 = 0.f;
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < 64; e += 2) {
-              s0 += ex2(fmaf(v[e], a.scale2, nm));
-              s1 += ex2(fmaf(v[e + 1], a.scale2, nm));
-            }
-            run_l = run_l * ex2(run_m - mn) + (s0 + s1);
+            for (int e = 0; e < CW; ++e) s4[e & 3] += ex2(fmaf(v[e], a.scale2, nm));
+            run_l = run_l * ex2(run_m - mn) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
             run_m = mn;
           }
         } else {
-          float nl[64];   // -lse2 of the tile's queries (16-byte broadcast loads)
+          float nl[CW];   // -lse2 of the chunk's queries (16-byte broadcast loads)
 #pragma unroll
-          for (int e = 0; e < 64; e += 4) {
-            const float4 t = *reinterpret_cast<const float4*>(lse_s + b * kTB + c * 64 + e);
+          for (int e = 0; e < CW; e += 4) {
+            const float4 t = *reinterpret_cast<const float4*>(lse_s + b * kTB + c * CW + e);
             nl[e] = t.x;
             nl[e + 1] = t.y;
             nl[e + 2] = t.z;
             nl[e + 3] = t.w;
           }
-          float s0 = 0.f, s1 = 0.f;
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
           if (full_tile) {
 #pragma unroll
-            for (int e = 0; e < 64; e += 2) {
-              s0 += ex2(fmaf(v[e], a.scale2, nl[e]));
-              s1 += ex2(fmaf(v[e + 1], a.scale2, nl[e + 1]));
-            }
+            for (int e = 0; e < CW; ++e) s4[e & 3] += ex2(fmaf(v[e], a.scale2, nl[e]));
           } else {
 #pragma unroll
-            for (int e = 0; e < 64; e += 2) {
+            for (int e = 0; e < CW; ++e) {
               const int i = c0 + e;
-              const float p0 = ex2(fmaf(v[e], a.scale2, nl[e]));
-              const float p1 = ex2(fmaf(v[e + 1], a.scale2, nl[e + 1]));
-              s0 += (i >= rowA && i < S) ? p0 : 0.f;
-              s1 += (i + 1 >= rowA && i + 1 < S) ? p1 : 0.f;
+              const float p = ex2(fmaf(v[e], a.scale2, nl[e]));
+              s4[e & 3] += (i >= rowA && i < S) ? p : 0.f;
             }
           }
-          csum += s0 + s1;
+          csum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty(b));
-      if (COLSUM) epi_bar();                      // lse_s[b] free for tile k+2
+      if (COLSUM) wg_bar(wg);                     // lse_s[b] free for this warpgroup's next tile
     }
-    if (!*abort_flag && rowA < S) {
-      if (COLSUM)
-        a.colsum[(size_t)head * a.Sp + rowA] = csum;
-      else
-        a.lse2[(size_t)head * a.Sp + rowA] = run_m + log2f(run_l);
+    // warpgroup 1 hands its per-row results to warpgroup 0
+    float* comb = reinterpret_cast<float*>(smem + SL.comb);
+    if (wg == 1) {
+      comb[r] = COLSUM ? csum : run_m;
+      comb[kTB + r] = run_l;
+    }
+    epi_all_bar();
+    if (wg == 0 && !*abort_flag && rowA < S) {
+      if (COLSUM) {
+        a.colsum[(size_t)head * a.Sp + rowA] = csum + comb[r];
+      } else {
+        const float m2 = comb[r], l2 = comb[kTB + r];
+        const float m = fmaxf(run_m, m2);
+        const float l = (run_m == -INFINITY ? 0.f : run_l * exp2f(run_m - m)) +
+                        (m2 == -INFINITY ? 0.f : l2 * exp2f(m2 - m));
+        a.lse2[(size_t)head * a.Sp + rowA] = m + log2f(l);
+      }
     }
   }
 
