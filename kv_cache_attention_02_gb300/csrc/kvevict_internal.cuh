@@ -101,7 +101,7 @@ struct PrefillSelectArgs {
   const __half* values;    // same layout as keys (null: keys only)
   __half* V;               // value arena (null: keys only)
   const float* colsum;     // [heads, S]
-  float* gscr;             // [heads, S] scratch for the prompt's Gumbel values
+  const float* gtab;       // [L*H, Sp] Gumbel value of (layer, head, prompt position)
   __half* K;
   float* score;
   float* gum;
@@ -140,6 +140,9 @@ size_t prefill_tc_smem(int D);
 cudaError_t prefill_tc_setup(int D);
 cudaError_t launch_prefill_tc(const PrefillScoreArgs& a, int D, cudaStream_t s);
 size_t prefill_select_smem(int S);
+// The prompt's Gumbel values depend on (layer, head, position) only, not on the
+// batch row: out[(l*H + h)*Sp + j] = g(seed, l, h, j) for j < S.
+cudaError_t launch_gumbel_table(uint64_t seed, int L, int H, int S, int Sp, float* out, cudaStream_t s);
 cudaError_t launch_prefill_select(const PrefillSelectArgs& a, int D, int heads, cudaStream_t s);
 
 // ---------------------------------------------------------------- device helpers

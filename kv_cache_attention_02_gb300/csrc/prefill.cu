@@ -3,11 +3,13 @@
 //
 // Bulk eviction (reading: the whole prompt is scored first, then the S - b
 // non-sink rows with the lowest (score + tau(S-1) * gumbel, slot) go at once):
-// one CTA per cache row sorts (r, slot) keys in shared memory, scans the
+// one CTA per cache row sorts (r, slot) keys in shared memory (the Gumbel
+// values come from a per-prompt (layer, head, position) table), scans the
 // survivors' new slots and writes them, each key re-rotated by
 // (new slot - old slot) RoPE positions in fp32 and stored as fp16.
 #include "kvevict_internal.cuh"
 
+#include <algorithm>
 #include <cfloat>
 
 namespace kvx {
@@ -45,12 +47,9 @@ __global__ void __launch_bounds__(kSThreads) prefill_select_kernel(const Prefill
   const __half* vsrc = a.V ? a.values + (size_t)hi * a.S_buf * D : nullptr;
   __half* Vg = a.V ? a.V + (li.row_base + (int64_t)slot_rem * li.cap) * D : nullptr;
   const float* col = a.colsum + (size_t)hi * a.Sp;
-  float* gs = a.gscr + (size_t)hi * a.Sp;
+  const float* gs = a.gtab + ((size_t)l * a.H + hh) * a.Sp;
   const int budget = li.budget;
   const int c = tid & 7;
-
-  for (int j = tid; j < S; j += kSThreads) gs[j] = gumbel_at(a.seed, l, hh, j);
-  __syncthreads();
 
   if (S <= budget) {  // the whole prompt fits: keep every row where it is
     for (int j0 = 0; j0 < S; j0 += kSThreads / 8) {
@@ -182,6 +181,14 @@ __global__ void __launch_bounds__(kSThreads) prefill_select_kernel(const Prefill
   if (tid == 0) a.pend[slot] = -1;
 }
 
+__global__ void gumbel_table_kernel(uint64_t seed, int H, int S, int Sp, int64_t n, float* out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t lh = i / S;
+    const int j = (int)(i - lh * S);
+    out[lh * Sp + j] = gumbel_at(seed, lh / H, lh % H, j);
+  }
+}
+
 // Current-step (TOVA-adapted) prompt scores: the prompt's last key attends
 // over every prompt key; score_j = softmax_j(K_j . k_{S-1} / sqrt(D)). One CTA
 // per cache row, 8 threads per key row, fp16 products accumulated in f32.
@@ -273,6 +280,14 @@ cudaError_t launch_prefill_lastrow(const PrefillScoreArgs& a, int D, cudaStream_
     prefill_lastrow_kernel<64><<<a.heads, 256, smem, s>>>(a);
   else
     prefill_lastrow_kernel<128><<<a.heads, 256, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gumbel_table(uint64_t seed, int L, int H, int S, int Sp, float* out, cudaStream_t s) {
+  const int64_t n = (int64_t)L * H * S;
+  if (n <= 0) return cudaSuccess;
+  const int blocks = (int)std::min<int64_t>((n + 255) / 256, 152 * 16);
+  gumbel_table_kernel<<<blocks, 256, 0, s>>>(seed, H, S, Sp, n, out);
   return cudaGetLastError();
 }
 

@@ -98,6 +98,7 @@ struct kvevict {
   int max_delta = 1;
   float* lse2 = nullptr;    // prefill scratch [heads, Sp_max]
   float* colsum = nullptr;
+  float* gtab = nullptr;    // [L*H, Sp_max] the prompt's Gumbel values
   int64_t Sp_max = 0;
   size_t decode_smem = 0;
   int decode_grid = 0;      // persistent decode CTAs
@@ -193,7 +194,7 @@ int enqueue_prompt_scores(kvevict* h, const uint16_t* keys, const uint16_t* valu
   pa.values = reinterpret_cast<const __half*>(values);
   pa.V = h->V;
   pa.colsum = colsum;
-  pa.gscr = lse2;  // pass 1's output is dead once the column sums exist
+  pa.gtab = h->gtab;   // filled by enqueue_gumbel_table for this prompt length
   pa.K = h->K;
   pa.score = h->score;
   pa.gum = h->gum;
@@ -218,6 +219,12 @@ int enqueue_prompt_scores(kvevict* h, const uint16_t* keys, const uint16_t* valu
   return KVEVICT_OK;
 }
 
+int enqueue_gumbel_table(kvevict* h, int32_t S, cudaStream_t s) {
+  const int Sp = (S + kvx::kPrefillRowPad - 1) / kvx::kPrefillRowPad * kvx::kPrefillRowPad;
+  KV_CUDA(kvx::launch_gumbel_table(h->cfg.seed, h->L, h->H, S, Sp, h->gtab, s));
+  return KVEVICT_OK;
+}
+
 // The whole prompt of every row (keys [B, L, H, S, D] on the device). BULK: one
 // scoring pass + bulk eviction. SEQUENTIAL: the first S0 = min(S, smallest
 // budget) tokens through the scorer (no row can evict before its budget is
@@ -228,7 +235,9 @@ int enqueue_prefill(kvevict* h, const uint16_t* keys, const uint16_t* values, in
   int32_t S0 = S;
   if (h->cfg.prefill_mode == KVEVICT_PREFILL_SEQUENTIAL)
     for (int32_t b : h->budgets) S0 = std::min(S0, b);
-  int rc = enqueue_prompt_scores(h, keys, values, S0, S, 0, h->B, h->lse2, h->colsum, s);
+  int rc = enqueue_gumbel_table(h, S0, s);
+  if (rc != KVEVICT_OK) return rc;
+  rc = enqueue_prompt_scores(h, keys, values, S0, S, 0, h->B, h->lse2, h->colsum, s);
   if (rc != KVEVICT_OK) return rc;
   if (evicted) KV_CUDA(cudaMemsetAsync(evicted, 0xFF, (size_t)S0 * BLH(h) * 4, s));
   if (S0 < S)
@@ -291,6 +300,7 @@ void free_all(kvevict* h) {
   cudaFree(h->rope_s);
   cudaFree(h->lse2);
   cudaFree(h->colsum);
+  cudaFree(h->gtab);
 }
 
 }  // namespace
@@ -422,9 +432,10 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
   if (c.max_prefill > 0) {
     KV_CUDA_CREATE(dalloc(&h->lse2, (size_t)h->heads * h->Sp_max));
     KV_CUDA_CREATE(dalloc(&h->colsum, (size_t)h->heads * h->Sp_max));
+    KV_CUDA_CREATE(dalloc(&h->gtab, (size_t)h->L * h->H * h->Sp_max));
   }
   h->bytes = (size_t)rows * h->D * 2 * (c.with_values ? 2 : 1) + (size_t)meta * 12 + (size_t)h->heads * 4 +
-             2 * (size_t)(h->max_delta + 1) * half * 4 + 2 * (size_t)h->heads * h->Sp_max * 4;
+             2 * (size_t)(h->max_delta + 1) * half * 4 + 2 * (size_t)h->heads * h->Sp_max * 4 + (size_t)h->L * h->H * h->Sp_max * 4;
 
   // RoPE constants for a shift back by d positions: c = f32(cos(-d w_i)),
   // s = f32(sin(-d w_i)), w_i = theta^(-2i/D), taken in fp64.
@@ -608,6 +619,10 @@ int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, cons
     h->ev_stage_elems = ev_need;
   }
   int k = 0;
+  if (S > 0 && !seq) {
+    const int rc = enqueue_gumbel_table(h, S, s);
+    if (rc != KVEVICT_OK) return rc;
+  }
   // prompt, batch chunk by batch chunk
   for (int b0 = 0; b0 < (S > 0 ? h->B : 0); b0 += bc, ++k) {
     const int nb = std::min(bc, h->B - b0);
