@@ -574,10 +574,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
           lo[pass] = *reinterpret_cast<const Chunk*>(row + c * CH * 2);
           hi[pass] = *reinterpret_cast<const Chunk*>(row + (HALF + c * CH) * 2);
         }
-        // the rows are in registers: hand the stage back before the arithmetic
-        // (the arrive releases, so the loads above complete before a refill)
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cta(empty(st));
         float dot[PR];
 #pragma unroll
         for (int pass = 0; pass < PR; ++pass) {
@@ -611,6 +607,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
             }
           }
         }
+        // Hand the stage back only after the arithmetic has consumed every
+        // value loaded from it: the TMA refill this permits is an async-proxy
+        // write ordered only through the barrier, so loads still in flight
+        // could read the next tile's bytes.
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cta(empty(st));
       }
       for (int t = P.ntiles; t < P.ntot && !*abort_flag; ++t) {   // value rows: move down one slot
         const int u = tg + t;
@@ -618,25 +620,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
         if (!wait_watch(full(st), (uint32_t)((u / kStages) & 1), abort_flag, a.err)) break;
         const unsigned char* tile = ring + (size_t)st * G::TILEB;
         const int r0 = P.vstart + (t - P.ntiles) * kTile;
-        constexpr int PR = kTile / kRowsPerPass;
-        Chunk lo[PR], hi[PR];
 #pragma unroll
-        for (int pass = 0; pass < PR; ++pass) {
-          const unsigned char* row = tile + (size_t)(pass * kRowsPerPass + rg) * G::ROWB;
-          lo[pass] = *reinterpret_cast<const Chunk*>(row + c * CH * 2);
-          hi[pass] = *reinterpret_cast<const Chunk*>(row + (HALF + c * CH) * 2);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cta(empty(st));
-#pragma unroll
-        for (int pass = 0; pass < PR; ++pass) {
-          const int R = r0 + pass * kRowsPerPass + rg;
+        for (int pass = 0; pass < kTile / kRowsPerPass; ++pass) {
+          const int rr = pass * kRowsPerPass + rg;
+          const int R = r0 + rr;
           if (R < nphys) {
+            const unsigned char* row = tile + (size_t)rr * G::ROWB;
             __half* dst = Vg + (size_t)(R - 1) * D;
-            *reinterpret_cast<Chunk*>(dst + c * CH) = lo[pass];
-            *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = hi[pass];
+            *reinterpret_cast<Chunk*>(dst + c * CH) = *reinterpret_cast<const Chunk*>(row + c * CH * 2);
+            *reinterpret_cast<Chunk*>(dst + HALF + c * CH) =
+                *reinterpret_cast<const Chunk*>(row + (HALF + c * CH) * 2);
           }
         }
+        __syncwarp();   // the stores above have consumed the loaded values
+        if (lane == 0) mbar_arrive_cta(empty(st));
       }
       for (int k = 0; k < P.nm && !*abort_flag; ++k)   // the metadata
         if (!wait_watch(full((um + k) % kStages), (uint32_t)(((um + k) / kStages) & 1), abort_flag, a.err)) break;
