@@ -136,7 +136,7 @@ def oracle_pass(wl, rows, threads=0):
 
 
 def cpu_sample_size(wl):
-    return max(1, os.cpu_count() or 1)
+    return 2 * max(1, os.cpu_count() or 1)   # two rows per core: about 10 s on 16 Grace cores
 
 
 def cpu_baseline(wl):
@@ -146,6 +146,19 @@ def cpu_baseline(wl):
             "sample": f"{len(rows)} cache rows spread over the layers, each a whole pass "
                       f"(prompt of {wl.prefill} + {wl.decode} decode steps), fp64 C oracle, "
                       f"OpenMP over rows; {dt:.1f} s"}
+
+
+def cpu_single_core():
+    """The oracle on one core: every row of the tiny H2O configuration and a few
+    rows of the Keyformer 3B configuration, each a whole pass."""
+    out = []
+    for wl, n in ((workloads.TINY_H2O, None), (workloads.KEYFORMER_3B, 4)):
+        rows = ([(b, l, h) for b in range(wl.batch) for l in range(wl.n_layers) for h in range(wl.n_kv_heads)]
+                if n is None else sample_rows(wl, n))
+        dt, used = oracle_pass(wl, rows, threads=1)
+        out.append({"workload": wl.name, "value": len(rows) * wl.decode / dt, "unit": UNIT, "cores": used,
+                    "rows": len(rows), "seconds": round(dt, 2)})
+    return out
 
 
 def run_reference(args):
@@ -387,9 +400,10 @@ def main():
                "d2h_bytes_per_step": ev_h.numel() * 4, "ms_per_step": dt * 1e3,
                "pass_ms": [round(x, 1) for x in e2e_ms], "clocks": e2e_clk}
 
-    cpu = None
+    cpu = single = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(wl)
+        single = cpu_single_core()
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -408,7 +422,10 @@ def main():
                      "peak_kind": f"of {peak_kind}"},
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "gpu_launches": args.steps * ((3 if wl.prefill else 0) + 1 + 1),
+        "cpu_single_core": single,
+        # per pass: Gumbel table, scorer passes 0 and 1 (or the last-row scorer), selection;
+        # one decode launch for every step; flush
+        "gpu_launches": args.steps * ((4 if wl.score_mode == 0 else 3) * (1 if wl.prefill else 0) + 1 + 1),
         "clocks": clk,
         "decode_head_steps_per_s": world * heads * T / (decode_ms / 1e3),
         "prefill_ms": prefill_ms, "decode_ms": decode_ms, "flush_ms": flush_ms,
