@@ -204,8 +204,17 @@ int kvevict_read_state(kvevict_t* h, int32_t b, int32_t l, int32_t head, uint16_
                        float* scores, float* gumbel, int32_t* positions, int32_t* n_kept,
                        void* stream);
 
-/* Synchronise the stream and report a kernel error word (DEVICE_CHECK) if set. */
+/* Synchronise the stream and report a kernel error word (DEVICE_CHECK) if set.
+ * After DEVICE_CHECK the state is not valid; kvevict_reset clears the error
+ * word and the state, after which the handle works as a new one. */
 int kvevict_check(kvevict_t* h, void* stream);
+
+/* Test hook for the failure path, with no counterpart on the pages: in the
+ * next decode launch, the first CTA's copy of its first key tile is never
+ * issued, so a wait on it runs out (1 s) and the kernel sets the error word
+ * (wait timeout) and returns; nothing faults or hangs. One-shot. Errors:
+ * INVALID_ARG (null handle). */
+int kvevict_test_stall_next_step(kvevict_t* h);
 
 /* Position the next decode key will occupy (= tokens absorbed so far). */
 int kvevict_next_pos(const kvevict_t* h, int64_t* p);

@@ -52,6 +52,7 @@ SIGNATURES = {
     "kvevict_create": (ctypes.c_int, [P, P, P]),
     "kvevict_destroy": (ctypes.c_int, [P]),
     "kvevict_reset": (ctypes.c_int, [P, P]),
+    "kvevict_test_stall_next_step": (ctypes.c_int, [P]),
     "kvevict_prefill": (ctypes.c_int, [P, P, i32, P]),
     "kvevict_prefill_ex": (ctypes.c_int, [P, P, i32, P, P]),
     "kvevict_prefill_kv": (ctypes.c_int, [P, P, P, i32, P, P]),
@@ -238,6 +239,10 @@ class KVEvict:
     def flush(self, stream=None):
         """Apply the last step's pending compaction (one kernel launch)."""
         _check(lib().kvevict_flush(self._h, _stream(stream)))
+
+    def test_stall_next_step(self):
+        """Test hook: the next decode launch makes one bounded wait run out."""
+        _check(lib().kvevict_test_stall_next_step(self._h))
 
     def check(self, stream=None):
         _check(lib().kvevict_check(self._h, _stream(stream)))

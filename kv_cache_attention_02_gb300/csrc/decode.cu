@@ -449,6 +449,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
           const int s = tg % kStages;
           if (tg >= kStages && !(ok = wait_watch(empty(s), (uint32_t)((tg / kStages - 1) & 1), abort_flag, a.err)))
             break;
+          if (a.stall && blockIdx.x == 0 && seq == 0 && t == 0) {   // test hook: a barrier nothing completes
+            ++tg;
+            continue;
+          }
           const int r0 = t < P.ntiles ? t * kTile : P.vstart + (t - P.ntiles) * kTile;
           const int rows = min(kTile, P.nphys - r0);
           const uint32_t bytes = (uint32_t)rows * G::ROWB;

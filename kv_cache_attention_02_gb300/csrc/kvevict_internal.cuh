@@ -68,6 +68,7 @@ struct DecodeArgs {
   int anneal_steps;        // A (0: constant tau_init)
   float scale2;            // log2(e)/sqrt(D): logits in base-2 units
   uint64_t seed;
+  int stall;               // test hook: CTA 0 never issues its first key tile's copy
 };
 
 struct FlushArgs {

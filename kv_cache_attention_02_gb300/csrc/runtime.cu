@@ -107,6 +107,7 @@ struct kvevict {
   size_t bytes = 0;
   int32_t* done = nullptr;  // [heads] decode steps applied to each row since reset
   int64_t dsteps = 0;       // decode steps launched since reset (every row takes each one)
+  bool stall_next = false;  // test hook (kvevict_test_stall_next_step)
   // host pipeline staging
   cudaStream_t copy_stream = nullptr;
   cudaEvent_t ev_ready[2] = {nullptr, nullptr};
@@ -164,6 +165,8 @@ int enqueue_steps(kvevict* h, const uint16_t* keys, const uint16_t* values, int6
   a.anneal_steps = h->cfg.anneal_steps;
   a.scale2 = (float)(1.4426950408889634 / std::sqrt((double)h->D));
   a.seed = h->cfg.seed;
+  a.stall = h->stall_next ? 1 : 0;
+  h->stall_next = false;
   KV_CUDA(kvx::launch_decode_step(a, h->D, h->decode_grid, h->decode_smem, s));
   h->dsteps += T;
   return KVEVICT_OK;
@@ -682,6 +685,12 @@ int kvevict_read_state(kvevict_t* h, int32_t b, int32_t l, int32_t head, uint16_
   rc = check_error_word(h, s);
   if (n_kept) *n_kept = n;
   return rc;
+}
+
+int kvevict_test_stall_next_step(kvevict_t* h) {
+  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  h->stall_next = true;
+  return KVEVICT_OK;
 }
 
 int kvevict_flush(kvevict_t* h, void* stream) {
