@@ -1,5 +1,6 @@
-// decode.cu -- the fused decode step (one launch per step over every row of
-// the cache) and the flush kernel that applies a pending compaction.
+// decode.cu -- the fused decode step (one launch runs a call's steps over
+// every row of the cache) and the flush kernel that applies a pending
+// compaction.
 //
 // What a step computes per (batch, layer, KV head) row follows page
 // "veloxquant_mlx.quantizers.keyformer module", keyformer_update steps 1-3 and

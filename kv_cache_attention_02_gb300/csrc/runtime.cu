@@ -1,6 +1,6 @@
 // runtime.cu -- the C ABI declared in include/kvevict.h: validation, the
-// budget taper, the device arena, launch sequencing, the cached CUDA graph of
-// decode steps and the host-buffer pipeline. Host code only; every step of the
+// budget taper, the device arena, launch sequencing (one decode launch per
+// call, whatever its step count) and the host-buffer pipeline. Host code only; every step of the
 // method runs in the kernels of decode.cu and prefill.cu.
 #include "kvevict.h"
 #include "kvevict_internal.cuh"
