@@ -203,26 +203,38 @@ def test_batched_equals_single_row(kvx, wgpu):
                 assert np.array_equal(st[i], full[(b, hh)][i])
 
 
-def test_run_host_equals_device_path(kvx, wgpu):
-    wl = SMALL[4]
+# run_host: prompt and decode copied from pinned host memory in chunks that
+# overlap compute. pyramidkv is large enough for several chunks of each (the
+# staging buffers hold 256 MiB).
+RUN_HOST_CASES = ["multi_tile_bulk", "tova_prompt", "sequential_prompt_pyramid", "d64_no_sinks",
+                  "pyramidkv"]
+
+
+@pytest.mark.parametrize("name", RUN_HOST_CASES)
+def test_run_host_equals_device_path(kvx, wgpu, name):
+    wl = next((w for w in SMALL if w.name == name), None) or workloads.ALL[name]
     pre, dec = wgpu.device_inputs(wl)
+    rows = all_rows(wl)
     h = kvx.from_workload(wl)
-    h.prefill(pre)
+    if pre is not None:
+        h.prefill(pre)
     ev = torch.zeros((wl.decode, wl.batch, wl.n_layers, wl.n_kv_heads), dtype=torch.int32,
                      device="cuda")
     h.decode(dec, ev)
-    want = {r: h.read_state(*r) for r in all_rows(wl)}
+    want = {r: h.read_state(*r) for r in rows}
     h.close()
     h2 = kvx.from_workload(wl)
-    pre_h = pre.cpu().pin_memory()
+    pre_h = pre.cpu().pin_memory() if pre is not None else None
     dec_h = dec.cpu().pin_memory()
     ev_h = torch.zeros(tuple(ev.shape), dtype=torch.int32).pin_memory()
     h2.run_host(pre_h, dec_h, ev_h)
     assert np.array_equal(ev_h.numpy(), ev.cpu().numpy())
-    for r in all_rows(wl):
+    for r in rows:
         for x, y in zip(h2.read_state(*r), want[r]):
             assert np.array_equal(x, y)
     h2.close()
+    del pre, dec
+    torch.cuda.empty_cache()
 
 
 def test_reset_replays_identically(kvx, wgpu):
