@@ -36,6 +36,9 @@ SCORE_ATOL = 1e-6
 class RowReport:
     steps: int = 0
     evictions: int = 0
+    evicted_first: int = 0        # evictions of the first candidate slot (n_sink)
+    evicted_last: int = 0         # evictions of the last candidate slot (the new row when recent = 0)
+    evicted_mid: int = 0          # evictions strictly between them
     ties: int = 0                 # steps whose two lowest r are within TIE_REL
     tie_divergences: int = 0      # ties where the CUDA path picked another tied row
     prefill_tie: bool = False
@@ -137,6 +140,13 @@ def _replay_steps(orc, prm, head, keys, gpu_ev, rep, what, checkpoints=None):
                     f"(r={head.r[eg] if 0 <= eg < head.n else None}), oracle {e} (r={head.r[e]}), "
                     f"ties {ties}")
                 return
+        last = head.n - 1 - prm.recent
+        if e == prm.n_sink:
+            rep.evicted_first += 1
+        elif e == last:
+            rep.evicted_last += 1
+        else:
+            rep.evicted_mid += 1
         head.evict(e)
         if checkpoints and (t + 1) in checkpoints:
             compare_state(rep, f"after step {t + 1}", head.state(), checkpoints[t + 1])

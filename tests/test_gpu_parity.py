@@ -153,6 +153,9 @@ SMALL = [
 ]
 
 
+_SLOT_KINDS = {"first": 0, "last": 0, "mid": 0}
+
+
 @pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
 def test_small_all_rows(kvx, wgpu, orc, wl):
     rows = all_rows(wl)
@@ -160,6 +163,19 @@ def test_small_all_rows(kvx, wgpu, orc, wl):
     res = run_gpu(kvx, wgpu, wl, rows, segments=seg)
     reps = compare_rows(orc, wl, rows, *res)
     assert sum(r.evictions for r in reps.values()) > 0
+    for r in reps.values():
+        _SLOT_KINDS["first"] += r.evicted_first
+        _SLOT_KINDS["last"] += r.evicted_last
+        _SLOT_KINDS["mid"] += r.evicted_mid
+
+
+def test_small_runs_evicted_first_mid_and_last_slots():
+    """Across the small configurations the decode step evicted (in agreement
+    with the oracle) the first candidate slot n_sink, the last candidate slot
+    and slots in between."""
+    if sum(_SLOT_KINDS.values()) == 0:
+        pytest.skip("run together with test_small_all_rows")
+    assert all(v > 0 for v in _SLOT_KINDS.values()), _SLOT_KINDS
 
 
 def test_step_path_equals_multistep_path(kvx, wgpu):
