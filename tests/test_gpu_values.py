@@ -26,7 +26,21 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
+def _random_cases(k=8):
+    """Seeded random small configurations (as in the random-configuration parity
+    tests) long enough that every layer evicts several times."""
+    import oracle as orc
+    from test_gpu_random_configs import _cases
+    out = []
+    for w in _cases(n=64, seed=77):
+        if w.prefill + w.decode > max(orc.budgets(w.n_layers, w.avg_budget, w.n_sink, w.beta)) + 5:
+            out.append(w.scaled(name=w.name + "_values"))
+        if len(out) == k:
+            break
+    return out
+
+
+@pytest.mark.parametrize("wl", CASES + _random_cases(), ids=lambda w: w.name)
 @pytest.mark.parametrize("path", ["multi", "step"])
 def test_values_follow_positions(wl, path):
     import kv_cache_attention_02_gb300 as kvx
