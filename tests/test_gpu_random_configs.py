@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 
-from test_gpu_parity import all_rows, compare_rows, run_gpu  # noqa: E402
+from test_gpu_parity import all_rows, compare_rows, run_gpu, sampled_rows  # noqa: E402
 
 _EDGES = [1, 2, 63, 64, 65, 127, 128, 129, 191, 192]
 
@@ -63,5 +63,48 @@ def test_random_config_all_rows(wl):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     rows = all_rows(wl)
+    res = run_gpu(kvx, wgpu, wl, rows, segments=[wl.decode // 2])
+    compare_rows(orc, wl, rows, *res)
+
+
+def _medium_cases(n=8, seed=4051):
+    """More rows than the decode step runs CTAs (up to 2 per SM), budgets of several
+    tiles: every CTA claims several rows per step, of mixed lengths."""
+    import oracle as orc
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        while True:
+            D = int(rng.choice([64, 128]))
+            B, L, H = int(rng.integers(2, 9)), int(rng.integers(2, 9)), int(rng.integers(4, 17))
+            if B * L * H < 320:
+                continue
+            n_sink = int(rng.integers(0, 6))
+            recent = int(rng.choice([0, int(rng.integers(1, 9))]))
+            avg = int(rng.integers(150, 700))
+            beta = float(rng.choice([1.0, 1.6, 2.2]))
+            if min(orc.budgets(L, avg, n_sink, beta)) < n_sink + recent + 1:
+                continue
+            break
+        out.append(Workload(f"random_medium_{i}", batch=B, n_layers=L, n_kv_heads=H, head_dim=D,
+                            avg_budget=avg, beta=beta, n_sink=n_sink,
+                            tau_init=float(np.round(rng.uniform(0, 2), 3)),
+                            tau_end=float(np.round(rng.uniform(0, 2), 3)),
+                            anneal_steps=int(rng.choice([0, int(rng.integers(100, 1200))])),
+                            rope_theta=500000.0, gumbel_seed=int(rng.integers(0, 2 ** 32)),
+                            key_seed=2000 + i, prefill=int(rng.integers(0, 900)),
+                            decode=int(rng.integers(40, 160)), recent=recent,
+                            score_mode=int(rng.integers(0, 2)), prefill_mode=int(rng.integers(0, 2))))
+    return out
+
+
+@pytest.mark.parametrize("wl", _medium_cases(), ids=lambda w: w.name)
+def test_random_medium_config_sampled_rows(wl):
+    import kv_cache_attention_02_gb300 as kvx
+    from workloads import gpu as wgpu
+    import oracle as orc
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    rows = sampled_rows(wl, k=12, seed=5)
     res = run_gpu(kvx, wgpu, wl, rows, segments=[wl.decode // 2])
     compare_rows(orc, wl, rows, *res)
