@@ -208,11 +208,20 @@ __device__ __forceinline__ void warp_argmin(float& r, int& i) {
   }
 }
 
+// 2^x on the MUFU (ex2.approx: relative error below 2^-22; a result below the
+// smallest normal flushes to zero, which only drops terms smaller than 2^-126
+// of the row's largest from a softmax sum).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Combine two (max, sum of 2^(x - max)) pairs (logits are kept in base-2 units).
 __device__ __forceinline__ void lse_combine(float& m, float& l, float m2, float l2) {
   const float mn = fmaxf(m, m2);
   if (mn == -INFINITY) return;
-  l = (m == -INFINITY ? 0.f : l * exp2f(m - mn)) + (m2 == -INFINITY ? 0.f : l2 * exp2f(m2 - mn));
+  l = (m == -INFINITY ? 0.f : l * ex2(m - mn)) + (m2 == -INFINITY ? 0.f : l2 * ex2(m2 - mn));
   m = mn;
 }
 
@@ -605,10 +614,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
             const float sv = dot[pass] * a.scale2;   // base-2 logit
             s_log[Rr[pass]] = sv;
             if (sv > run_m) {
-              run_l = run_l * exp2f(run_m - sv) + 1.f;
+              run_l = run_l * ex2(run_m - sv) + 1.f;
               run_m = sv;
             } else {
-              run_l += exp2f(sv - run_m);
+              run_l += ex2(sv - run_m);
             }
           }
         }
@@ -657,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
       int best_R = INT_MAX;
       for (int R = tid; R < NR; R += kConsumers) {
         if (R == e_prev) continue;
-        const float attn = exp2f(s_log[R] - m) * inv_l;
+        const float attn = ex2(s_log[R] - m) * inv_l;
         const float ns = a.mode ? attn : (R < nphys ? s_sc[R] : 0.f) + attn;   // current-step or cumulative
         const bool moved = shift && R > e_prev;
         const int j = R - (moved ? 1 : 0);                                     // slot after compaction
