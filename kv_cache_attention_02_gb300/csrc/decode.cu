@@ -604,15 +604,22 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
           }
           dot[pass] = live[pass] ? dot_chunks<CH>(lo[pass], hi[pass], q_lo, q_hi) : 0.f;
         }
-#pragma unroll
-        for (int o = 1; o < kTPR; o <<= 1)
-#pragma unroll
-          for (int pass = 0; pass < PR; ++pass) dot[pass] += __shfl_xor_sync(0xffffffffu, dot[pass], o);
-#pragma unroll
-        for (int pass = 0; pass < PR; ++pass) {
-          if (live[pass] && c == 0) {
-            const float sv = dot[pass] * a.scale2;   // base-2 logit
-            s_log[Rr[pass]] = sv;
+        static_assert(PR == 2, "the reduce-scatter below pairs two rows per thread");
+        {
+          // reduce-scatter over the 8 threads of a row group: after the first
+          // exchange even threads carry row 0's partial sums and odd ones row
+          // 1's; two more rounds finish both (the association is the plain
+          // butterfly's, so the sums are the same)
+          const bool odd = (c & 1) != 0;
+          float mine = odd ? dot[1] : dot[0];
+          mine += __shfl_xor_sync(0xffffffffu, odd ? dot[0] : dot[1], 1);
+          mine += __shfl_xor_sync(0xffffffffu, mine, 2);
+          mine += __shfl_xor_sync(0xffffffffu, mine, 4);
+          const bool lv = odd ? live[1] : live[0];
+          const int Rw = odd ? Rr[1] : Rr[0];
+          if (lv && c < 2) {
+            const float sv = mine * a.scale2;   // base-2 logit
+            s_log[Rw] = sv;
             if (sv > run_m) {
               run_l = run_l * ex2(run_m - sv) + 1.f;
               run_m = sv;
