@@ -11,8 +11,10 @@ at their positions, generated on the device before the timed region.
 Prints one JSON line. ``value`` = decode head-steps (batch x layers x KV heads
 x decode tokens) per second of whole-pass time, inputs resident in HBM;
 ``e2e`` = the same metric through ``kvevict_run_host`` with the keys in pinned
-host memory and the evicted-slot log copied back, copies inside the timed
-region; ``roofline`` = the decode kernel's algorithmic bytes (from the actual
+host memory and the evicted-slot log copied back, every host<->device transfer
+inside the timed region (the library moves page-locked buffers with its own
+kernels: the prompt is staged by a copy kernel, the decode keys are read in
+place over the CPU-GPU link); ``roofline`` = the decode kernel's algorithmic bytes (from the actual
 eviction log) over its time, against the measured HBM copy bandwidth;
 ``cpu_baseline`` = the fp64 CPU oracle on a bounded sample of the same
 workload on this host's cores.

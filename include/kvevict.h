@@ -21,8 +21,11 @@
  * Conventions shared by every entry point:
  *  - fp16 values cross the boundary as uint16_t bit patterns (IEEE binary16).
  *  - Device pointers are CUDA global-memory pointers on the device that was
- *    current at kvevict_create; host pointers are plain host memory (pinned
- *    memory lets the copies overlap with compute).
+ *    current at kvevict_create (mapped page-locked host memory counts as
+ *    one); device key and value buffers must start on a 16-byte boundary
+ *    (INVALID_ARG otherwise). Host pointers are plain host memory; the
+ *    host-buffer entry point moves page-locked buffers with its own kernels
+ *    (see kvevict_run_host).
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream). All work
  *    is enqueued on it; calls return before the GPU finishes unless stated.
  *  - The caller owns every buffer it passes and keeps it alive until the
@@ -177,10 +180,16 @@ int kvevict_decode(kvevict_t* h, const uint16_t* keys, int32_t T, int32_t* evict
 
 /* End to end from host memory: prefill S prompt keys (host fp16
  * [B, L, H, S, D]; S may be 0) then T decode steps (host fp16 [T, B, L, H, D]),
- * copying the inputs to the device in chunks that overlap with compute and
- * the evicted slots back to host int32 [T, B, L, H] (or NULL). The state must
- * be empty. Returns after the stream has finished. Device staging is allocated
- * on first use and kept with the handle.
+ * with the evicted slots written back to host int32 [T, B, L, H] (or NULL).
+ * The state must be empty. Returns after the stream has finished.
+ * Each buffer must be one allocation. A page-locked buffer (cudaHostAlloc,
+ * cudaMallocHost or cudaHostRegister; both its ends are checked) is accessed
+ * by the library's kernels through its device mapping: the prompt is staged
+ * to the device by a copy kernel, the decode keys are read in place by the
+ * decode step, and the evicted slots are written back by a copy kernel.
+ * Pageable memory goes through cudaMemcpyAsync in chunks on a second stream
+ * that overlap with compute. Device staging (up to 2 x 256 MiB, or one batch's
+ * prompt) is allocated on first use and kept with the handle.
  * Errors: INVALID_ARG, BAD_STATE, OOM, CUDA, DEVICE_CHECK. */
 int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S,
                      const uint16_t* decode_keys, int32_t T, int32_t* evicted, void* stream);

@@ -717,12 +717,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
       }
       // every consumer is done with s_log, the metadata and the reduction
       // scratch, and every write of this row's step has been issued: publish
-      // the step, free the metadata stages and the row's slot
+      // the step, free the metadata stages and the row's slot. The named
+      // barrier orders every consumer's writes before thread 0's release (the
+      // barrier synchronises at CTA scope, and a release is cumulative over
+      // what precedes it in causality order), so no separate fence is needed
+      // for a CTA that acquires the counter to see them.
       consumers_sync();
-      if (tid == 0) {
-        __threadfence();
-        st_release(a.done + hd.head, a.s0 + hd.t + 1);
-      }
+      if (tid == 0) st_release(a.done + hd.head, a.s0 + hd.t + 1);
       if (lane == 0) {
         for (int k = 0; k < P.nm; ++k) mbar_arrive_cta(empty((um + k) % kStages));
         mbar_arrive_cta(rempty(q));

@@ -18,6 +18,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <type_traits>
 
@@ -131,6 +132,13 @@ size_t decode_step_smem(int D, int capm_max);
 cudaError_t decode_step_ctas_per_sm(int D, size_t smem, int* ctas);
 cudaError_t launch_decode_step(const DecodeArgs& a, int D, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_flush(const FlushArgs& a, int D, int heads, cudaStream_t s);
+
+// Page-locked host memory (staging.cu). mapped_host: the device address of the
+// host buffer [p, p + bytes) when both its ends are page-locked and mapped into
+// one device range, else nullptr (pageable memory). launch_copy: bytes from src
+// to dst with SM loads and stores; either side may be a mapped host address.
+void* mapped_host(const void* p, size_t bytes);
+cudaError_t launch_copy(const void* src, void* dst, size_t bytes, int sms, cudaStream_t s);
 
 cudaError_t prefill_setup(int D, int max_prefill);  // bulk-eviction kernel's shared memory
 // current-step (TOVA) prompt scores: softmax of the last prompt key against every prompt key

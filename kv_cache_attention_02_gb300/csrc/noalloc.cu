@@ -92,6 +92,10 @@ extern "C" int kvevict_prefill_scores_noalloc(const uint16_t* keys, int32_t head
     kvx::set_last_error("keys and colsum must not be null");
     return KVEVICT_ERR_INVALID_ARG;
   }
+  if ((reinterpret_cast<uintptr_t>(keys) & 15) != 0) {
+    kvx::set_last_error("keys must be 16-byte aligned");
+    return KVEVICT_ERR_INVALID_ARG;
+  }
   if (head_dim != 64 && head_dim != 128) {
     kvx::set_last_error("head_dim must be 64 or 128");
     return KVEVICT_ERR_INVALID_ARG;

@@ -102,6 +102,7 @@ struct kvevict {
   int64_t Sp_max = 0;
   size_t decode_smem = 0;
   int decode_grid = 0;      // persistent decode CTAs
+  int sms = 0;              // SMs on the device
   int64_t next_pos = 0;
   bool stepped = false;
   size_t bytes = 0;
@@ -416,6 +417,7 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
     KV_CUDA_CREATE(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device));
     if (per_sm < 1) return bail(fail(KVEVICT_ERR_INVALID_ARG, "decode step does not fit on an SM"));
     h->decode_grid = (int)std::min<int64_t>((int64_t)per_sm * sms, h->heads);
+    h->sms = sms;
   }
   KV_CUDA_CREATE(kvx::prefill_setup(h->D, c.max_prefill));
   KV_CUDA_CREATE(kvx::prefill_tc_setup(h->D));
@@ -489,10 +491,16 @@ int kvevict_reset(kvevict_t* h, void* stream) {
 
 namespace {
 
+// Device key and value buffers start on a 16-byte boundary (the prompt scorer
+// reads them with TMA, the decode step with 4- or 8-byte words).
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
 int prefill_impl(kvevict* h, const uint16_t* keys, const uint16_t* values, int32_t S, int32_t* evicted,
                  void* stream) {
   if (S < 0 || S > h->cfg.max_prefill) return fail(KVEVICT_ERR_INVALID_ARG, "S must be in [0, max_prefill]");
   if (S > 0 && (!keys || (h->V && !values))) return fail(KVEVICT_ERR_INVALID_ARG, "keys or values is null");
+  if (S > 0 && (!aligned16(keys) || !aligned16(values)))
+    return fail(KVEVICT_ERR_INVALID_ARG, "keys and values must be 16-byte aligned");
   if (h->next_pos != 0 || h->stepped) return fail(KVEVICT_ERR_BAD_STATE, "prefill needs an empty state");
   if (S == 0) return KVEVICT_OK;
   const int rc = enqueue_prefill(h, keys, values, S, evicted, (cudaStream_t)stream);
@@ -503,6 +511,8 @@ int prefill_impl(kvevict* h, const uint16_t* keys, const uint16_t* values, int32
 
 int step_impl(kvevict* h, const uint16_t* k_new, const uint16_t* v_new, int32_t* evicted, void* stream) {
   if (!k_new || (h->V && !v_new)) return fail(KVEVICT_ERR_INVALID_ARG, "k_new or v_new is null");
+  if (!aligned16(k_new) || !aligned16(v_new))
+    return fail(KVEVICT_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
   const int rc = enqueue_steps(h, k_new, v_new, h->D, 0, evicted, 1, h->next_pos, (cudaStream_t)stream);
   if (rc != KVEVICT_OK) return rc;
   h->next_pos += 1;
@@ -515,6 +525,8 @@ int decode_impl(kvevict* h, const uint16_t* keys, const uint16_t* values, int32_
   if (T < 0) return fail(KVEVICT_ERR_INVALID_ARG, "T must be >= 0");
   if (T == 0) return KVEVICT_OK;
   if (!keys || (h->V && !values)) return fail(KVEVICT_ERR_INVALID_ARG, "keys or values is null");
+  if (!aligned16(keys) || !aligned16(values))
+    return fail(KVEVICT_ERR_INVALID_ARG, "keys and values must be 16-byte aligned");
   const int rc = enqueue_steps(h, keys, values, h->D, BLHD(h), evicted, T, h->next_pos, (cudaStream_t)stream);
   if (rc != KVEVICT_OK) return rc;
   h->next_pos += T;
@@ -585,17 +597,25 @@ int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, cons
   if (h->next_pos != 0 || h->stepped) return fail(KVEVICT_ERR_BAD_STATE, "run_host needs an empty state");
   if (int rc = keys_only(h)) return rc;
   cudaStream_t s = (cudaStream_t)stream;
-  // Staging: two buffers of up to 256 MiB (or one batch's prompt / one step,
-  // whichever is larger), so copies of chunk k+1 overlap compute on chunk k.
   const size_t per_batch = (size_t)h->L * h->H * (size_t)S * h->D;
   const size_t per_step = (size_t)BLHD(h);
+  // Page-locked buffers are moved by the library's kernels through their
+  // device mapping: the prompt is staged by a copy kernel and the decode keys
+  // are read in place by the decode step. Other host memory is staged with
+  // cudaMemcpyAsync on a second stream, overlapping compute.
+  const void* pre_map = S > 0 ? kvx::mapped_host(prefill_keys, (size_t)h->B * per_batch * 2) : nullptr;
+  const void* dec_map = T > 0 ? kvx::mapped_host(decode_keys, (size_t)T * per_step * 2) : nullptr;
+  const bool dec_inplace = dec_map && aligned16(dec_map);   // else staged by the copy kernel
+  void* ev_map = (evicted && T > 0) ? kvx::mapped_host(evicted, (size_t)T * BLH(h) * 4) : nullptr;
+  // Staging: two buffers of up to 256 MiB (or one batch's prompt / one step,
+  // whichever is larger), so copies of chunk k+1 overlap compute on chunk k.
   const size_t budget_elems = (size_t)128 << 20;  // 256 MiB of fp16
   const bool seq = h->cfg.prefill_mode == KVEVICT_PREFILL_SEQUENTIAL;
   const int bc = S <= 0 ? 0
                  : seq ? h->B   // sequential steps run over every row: stage the whole prompt
                        : (int)std::max<size_t>(1, std::min<size_t>(h->B, budget_elems / std::max<size_t>(per_batch, 1)));
   const int tc = T > 0 ? (int)std::max<size_t>(1, std::min<size_t>((size_t)T, budget_elems / per_step)) : 0;
-  const size_t need = std::max((size_t)bc * per_batch, (size_t)tc * per_step);
+  const size_t need = std::max((size_t)bc * per_batch, dec_inplace ? (size_t)0 : (size_t)tc * per_step);
   if (!h->copy_stream) {
     KV_CUDA(cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking));
     for (int i = 0; i < 2; ++i) {
@@ -621,6 +641,19 @@ int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, cons
     }
     h->ev_stage_elems = ev_need;
   }
+  // one chunk of input into staging buffer buf, ordered before work on s
+  auto stage_in = [&](int buf, const void* host, const void* mapped, size_t off, size_t bytes) -> int {
+    if (mapped) {
+      KV_CUDA(kvx::launch_copy(static_cast<const char*>(mapped) + off, h->stage[buf], bytes, h->sms, s));
+      return KVEVICT_OK;
+    }
+    KV_CUDA(cudaStreamWaitEvent(h->copy_stream, h->ev_free[buf], 0));
+    KV_CUDA(cudaMemcpyAsync(h->stage[buf], static_cast<const char*>(host) + off, bytes, cudaMemcpyHostToDevice,
+                            h->copy_stream));
+    KV_CUDA(cudaEventRecord(h->ev_ready[buf], h->copy_stream));
+    KV_CUDA(cudaStreamWaitEvent(s, h->ev_ready[buf], 0));
+    return KVEVICT_OK;
+  };
   int k = 0;
   if (S > 0 && !seq) {
     const int rc = enqueue_gumbel_table(h, S, s);
@@ -630,13 +663,10 @@ int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, cons
   for (int b0 = 0; b0 < (S > 0 ? h->B : 0); b0 += bc, ++k) {
     const int nb = std::min(bc, h->B - b0);
     const int buf = k & 1;
-    KV_CUDA(cudaStreamWaitEvent(h->copy_stream, h->ev_free[buf], 0));
-    KV_CUDA(cudaMemcpyAsync(h->stage[buf], prefill_keys + (size_t)b0 * per_batch, (size_t)nb * per_batch * 2,
-                            cudaMemcpyHostToDevice, h->copy_stream));
-    KV_CUDA(cudaEventRecord(h->ev_ready[buf], h->copy_stream));
-    KV_CUDA(cudaStreamWaitEvent(s, h->ev_ready[buf], 0));
-    const int rc = seq ? enqueue_prefill(h, h->stage[buf], nullptr, S, nullptr, s)
-                       : enqueue_prompt_scores(h, h->stage[buf], nullptr, S, S, b0, nb, h->lse2, h->colsum, s);
+    int rc = stage_in(buf, prefill_keys, pre_map, (size_t)b0 * per_batch * 2, (size_t)nb * per_batch * 2);
+    if (rc != KVEVICT_OK) return rc;
+    rc = seq ? enqueue_prefill(h, h->stage[buf], nullptr, S, nullptr, s)
+             : enqueue_prompt_scores(h, h->stage[buf], nullptr, S, S, b0, nb, h->lse2, h->colsum, s);
     if (rc != KVEVICT_OK) return rc;
     KV_CUDA(cudaEventRecord(h->ev_free[buf], s));
   }
@@ -645,19 +675,24 @@ int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, cons
   for (int t0 = 0; t0 < T; t0 += tc, ++k) {
     const int nt = std::min(tc, T - t0);
     const int buf = k & 1;
-    KV_CUDA(cudaStreamWaitEvent(h->copy_stream, h->ev_free[buf], 0));
-    KV_CUDA(cudaMemcpyAsync(h->stage[buf], decode_keys + (size_t)t0 * per_step, (size_t)nt * per_step * 2,
-                            cudaMemcpyHostToDevice, h->copy_stream));
-    KV_CUDA(cudaEventRecord(h->ev_ready[buf], h->copy_stream));
-    KV_CUDA(cudaStreamWaitEvent(s, h->ev_ready[buf], 0));
-    const int rc = enqueue_steps(h, h->stage[buf], nullptr, h->D, (int64_t)per_step,
-                                 evicted ? h->ev_stage[buf] : nullptr, nt, h->next_pos, s);
+    const uint16_t* keys =
+        dec_inplace ? static_cast<const uint16_t*>(dec_map) + (size_t)t0 * per_step : h->stage[buf];
+    if (!dec_inplace) {
+      const int rc = stage_in(buf, decode_keys, dec_map, (size_t)t0 * per_step * 2, (size_t)nt * per_step * 2);
+      if (rc != KVEVICT_OK) return rc;
+    }
+    const int rc = enqueue_steps(h, keys, nullptr, h->D, (int64_t)per_step, evicted ? h->ev_stage[buf] : nullptr,
+                                 nt, h->next_pos, s);
     if (rc != KVEVICT_OK) return rc;
     h->next_pos += nt;
     h->stepped = true;
-    if (evicted)
-      KV_CUDA(cudaMemcpyAsync(evicted + (size_t)t0 * BLH(h), h->ev_stage[buf], (size_t)nt * BLH(h) * 4,
-                              cudaMemcpyDeviceToHost, s));
+    if (evicted) {
+      const size_t off = (size_t)t0 * BLH(h), bytes = (size_t)nt * BLH(h) * 4;
+      if (ev_map)
+        KV_CUDA(kvx::launch_copy(h->ev_stage[buf], static_cast<int32_t*>(ev_map) + off, bytes, h->sms, s));
+      else
+        KV_CUDA(cudaMemcpyAsync(evicted + off, h->ev_stage[buf], bytes, cudaMemcpyDeviceToHost, s));
+    }
     KV_CUDA(cudaEventRecord(h->ev_free[buf], s));
   }
   return check_error_word(h, s);

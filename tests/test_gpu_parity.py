@@ -219,15 +219,30 @@ def test_batched_equals_single_row(kvx, wgpu):
                 assert np.array_equal(st[i], full[(b, hh)][i])
 
 
-# run_host: prompt and decode copied from pinned host memory in chunks that
-# overlap compute. pyramidkv is large enough for several chunks of each (the
-# staging buffers hold 256 MiB).
+# run_host: the inputs come from host memory. Page-locked buffers are moved by
+# the library's kernels (the prompt staged by a copy kernel, the decode keys
+# read in place), pageable ones by cudaMemcpyAsync chunks that overlap compute;
+# a page-locked buffer that does not start on a 16-byte boundary is staged by
+# the copy kernel with narrower words. pyramidkv is large enough for several
+# chunks of each (the staging buffers hold 256 MiB).
 RUN_HOST_CASES = ["multi_tile_bulk", "tova_prompt", "sequential_prompt_pyramid", "d64_no_sinks",
                   "pyramidkv"]
+RUN_HOST_MEMORY = [(n, "pinned") for n in RUN_HOST_CASES] + [(n, "pageable") for n in RUN_HOST_CASES] + [
+    ("multi_tile_bulk", "pinned_prompt_pageable_decode"), ("tova_prompt", "pageable_prompt_pinned_decode"),
+    ("multi_tile_bulk", "pinned_misaligned"), ("d64_no_sinks", "pinned_misaligned")]
 
 
-@pytest.mark.parametrize("name", RUN_HOST_CASES)
-def test_run_host_equals_device_path(kvx, wgpu, name):
+def _host_copy(t, pinned, offset_elems=0):
+    """A contiguous host copy of t, page-locked or not, starting offset_elems
+    elements into its allocation."""
+    flat = torch.empty(t.numel() + offset_elems, dtype=t.dtype, pin_memory=pinned)
+    view = flat[offset_elems:].view(t.shape)
+    view.copy_(t.cpu() if t.is_cuda else t)
+    return view
+
+
+@pytest.mark.parametrize("name,memory", RUN_HOST_MEMORY, ids=[f"{n}-{m}" for n, m in RUN_HOST_MEMORY])
+def test_run_host_equals_device_path(kvx, wgpu, name, memory):
     wl = next((w for w in SMALL if w.name == name), None) or workloads.ALL[name]
     pre, dec = wgpu.device_inputs(wl)
     rows = all_rows(wl)
@@ -239,10 +254,13 @@ def test_run_host_equals_device_path(kvx, wgpu, name):
     h.decode(dec, ev)
     want = {r: h.read_state(*r) for r in rows}
     h.close()
+    pin_pre = memory in ("pinned", "pinned_prompt_pageable_decode", "pinned_misaligned")
+    pin_dec = memory in ("pinned", "pageable_prompt_pinned_decode", "pinned_misaligned")
+    off = 1 if memory == "pinned_misaligned" else 0   # 2 bytes for keys, 4 for the slots
     h2 = kvx.from_workload(wl)
-    pre_h = pre.cpu().pin_memory() if pre is not None else None
-    dec_h = dec.cpu().pin_memory()
-    ev_h = torch.zeros(tuple(ev.shape), dtype=torch.int32).pin_memory()
+    pre_h = _host_copy(pre, pin_pre, off) if pre is not None else None
+    dec_h = _host_copy(dec, pin_dec, off)
+    ev_h = _host_copy(torch.full(tuple(ev.shape), -9, dtype=torch.int32), pin_dec, off)
     h2.run_host(pre_h, dec_h, ev_h)
     assert np.array_equal(ev_h.numpy(), ev.cpu().numpy())
     for r in rows:
@@ -251,6 +269,25 @@ def test_run_host_equals_device_path(kvx, wgpu, name):
     h2.close()
     del pre, dec
     torch.cuda.empty_cache()
+
+
+def test_misaligned_device_keys_are_rejected(kvx, wgpu):
+    wl = SMALL[0]
+    pre, dec = wgpu.device_inputs(wl)
+    h = kvx.from_workload(wl)
+    shifted = lambda t: torch.empty(t.numel() + 8, dtype=t.dtype, device="cuda")[1:1 + t.numel()].view(t.shape)
+    with pytest.raises(kvx.KVEvictError) as err:
+        h.prefill(shifted(pre))
+    assert err.value.code == kvx.ERR_INVALID_ARG and "16-byte" in str(err.value)
+    h.prefill(pre)
+    for call in (lambda: h.decode(shifted(dec)), lambda: h.step(shifted(dec[0]))):
+        with pytest.raises(kvx.KVEvictError) as err:
+            call()
+        assert err.value.code == kvx.ERR_INVALID_ARG
+    assert h.next_pos == wl.prefill   # nothing ran
+    h.decode(dec)
+    h.check()
+    h.close()
 
 
 def test_reset_replays_identically(kvx, wgpu):
