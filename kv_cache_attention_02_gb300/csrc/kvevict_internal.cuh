@@ -137,8 +137,9 @@ cudaError_t launch_flush(const FlushArgs& a, int D, int heads, cudaStream_t s);
 // host buffer [p, p + bytes) when both its ends are page-locked and mapped into
 // one device range, else nullptr (pageable memory). launch_copy: bytes from src
 // to dst with SM loads and stores; either side may be a mapped host address.
+// background: one small block per SM, sized to run beside the prompt scorer.
 void* mapped_host(const void* p, size_t bytes);
-cudaError_t launch_copy(const void* src, void* dst, size_t bytes, int sms, cudaStream_t s);
+cudaError_t launch_copy(const void* src, void* dst, size_t bytes, int sms, bool background, cudaStream_t s);
 
 cudaError_t prefill_setup(int D, int max_prefill);  // bulk-eviction kernel's shared memory
 // current-step (TOVA) prompt scores: softmax of the last prompt key against every prompt key

@@ -641,15 +641,16 @@ int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, cons
     }
     h->ev_stage_elems = ev_need;
   }
-  // one chunk of input into staging buffer buf, ordered before work on s
+  // one chunk of input into staging buffer buf on the copy stream, ordered
+  // after the last work on that buffer and before the next work on s
   auto stage_in = [&](int buf, const void* host, const void* mapped, size_t off, size_t bytes) -> int {
-    if (mapped) {
-      KV_CUDA(kvx::launch_copy(static_cast<const char*>(mapped) + off, h->stage[buf], bytes, h->sms, s));
-      return KVEVICT_OK;
-    }
     KV_CUDA(cudaStreamWaitEvent(h->copy_stream, h->ev_free[buf], 0));
-    KV_CUDA(cudaMemcpyAsync(h->stage[buf], static_cast<const char*>(host) + off, bytes, cudaMemcpyHostToDevice,
-                            h->copy_stream));
+    if (mapped)
+      KV_CUDA(kvx::launch_copy(static_cast<const char*>(mapped) + off, h->stage[buf], bytes, h->sms, true,
+                               h->copy_stream));
+    else
+      KV_CUDA(cudaMemcpyAsync(h->stage[buf], static_cast<const char*>(host) + off, bytes, cudaMemcpyHostToDevice,
+                              h->copy_stream));
     KV_CUDA(cudaEventRecord(h->ev_ready[buf], h->copy_stream));
     KV_CUDA(cudaStreamWaitEvent(s, h->ev_ready[buf], 0));
     return KVEVICT_OK;
@@ -689,7 +690,7 @@ int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, cons
     if (evicted) {
       const size_t off = (size_t)t0 * BLH(h), bytes = (size_t)nt * BLH(h) * 4;
       if (ev_map)
-        KV_CUDA(kvx::launch_copy(h->ev_stage[buf], static_cast<int32_t*>(ev_map) + off, bytes, h->sms, s));
+        KV_CUDA(kvx::launch_copy(h->ev_stage[buf], static_cast<int32_t*>(ev_map) + off, bytes, h->sms, false, s));
       else
         KV_CUDA(cudaMemcpyAsync(evicted + off, h->ev_stage[buf], bytes, cudaMemcpyDeviceToHost, s));
     }

@@ -14,11 +14,16 @@ namespace kvx {
 namespace {
 
 constexpr int kCopyThreads = 256;
+// The background form: one 128-thread block per SM, at most 32 registers a
+// thread, so that a block fits beside two CTAs of the prompt scorer (2 x 320
+// threads at up to 96 registers, about 100 KB of shared memory each) and the
+// copy of the next prompt chunk runs under the scoring of the current one.
+constexpr int kBgThreads = 128;
 
 // dst[i] = src[i] for i < n, four independent loads in flight per thread.
-template <typename W>
-__global__ void __launch_bounds__(kCopyThreads) copy_words_kernel(const W* __restrict__ src, W* __restrict__ dst,
-                                                                  size_t n) {
+template <typename W, int THREADS, int MIN_BLOCKS>
+__global__ void __launch_bounds__(THREADS, MIN_BLOCKS) copy_words_kernel(const W* __restrict__ src,
+                                                                        W* __restrict__ dst, size_t n) {
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   for (; i + 3 * stride < n; i += 4 * stride) {
@@ -32,11 +37,18 @@ __global__ void __launch_bounds__(kCopyThreads) copy_words_kernel(const W* __res
 }
 
 template <typename W>
-cudaError_t launch_words(const void* src, void* dst, size_t bytes, int sms, cudaStream_t s) {
+cudaError_t launch_words(const void* src, void* dst, size_t bytes, int sms, bool background, cudaStream_t s) {
   const size_t n = bytes / sizeof(W);
-  const size_t want = (n + 4 * (size_t)kCopyThreads - 1) / (4 * (size_t)kCopyThreads);
-  const unsigned blocks = (unsigned)std::max<size_t>(1, std::min<size_t>(want, (size_t)std::max(1, sms) * 4));
-  copy_words_kernel<W><<<blocks, kCopyThreads, 0, s>>>(static_cast<const W*>(src), static_cast<W*>(dst), n);
+  const int threads = background ? kBgThreads : kCopyThreads;
+  const size_t want = (n + 4 * (size_t)threads - 1) / (4 * (size_t)threads);
+  const size_t cap = (size_t)std::max(1, sms) * (background ? 1 : 4);
+  const unsigned blocks = (unsigned)std::max<size_t>(1, std::min<size_t>(want, cap));
+  if (background)
+    copy_words_kernel<W, kBgThreads, 16><<<blocks, kBgThreads, 0, s>>>(static_cast<const W*>(src),
+                                                                       static_cast<W*>(dst), n);
+  else
+    copy_words_kernel<W, kCopyThreads, 1><<<blocks, kCopyThreads, 0, s>>>(static_cast<const W*>(src),
+                                                                          static_cast<W*>(dst), n);
   return cudaGetLastError();
 }
 
@@ -61,14 +73,14 @@ void* mapped_host(const void* p, size_t bytes) {
   return a0.devicePointer;
 }
 
-cudaError_t launch_copy(const void* src, void* dst, size_t bytes, int sms, cudaStream_t s) {
+cudaError_t launch_copy(const void* src, void* dst, size_t bytes, int sms, bool background, cudaStream_t s) {
   if (bytes == 0) return cudaSuccess;
   const uintptr_t al = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) | (uintptr_t)bytes;
-  if ((al & 15) == 0) return launch_words<uint4>(src, dst, bytes, sms, s);
-  if ((al & 7) == 0) return launch_words<uint2>(src, dst, bytes, sms, s);
-  if ((al & 3) == 0) return launch_words<uint32_t>(src, dst, bytes, sms, s);
-  if ((al & 1) == 0) return launch_words<uint16_t>(src, dst, bytes, sms, s);
-  return launch_words<uint8_t>(src, dst, bytes, sms, s);
+  if ((al & 15) == 0) return launch_words<uint4>(src, dst, bytes, sms, background, s);
+  if ((al & 7) == 0) return launch_words<uint2>(src, dst, bytes, sms, background, s);
+  if ((al & 3) == 0) return launch_words<uint32_t>(src, dst, bytes, sms, background, s);
+  if ((al & 1) == 0) return launch_words<uint16_t>(src, dst, bytes, sms, background, s);
+  return launch_words<uint8_t>(src, dst, bytes, sms, background, s);
 }
 
 }  // namespace kvx
