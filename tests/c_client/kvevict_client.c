@@ -1,14 +1,15 @@
 /* A plain C client of the kvevict C ABI (no Python): one handle driven through
- * the device-buffer path (prefill + decode + read_state) and a second through
- * the host-buffer path (run_host), on the same synthetic keys. Checks:
+ * the device-buffer path (prefill + decode + read_state), a second through the
+ * host-buffer path (run_host) from malloc'd (pageable) memory and a third from
+ * cudaMallocHost (page-locked) memory, on the same synthetic keys. Checks:
  *   - every call returns KVEVICT_OK and the error word stays clear;
  *   - each row keeps min(position, budget) rows, its sinks (positions
  *     0..n_sink-1) in place, positions strictly increasing;
  *   - scores are finite and non-negative, and the kept rows' scores sum to at
  *     most the number of tokens the row has seen (each step adds one softmax,
  *     of mass 1; evicted rows take theirs with them);
- *   - the host-buffer path gives the same evicted slots and the same state bit
- *     for bit.
+ *   - both host-buffer runs give the same evicted slots and the same state
+ *     bit for bit as the device-buffer path.
  * Exit status 0 on success. Build: gcc -std=c11 ... -lkvevict -lcudart. */
 #include <cuda_runtime.h>
 #include <math.h>
@@ -161,26 +162,41 @@ int main(void) {
   int32_t *p1 = (int32_t*)malloc(rowbuf * 4), *p2 = (int32_t*)malloc(rowbuf * 4);
   if (check_rows(h, budgets, S + T, k1, s1, g1, p1, cap)) return 1;
 
-  /* host-buffer path on a second handle: same keys, same results */
-  kvevict_t* h2 = NULL;
-  CHECK(kvevict_create(&cfg, NULL, &h2));
-  CHECK(kvevict_run_host(h2, hpre, S, hdec, T, ev_host_path, NULL));
-  if (memcmp(ev_dev_path, ev_host_path, nev * 4) != 0) {
-    fprintf(stderr, "run_host evicted other slots than the device path\n");
-    return 1;
-  }
-  for (int b = 0; b < B; ++b)
-    for (int l = 0; l < L; ++l)
-      for (int hh = 0; hh < H; ++hh) {
-        int32_t n1 = 0, n2 = 0;
-        CHECK(kvevict_read_state(h, b, l, hh, k1, s1, g1, p1, &n1, NULL));
-        CHECK(kvevict_read_state(h2, b, l, hh, k2, s2, g2, p2, &n2, NULL));
-        if (n1 != n2 || memcmp(k1, k2, (size_t)n1 * D * 2) || memcmp(s1, s2, (size_t)n1 * 4) ||
-            memcmp(g1, g2, (size_t)n1 * 4) || memcmp(p1, p2, (size_t)n1 * 4)) {
-          fprintf(stderr, "row (%d,%d,%d): run_host state differs\n", b, l, hh);
-          return 1;
+  /* host-buffer path on a second handle (pageable buffers) and a third
+   * (page-locked buffers): same keys, same results */
+  uint16_t *lpre = NULL, *ldec = NULL;
+  int32_t* ev_locked = NULL;
+  CUDA(cudaMallocHost((void**)&lpre, npre * 2));
+  CUDA(cudaMallocHost((void**)&ldec, ndec * 2));
+  CUDA(cudaMallocHost((void**)&ev_locked, nev * 4));
+  memcpy(lpre, hpre, npre * 2);
+  memcpy(ldec, hdec, ndec * 2);
+  memset(ev_locked, 0xff, nev * 4);
+  kvevict_t* hosts[2] = {NULL, NULL};
+  for (int v = 0; v < 2; ++v) {
+    int32_t* ev_out = v == 0 ? ev_host_path : ev_locked;
+    CHECK(kvevict_create(&cfg, NULL, &hosts[v]));
+    CHECK(kvevict_run_host(hosts[v], v == 0 ? hpre : lpre, S, v == 0 ? hdec : ldec, T, ev_out, NULL));
+    if (memcmp(ev_dev_path, ev_out, nev * 4) != 0) {
+      fprintf(stderr, "run_host (%s memory) evicted other slots than the device path\n",
+              v == 0 ? "pageable" : "page-locked");
+      return 1;
+    }
+    for (int b = 0; b < B; ++b)
+      for (int l = 0; l < L; ++l)
+        for (int hh = 0; hh < H; ++hh) {
+          int32_t n1 = 0, n2 = 0;
+          CHECK(kvevict_read_state(h, b, l, hh, k1, s1, g1, p1, &n1, NULL));
+          CHECK(kvevict_read_state(hosts[v], b, l, hh, k2, s2, g2, p2, &n2, NULL));
+          if (n1 != n2 || memcmp(k1, k2, (size_t)n1 * D * 2) || memcmp(s1, s2, (size_t)n1 * 4) ||
+              memcmp(g1, g2, (size_t)n1 * 4) || memcmp(p1, p2, (size_t)n1 * 4)) {
+            fprintf(stderr, "row (%d,%d,%d): run_host (%s memory) state differs\n", b, l, hh,
+                    v == 0 ? "pageable" : "page-locked");
+            return 1;
+          }
         }
-      }
+  }
+  kvevict_t* h2 = hosts[0];
 
   /* an invalid call is refused with a message, and the handle keeps working */
   if (kvevict_prefill(h, dpre, S, NULL) != KVEVICT_ERR_BAD_STATE || kvevict_last_error()[0] == '\0') {
@@ -193,6 +209,10 @@ int main(void) {
 
   CHECK(kvevict_destroy(h));
   CHECK(kvevict_destroy(h2));
+  CHECK(kvevict_destroy(hosts[1]));
+  cudaFreeHost(lpre);
+  cudaFreeHost(ldec);
+  cudaFreeHost(ev_locked);
   cudaFree(dpre);
   cudaFree(ddec);
   cudaFree(dev);
