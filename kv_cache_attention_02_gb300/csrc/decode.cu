@@ -217,68 +217,70 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Combine two (max, sum of 2^(x - max)) pairs (logits are kept in base-2 units).
-__device__ __forceinline__ void lse_combine(float& m, float& l, float m2, float l2) {
-  const float mn = fmaxf(m, m2);
-  if (mn == -INFINITY) return;
-  l = (m == -INFINITY ? 0.f : l * ex2(m - mn)) + (m2 == -INFINITY ? 0.f : l2 * ex2(m2 - mn));
-  m = mn;
-}
-
-// Block-wide (max, sum) over the 256 consumer threads.
+// Block-wide (max, sum of 2^(x - max)) over the 256 consumer threads, logits
+// in base-2 units: the block max first (warp shuffles, then every thread
+// combines the eight warp maxima itself), then each thread's running sum
+// rescaled to it once and the sums added the same way. One barrier per half;
+// a row's step waits on this, so the few-row shapes feel every round.
 __device__ void block_lse(float& m, float& l, float* red) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float wm = m;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
-    lse_combine(m, l, m2, l2);
-  }
-  if (lane == 0) { red[w] = m; red[16 + w] = l; }
+  for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+  if (lane == 0) red[w] = wm;
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-  if (w == 0) {
-    m = lane < kConsumerWarps ? red[lane] : -INFINITY;
-    l = lane < kConsumerWarps ? red[16 + lane] : 0.f;
+  float M = red[0];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
-      lse_combine(m, l, m2, l2);
-    }
-    if (lane == 0) { red[32] = m; red[33] = l; }
-  }
+  for (int k = 1; k < kConsumerWarps; ++k) M = fmaxf(M, red[k]);
+  float ls = m == -INFINITY ? 0.f : l * ex2(m - M);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+  if (lane == 0) red[16 + w] = ls;
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-  m = red[32];
-  l = red[33];
+  float L = red[16];
+#pragma unroll
+  for (int k = 1; k < kConsumerWarps; ++k) L += red[16 + k];
+  m = M;
+  l = L;
 }
 
+// Block-wide (r, slot) argmin, lowest slot on ties: warp shuffles, then every
+// thread merges the eight warp candidates itself.
 __device__ int block_argmin(float r, int i, float* redf, int* redi) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   warp_argmin(r, i);
   if (lane == 0) { redf[40 + w] = r; redi[40 + w] = i; }
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-  if (w == 0) {
-    r = lane < kConsumerWarps ? redf[40 + lane] : INFINITY;
-    i = lane < kConsumerWarps ? redi[40 + lane] : INT_MAX;
-    warp_argmin(r, i);
-    if (lane == 0) redi[63] = i;
+  float rb = redf[40];
+  int ib = redi[40];
+#pragma unroll
+  for (int k = 1; k < kConsumerWarps; ++k) {
+    const float r2 = redf[40 + k];
+    const int i2 = redi[40 + k];
+    if (r2 < rb || (r2 == rb && i2 < ib)) { rb = r2; ib = i2; }
   }
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-  return redi[63];
+  return ib;
 }
 
 __device__ __forceinline__ void mbar_arrive_cta(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ int ld_acquire(const int32_t* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void st_release(int32_t* p, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void st_release(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+// A row's published state: steps applied, and the slot its last step evicted
+// (left in place for the next step to compact), -1 for none.
+__device__ __forceinline__ unsigned long long pack_done(int steps, int e_log) {
+  return ((unsigned long long)(unsigned)steps << 32) | (unsigned)(e_log + 1);
+}
+__device__ __forceinline__ int done_steps(unsigned long long w) { return (int)(w >> 32); }
+__device__ __forceinline__ int done_pending(unsigned long long w) { return (int)(unsigned)(w & 0xffffffffull) - 1; }
 // Order this thread's later async-proxy (TMA) reads of global memory after the
 // generic-proxy writes it has synchronised with.
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -401,19 +403,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
         if (values)
           reinterpret_cast<Word*>(slot + 64 + G::ROWB)[lane] = reinterpret_cast<const Word*>(a.v_new + src)[lane];
         if (lane == 0) {
-          // step t of this row needs step t - 1 applied (by whichever CTA ran it)
-          if (t > 0 && ld_acquire(a.done + row) < a.s0 + t) {
-            const uint64_t t0 = global_timer_ns();
-            while (ld_acquire(a.done + row) < a.s0 + t) {
-              if (*abort_flag) { ready = false; break; }
-              if (global_timer_ns() - t0 > kWaitLimitNs) {
-                *abort_flag = 1;
-                atomicOr(a.err, kErrWaitTimeout);
-                ready = false;
-                break;
-              }
-            }
-          }
+          // What does not depend on the row's previous step is staged before
+          // waiting for it (the Gumbel value's fp64 logs are slow on this GPU
+          // and would otherwise lengthen each row's step-to-step chain).
           const LayerInfo li = a.layers[l];
           const int64_t p = a.p0 + t;
           hd->kbase = li.row_base + (int64_t)rem * li.cap;
@@ -422,11 +414,32 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
           hd->head = row;
           hd->t = t;
           hd->n = (int)(p < (int64_t)li.budget ? p : (int64_t)li.budget);
-          hd->e_prev = __ldcg(a.pend + row);
           hd->budget = li.budget;
           hd->capm = li.capm;
           hd->gnew = gumbel_at(a.seed, l, hh, p);
           hd->tau = tau_at(a, p);
+          // step t of this row needs step t - 1 applied (by whichever CTA ran
+          // it); that step's published word also carries the slot it left to
+          // compact. A launch's first step takes it from the pending array
+          // (written by the previous launch, the prompt, or a flush).
+          if (t > 0) {
+            unsigned long long w = ld_acquire(a.done + row);
+            if (done_steps(w) < a.s0 + t) {
+              const uint64_t t0 = global_timer_ns();
+              while (done_steps(w = ld_acquire(a.done + row)) < a.s0 + t) {
+                if (*abort_flag) { ready = false; break; }
+                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                  *abort_flag = 1;
+                  atomicOr(a.err, kErrWaitTimeout);
+                  ready = false;
+                  break;
+                }
+              }
+            }
+            hd->e_prev = done_pending(w);
+          } else {
+            hd->e_prev = __ldcg(a.pend + row);
+          }
         }
         ready = __shfl_sync(0xffffffffu, ready, 0);
       } else if (lane == 0) {
@@ -701,11 +714,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
           *reinterpret_cast<Chunk*>(vd + HALF + c * CH) = v_hi;
         }
       }
+      const int e_log_out = evict ? R_e - ((shift && R_e > e_prev) ? 1 : 0) : -1;   // slot after compaction
       if (tid == 0) {
         const int head = hd.head;
         gg[n] = gnew;
         pg[n] = (int32_t)hd.p;
-        const int e_log = evict ? R_e - ((shift && R_e > e_prev) ? 1 : 0) : -1;
+        const int e_log = e_log_out;
         a.pend[head] = e_log;
         if (a.evicted) {
           const int l = head / BH;
@@ -723,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
       // what precedes it in causality order), so no separate fence is needed
       // for a CTA that acquires the counter to see them.
       consumers_sync();
-      if (tid == 0) st_release(a.done + hd.head, a.s0 + hd.t + 1);
+      if (tid == 0) st_release(a.done + hd.head, pack_done(a.s0 + hd.t + 1, e_log_out));
       if (lane == 0) {
         for (int k = 0; k < P.nm; ++k) mbar_arrive_cta(empty((um + k) % kStages));
         mbar_arrive_cta(rempty(q));

@@ -49,7 +49,9 @@ struct DecodeArgs {
   float* gum;
   int32_t* pos;
   int32_t* pend;
-  int32_t* done;           // [rows] decode steps applied to each row since reset
+  // [rows] per row: (decode steps applied since reset) << 32 | (slot the last
+  // step evicted and left in place + 1, 0 for none), one release store per step
+  unsigned long long* done;
   int32_t* evicted;        // [T, B, L, H] user layout (ev_step apart), or null
   int64_t ev_step;
   const LayerInfo* layers;
@@ -128,7 +130,7 @@ cudaError_t decode_step_setup(int D, size_t smem);
 size_t decode_step_smem(int D, int capm_max);
 // One launch runs a.T decode steps: persistent CTAs (grid = CTAs per SM x SMs,
 // at most one per row) claim (step, row) pairs in order from a.ticket; a row's
-// step t waits until a.done[row] shows step t - 1 applied.
+// step t waits until the high half of a.done[row] shows step t - 1 applied.
 cudaError_t decode_step_ctas_per_sm(int D, size_t smem, int* ctas);
 cudaError_t launch_decode_step(const DecodeArgs& a, int D, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_flush(const FlushArgs& a, int D, int heads, cudaStream_t s);

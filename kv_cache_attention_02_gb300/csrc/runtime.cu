@@ -106,7 +106,7 @@ struct kvevict {
   int64_t next_pos = 0;
   bool stepped = false;
   size_t bytes = 0;
-  int32_t* done = nullptr;  // [heads] decode steps applied to each row since reset
+  unsigned long long* done = nullptr;  // [heads] steps applied << 32 | pending slot + 1
   int64_t dsteps = 0;       // decode steps launched since reset (every row takes each one)
   bool stall_next = false;  // test hook (kvevict_test_stall_next_step)
   // host pipeline staging
@@ -457,7 +457,7 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
   KV_CUDA_CREATE(cudaMemcpy(h->d_layers, h->layers.data(), h->layers.size() * sizeof(LayerInfo),
                             cudaMemcpyHostToDevice));
   KV_CUDA_CREATE(cudaMemsetAsync(h->pend, 0xFF, (size_t)h->heads * 4, s));
-  KV_CUDA_CREATE(cudaMemsetAsync(h->done, 0, (size_t)h->heads * 4, s));
+  KV_CUDA_CREATE(cudaMemsetAsync(h->done, 0, (size_t)h->heads * 8, s));
   KV_CUDA_CREATE(cudaMemsetAsync(h->err, 0, sizeof(int), s));
   KV_CUDA_CREATE(cudaMemsetAsync(h->ticket, 0, sizeof(unsigned long long), s));
   KV_CUDA_CREATE(cudaStreamSynchronize(s));
@@ -478,7 +478,7 @@ int kvevict_reset(kvevict_t* h, void* stream) {
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   cudaStream_t s = (cudaStream_t)stream;
   KV_CUDA(cudaMemsetAsync(h->pend, 0xFF, (size_t)h->heads * 4, s));
-  KV_CUDA(cudaMemsetAsync(h->done, 0, (size_t)h->heads * 4, s));
+  KV_CUDA(cudaMemsetAsync(h->done, 0, (size_t)h->heads * 8, s));
   KV_CUDA(cudaMemsetAsync(h->err, 0, sizeof(int), s));
   KV_CUDA(cudaMemsetAsync(h->ticket, 0, sizeof(unsigned long long), s));   // left set by an aborted launch
   h->next_pos = 0;
