@@ -16,7 +16,10 @@ namespace kvx {
 namespace {
 
 // ---------------------------------------------------------------- bulk eviction
-constexpr int kSThreads = 1024;
+// 256 threads a CTA, four CTAs an SM: while one CTA sorts (barrier-bound,
+// no HBM traffic) the others move rows.
+constexpr int kSThreads = 256;
+constexpr int kSWarps = kSThreads / 32;
 
 __device__ __forceinline__ uint32_t ordered_bits(float f) {
   const uint32_t u = __float_as_uint(f);
@@ -24,7 +27,7 @@ __device__ __forceinline__ uint32_t ordered_bits(float f) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kSThreads) prefill_select_kernel(const PrefillSelectArgs a) {
+__global__ void __launch_bounds__(kSThreads, 4) prefill_select_kernel(const PrefillSelectArgs a) {
   constexpr int CH = D / 16, HALF = D / 2;
   using Chunk = typename std::conditional<CH == 8, uint4, uint2>::type;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -51,20 +54,39 @@ __global__ void __launch_bounds__(kSThreads) prefill_select_kernel(const Prefill
   const int budget = li.budget;
   const int c = tid & 7;
 
+  // Rows move 8 threads to a row, kRowsInFlight rows per thread per round:
+  // every load of a round is issued before the first store, so a thread keeps
+  // several HBM reads in flight instead of one (as many as fit in the 64
+  // registers a thread has at four 256-thread CTAs an SM).
+  constexpr int RPP = kSThreads / 8;   // rows per pass
+  constexpr int kRowsInFlight = D == 128 ? 3 : 4;
+
   if (S <= budget) {  // the whole prompt fits: keep every row where it is
-    for (int j0 = 0; j0 < S; j0 += kSThreads / 8) {
-      const int j = j0 + (tid >> 3);
-      if (j < S) {
-        const Chunk lo = *reinterpret_cast<const Chunk*>(src + (size_t)j * D + c * CH);
-        const Chunk hi2 = *reinterpret_cast<const Chunk*>(src + (size_t)j * D + HALF + c * CH);
-        *reinterpret_cast<Chunk*>(Kg + (size_t)j * D + c * CH) = lo;
-        *reinterpret_cast<Chunk*>(Kg + (size_t)j * D + HALF + c * CH) = hi2;
-        if (c == 0) { scg[j] = col[j]; gg[j] = gs[j]; pg[j] = j; }
-        if (Vg) {
-          *reinterpret_cast<Chunk*>(Vg + (size_t)j * D + c * CH) =
-              *reinterpret_cast<const Chunk*>(vsrc + (size_t)j * D + c * CH);
-          *reinterpret_cast<Chunk*>(Vg + (size_t)j * D + HALF + c * CH) =
-              *reinterpret_cast<const Chunk*>(vsrc + (size_t)j * D + HALF + c * CH);
+    for (int j0 = 0; j0 < S; j0 += RPP * kRowsInFlight) {
+      Chunk lo[kRowsInFlight], hi2[kRowsInFlight];
+      float sv[kRowsInFlight], gv[kRowsInFlight];
+#pragma unroll
+      for (int u = 0; u < kRowsInFlight; ++u) {
+        const int j = j0 + u * RPP + (tid >> 3);
+        if (j < S) {
+          lo[u] = *reinterpret_cast<const Chunk*>(src + (size_t)j * D + c * CH);
+          hi2[u] = *reinterpret_cast<const Chunk*>(src + (size_t)j * D + HALF + c * CH);
+          if (c == 0) { sv[u] = col[j]; gv[u] = gs[j]; }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kRowsInFlight; ++u) {
+        const int j = j0 + u * RPP + (tid >> 3);
+        if (j < S) {
+          *reinterpret_cast<Chunk*>(Kg + (size_t)j * D + c * CH) = lo[u];
+          *reinterpret_cast<Chunk*>(Kg + (size_t)j * D + HALF + c * CH) = hi2[u];
+          if (c == 0) { scg[j] = sv[u]; gg[j] = gv[u]; pg[j] = j; }
+          if (Vg) {
+            *reinterpret_cast<Chunk*>(Vg + (size_t)j * D + c * CH) =
+                *reinterpret_cast<const Chunk*>(vsrc + (size_t)j * D + c * CH);
+            *reinterpret_cast<Chunk*>(Vg + (size_t)j * D + HALF + c * CH) =
+                *reinterpret_cast<const Chunk*>(vsrc + (size_t)j * D + HALF + c * CH);
+          }
         }
       }
     }
@@ -124,7 +146,7 @@ __global__ void __launch_bounds__(kSThreads) prefill_select_kernel(const Prefill
   if (lane == 31) wsum[wid] = incl;
   __syncthreads();
   if (wid == 0) {
-    int v = wsum[lane];
+    int v = lane < kSWarps ? wsum[lane] : 0;
     int iv = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -142,18 +164,31 @@ __global__ void __launch_bounds__(kSThreads) prefill_select_kernel(const Prefill
   __syncthreads();
 
   // write survivors, each re-rotated by (new slot - old slot)
-  for (int j0 = 0; j0 < S; j0 += kSThreads / 8) {
-    const int j = j0 + (tid >> 3);
-    if (j < S && !flag[j]) {
+  for (int j0 = 0; j0 < S; j0 += RPP * kRowsInFlight) {
+    Chunk lo[kRowsInFlight], hi2[kRowsInFlight];
+    float sv[kRowsInFlight], gv[kRowsInFlight];
+    bool live[kRowsInFlight];
+#pragma unroll
+    for (int u = 0; u < kRowsInFlight; ++u) {
+      const int j = j0 + u * RPP + (tid >> 3);
+      live[u] = j < S && !flag[j];
+      if (live[u]) {
+        lo[u] = *reinterpret_cast<const Chunk*>(src + (size_t)j * D + c * CH);
+        hi2[u] = *reinterpret_cast<const Chunk*>(src + (size_t)j * D + HALF + c * CH);
+        if (c == 0) { sv[u] = col[j]; gv[u] = gs[j]; }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRowsInFlight; ++u) {
+      if (!live[u]) continue;
+      const int j = j0 + u * RPP + (tid >> 3);
       const int ns = newslot[j];
       const int d = j - ns;   // shift back by d positions
-      Chunk lo = *reinterpret_cast<const Chunk*>(src + (size_t)j * D + c * CH);
-      Chunk hi2 = *reinterpret_cast<const Chunk*>(src + (size_t)j * D + HALF + c * CH);
       if (d > 0) {
         const float* tc = a.rope_c + (size_t)d * HALF + c * CH;
         const float* ts = a.rope_s + (size_t)d * HALF + c * CH;
-        __half2* h_lo = reinterpret_cast<__half2*>(&lo);
-        __half2* h_hi = reinterpret_cast<__half2*>(&hi2);
+        __half2* h_lo = reinterpret_cast<__half2*>(&lo[u]);
+        __half2* h_hi = reinterpret_cast<__half2*>(&hi2[u]);
 #pragma unroll
         for (int k = 0; k < CH / 2; ++k) {
           const float2 fa = __half22float2(h_lo[k]);
@@ -167,9 +202,9 @@ __global__ void __launch_bounds__(kSThreads) prefill_select_kernel(const Prefill
           h_hi[k] = __halves2half2(__float2half_rn(y0), __float2half_rn(y1));
         }
       }
-      *reinterpret_cast<Chunk*>(Kg + (size_t)ns * D + c * CH) = lo;
-      *reinterpret_cast<Chunk*>(Kg + (size_t)ns * D + HALF + c * CH) = hi2;
-      if (c == 0) { scg[ns] = col[j]; gg[ns] = gs[j]; pg[ns] = j; }
+      *reinterpret_cast<Chunk*>(Kg + (size_t)ns * D + c * CH) = lo[u];
+      *reinterpret_cast<Chunk*>(Kg + (size_t)ns * D + HALF + c * CH) = hi2[u];
+      if (c == 0) { scg[ns] = sv[u]; gg[ns] = gv[u]; pg[ns] = j; }
       if (Vg) {   // value rows move with their keys, never rotated
         *reinterpret_cast<Chunk*>(Vg + (size_t)ns * D + c * CH) =
             *reinterpret_cast<const Chunk*>(vsrc + (size_t)j * D + c * CH);
