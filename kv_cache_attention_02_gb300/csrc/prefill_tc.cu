@@ -217,6 +217,26 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   }
 }
 
+
+// Two f32 lanes per instruction (sm_100+ packed FP32): the same per-lane
+// rounding as fmaf / a + b.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
 template <int D, bool COLSUM>
 __global__ void __launch_bounds__(kTCThreads, 2)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const PrefillScoreArgs a) {
@@ -324,7 +344,7 @@ __global__ void __launch_bounds__(kTCThreads, 2)
     const int rowA = ablk * kTB + r;              // query row i (pass 1) / key row j (pass 2)
     const int et = tid - 64 - wg * kTB;           // 0..127 within the warpgroup
     const float* lse_h = a.lse2 + (size_t)head * a.Sp;
-    constexpr int CW = COLSUM ? 32 : 64;          // accumulator columns per TMEM read
+    constexpr int CW = 64;                        // accumulator columns per TMEM read
     float run_m = -INFINITY, run_l = 0.f, csum = 0.f;
     for (int k = wg; k < nblk; k += 2) {
       const int colB0 = (first + k) * kTB;
@@ -364,32 +384,48 @@ __global__ void __launch_bounds__(kTCThreads, 2)
           if (cm != -INFINITY) {
             const float mn = fmaxf(run_m, cm * a.scale2);
             const float nm = -mn;
-            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+            const float2 sc2 = make_float2(a.scale2, a.scale2), nm2 = make_float2(nm, nm);
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);   // sums of e % 4 = 0, 1 | 2, 3
 #pragma unroll
-            for (int e = 0; e < CW; ++e) s4[e & 3] += ex2(fmaf(v[e], a.scale2, nm));
-            run_l = run_l * ex2(run_m - mn) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+            for (int e = 0; e < CW; e += 4) {
+              const float2 t0 = ffma2(make_float2(v[e], v[e + 1]), sc2, nm2);
+              const float2 t1 = ffma2(make_float2(v[e + 2], v[e + 3]), sc2, nm2);
+              acc0 = fadd2(acc0, make_float2(ex2(t0.x), ex2(t0.y)));
+              acc1 = fadd2(acc1, make_float2(ex2(t1.x), ex2(t1.y)));
+            }
+            run_l = run_l * ex2(run_m - mn) + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
             run_m = mn;
           }
         } else {
-          float nl[CW];   // -lse2 of the chunk's queries (16-byte broadcast loads)
-#pragma unroll
-          for (int e = 0; e < CW; e += 4) {
-            const float4 t = *reinterpret_cast<const float4*>(lse_s + b * kTB + c * CW + e);
-            nl[e] = t.x;
-            nl[e + 1] = t.y;
-            nl[e + 2] = t.z;
-            nl[e + 3] = t.w;
-          }
+          // -lse2 of the chunk's queries, read as 16-byte broadcasts where used
+          const float* nlp = lse_s + b * kTB + c * CW;
           float s4[4] = {0.f, 0.f, 0.f, 0.f};
           if (full_tile) {
+            const float2 sc2 = make_float2(a.scale2, a.scale2);
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int e = 0; e < CW; ++e) s4[e & 3] += ex2(fmaf(v[e], a.scale2, nl[e]));
+            for (int e = 0; e < CW; e += 4) {
+              const float4 nl = *reinterpret_cast<const float4*>(nlp + e);
+              const float2 t0 = ffma2(make_float2(v[e], v[e + 1]), sc2, make_float2(nl.x, nl.y));
+              const float2 t1 = ffma2(make_float2(v[e + 2], v[e + 3]), sc2, make_float2(nl.z, nl.w));
+              acc0 = fadd2(acc0, make_float2(ex2(t0.x), ex2(t0.y)));
+              acc1 = fadd2(acc1, make_float2(ex2(t1.x), ex2(t1.y)));
+            }
+            s4[0] = acc0.x;
+            s4[1] = acc0.y;
+            s4[2] = acc1.x;
+            s4[3] = acc1.y;
           } else {
 #pragma unroll
-            for (int e = 0; e < CW; ++e) {
-              const int i = c0 + e;
-              const float p = ex2(fmaf(v[e], a.scale2, nl[e]));
-              s4[e & 3] += (i >= rowA && i < S) ? p : 0.f;
+            for (int e = 0; e < CW; e += 4) {
+              const float4 nl = *reinterpret_cast<const float4*>(nlp + e);
+              const float n4[4] = {nl.x, nl.y, nl.z, nl.w};
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int i = c0 + e + u;
+                const float p = ex2(fmaf(v[e + u], a.scale2, n4[u]));
+                s4[u] += (i >= rowA && i < S) ? p : 0.f;
+              }
             }
           }
           csum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
