@@ -6,7 +6,13 @@ or none, cumulative or current-step scores, bulk or sequential prompts, constant
 or annealed tau, and budgets and prompt lengths placed on and around the
 64-row tile boundaries of the decode step and the 128-row blocks of the prompt
 scorer.
+
+The counts and the seed can be raised for a longer soak without changing the
+defaults: KVEVICT_RANDOM_SMALL / KVEVICT_RANDOM_MEDIUM (cases of each kind)
+and KVEVICT_RANDOM_SEED (small cases use it, medium cases it + 1).
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -49,7 +55,12 @@ def _draw(i, rng, orc):
                         prefill_mode=prefill_mode)
 
 
-def _cases(n=32, seed=2026):
+_SEED = os.environ.get("KVEVICT_RANDOM_SEED")
+_N_SMALL = int(os.environ.get("KVEVICT_RANDOM_SMALL", "32"))
+_N_MEDIUM = int(os.environ.get("KVEVICT_RANDOM_MEDIUM", "8"))
+
+
+def _cases(n=_N_SMALL, seed=int(_SEED) if _SEED else 2026):
     import oracle as orc
     rng = np.random.default_rng(seed)
     return [_draw(i, rng, orc) for i in range(n)]
@@ -67,7 +78,7 @@ def test_random_config_all_rows(wl):
     compare_rows(orc, wl, rows, *res)
 
 
-def _medium_cases(n=8, seed=4051):
+def _medium_cases(n=_N_MEDIUM, seed=int(_SEED) + 1 if _SEED else 4051):
     """More rows than the decode step runs CTAs (up to 2 per SM), budgets of several
     tiles: every CTA claims several rows per step, of mixed lengths."""
     import oracle as orc
