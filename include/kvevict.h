@@ -234,6 +234,32 @@ int kvevict_layer_budget(const kvevict_t* h, int32_t l, int32_t* budget);
 /* Device bytes held by the handle (arena + scratch + staging). */
 int kvevict_device_bytes(const kvevict_t* h, size_t* bytes);
 
+/* Checkpoint and resume. The pages keep the state in an immutable object
+ * returned by each call (page "veloxquant_mlx.quantizers.keyformer module",
+ * KeyformerState); here it lives in the handle's device arena, and these calls
+ * copy it to and from host memory. A snapshot holds every row's keys (and
+ * values), scores, Gumbel values and positions, the next position and whether
+ * a decode step has run, plus the handle's shape, layer budgets and method
+ * parameters (n_sink, recent, score mode, tau schedule, RoPE base, seed); the
+ * frozen Gumbel values depend only on (seed, layer, head, position), so a
+ * resumed handle continues exactly as the saved one would have.
+ *
+ * kvevict_state_bytes: size of a snapshot of this handle.
+ * kvevict_save_state: applies any pending compaction (as kvevict_flush), then
+ *   copies the state into buf (host memory, at least kvevict_state_bytes
+ *   bytes, caller-owned); returns after the stream has finished. Errors:
+ *   INVALID_ARG (null, buffer too small), CUDA, DEVICE_CHECK (the handle's
+ *   error word is set; buf's contents are then unspecified).
+ * kvevict_load_state: replaces this handle's state with the snapshot in buf
+ *   (host memory, bytes long); returns after the stream has finished, so buf
+ *   may be freed. The handle must have the snapshot's batch, layers, KV heads,
+ *   head_dim, value rows, layer budgets and method parameters; max_prefill and
+ *   prefill_mode may differ. Errors: INVALID_ARG (not a snapshot, a size or
+ *   configuration mismatch; the handle is unchanged), CUDA. */
+int kvevict_state_bytes(const kvevict_t* h, size_t* bytes);
+int kvevict_save_state(kvevict_t* h, void* buf, size_t bytes, void* stream);
+int kvevict_load_state(kvevict_t* h, const void* buf, size_t bytes, void* stream);
+
 /* Prompt scoring that allocates nothing. The paper has no counterpart: this is
  * for callers that cannot call cudaMalloc -- an inference engine that reserves
  * the whole device heap for its own memory pool at start-up (a further

@@ -68,6 +68,9 @@ SIGNATURES = {
     "kvevict_next_pos": (ctypes.c_int, [P, P]),
     "kvevict_layer_budget": (ctypes.c_int, [P, i32, P]),
     "kvevict_device_bytes": (ctypes.c_int, [P, P]),
+    "kvevict_state_bytes": (ctypes.c_int, [P, P]),
+    "kvevict_save_state": (ctypes.c_int, [P, P, ctypes.c_size_t, P]),
+    "kvevict_load_state": (ctypes.c_int, [P, P, ctypes.c_size_t, P]),
     "kvevict_last_error": (ctypes.c_char_p, []),
     "kvevict_prefill_scores_noalloc": (ctypes.c_int, [P, i32, i32, i32, P, P]),
 }
@@ -262,6 +265,25 @@ class KVEvict:
         v = ctypes.c_size_t(0)
         _check(lib().kvevict_device_bytes(self._h, ctypes.addressof(v)))
         return v.value
+
+    # ------------------------------------------------------- checkpoint / resume
+    def state_bytes(self) -> int:
+        v = ctypes.c_size_t(0)
+        _check(lib().kvevict_state_bytes(self._h, ctypes.addressof(v)))
+        return v.value
+
+    def save_state(self, out=None, stream=None) -> np.ndarray:
+        """Snapshot of the cache state as a uint8 host array (or into `out`)."""
+        n = self.state_bytes()
+        buf = np.empty(n, np.uint8) if out is None else out
+        assert buf.dtype == np.uint8 and buf.flags["C_CONTIGUOUS"] and buf.size >= n
+        _check(lib().kvevict_save_state(self._h, buf.ctypes.data, buf.size, _stream(stream)))
+        return buf
+
+    def load_state(self, snapshot, stream=None):
+        """Replace the cache state with a snapshot from save_state."""
+        buf = np.ascontiguousarray(snapshot, dtype=np.uint8)
+        _check(lib().kvevict_load_state(self._h, buf.ctypes.data, buf.size, _stream(stream)))
 
 
 def from_workload(wl, stream=None, with_values=False) -> KVEvict:

@@ -5,11 +5,14 @@
 #include "kvevict.h"
 #include "kvevict_internal.cuh"
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <climits>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <string>
+#include <utility>
 #include <vector>
 
 using kvx::LayerInfo;
@@ -17,6 +20,16 @@ using kvx::LayerInfo;
 namespace {
 
 thread_local std::string g_last_error;
+
+// An NVTX range around each entry point, named after it, for profilers
+// (`ncu --nvtx`, Nsight Systems); without a tool attached it costs a branch.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define KV_RANGE() NvtxRange kv_range_(__func__)
 
 int fail(int code, const std::string& msg) {
   g_last_error = msg;
@@ -319,6 +332,7 @@ int kvevict_budgets(int32_t n_layers, int32_t avg_budget, int32_t n_sink, double
 }
 
 int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
+  KV_RANGE();
   g_last_error.clear();
   if (!cfg || !out) return fail(KVEVICT_ERR_INVALID_ARG, "cfg and out must not be null");
   const kvevict_config& c = *cfg;
@@ -467,6 +481,7 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
 }
 
 int kvevict_destroy(kvevict_t* h) {
+  KV_RANGE();
   if (!h) return KVEVICT_OK;
   cudaDeviceSynchronize();
   free_all(h);
@@ -475,6 +490,7 @@ int kvevict_destroy(kvevict_t* h) {
 }
 
 int kvevict_reset(kvevict_t* h, void* stream) {
+  KV_RANGE();
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   cudaStream_t s = (cudaStream_t)stream;
   KV_CUDA(cudaMemsetAsync(h->pend, 0xFF, (size_t)h->heads * 4, s));
@@ -547,23 +563,27 @@ int with_values(const kvevict* h) {
 extern "C" {
 
 int kvevict_prefill_ex(kvevict_t* h, const uint16_t* keys, int32_t S, int32_t* evicted, void* stream) {
+  KV_RANGE();
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   if (int rc = keys_only(h)) return rc;
   return prefill_impl(h, keys, nullptr, S, evicted, stream);
 }
 
 int kvevict_prefill(kvevict_t* h, const uint16_t* keys, int32_t S, void* stream) {
+  KV_RANGE();
   return kvevict_prefill_ex(h, keys, S, nullptr, stream);
 }
 
 int kvevict_prefill_kv(kvevict_t* h, const uint16_t* keys, const uint16_t* values, int32_t S,
                        int32_t* evicted, void* stream) {
+  KV_RANGE();
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   if (int rc = with_values(h)) return rc;
   return prefill_impl(h, keys, values, S, evicted, stream);
 }
 
 int kvevict_step(kvevict_t* h, const uint16_t* k_new, int32_t* evicted, void* stream) {
+  KV_RANGE();
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   if (int rc = keys_only(h)) return rc;
   return step_impl(h, k_new, nullptr, evicted, stream);
@@ -571,12 +591,14 @@ int kvevict_step(kvevict_t* h, const uint16_t* k_new, int32_t* evicted, void* st
 
 int kvevict_step_kv(kvevict_t* h, const uint16_t* k_new, const uint16_t* v_new, int32_t* evicted,
                     void* stream) {
+  KV_RANGE();
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   if (int rc = with_values(h)) return rc;
   return step_impl(h, k_new, v_new, evicted, stream);
 }
 
 int kvevict_decode(kvevict_t* h, const uint16_t* keys, int32_t T, int32_t* evicted, void* stream) {
+  KV_RANGE();
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   if (int rc = keys_only(h)) return rc;
   return decode_impl(h, keys, nullptr, T, evicted, stream);
@@ -584,6 +606,7 @@ int kvevict_decode(kvevict_t* h, const uint16_t* keys, int32_t T, int32_t* evict
 
 int kvevict_decode_kv(kvevict_t* h, const uint16_t* keys, const uint16_t* values, int32_t T,
                       int32_t* evicted, void* stream) {
+  KV_RANGE();
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   if (int rc = with_values(h)) return rc;
   return decode_impl(h, keys, values, T, evicted, stream);
@@ -591,6 +614,7 @@ int kvevict_decode_kv(kvevict_t* h, const uint16_t* keys, const uint16_t* values
 
 int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, const uint16_t* decode_keys,
                      int32_t T, int32_t* evicted, void* stream) {
+  KV_RANGE();
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   if (S < 0 || S > h->cfg.max_prefill || T < 0) return fail(KVEVICT_ERR_INVALID_ARG, "bad S or T");
   if ((S > 0 && !prefill_keys) || (T > 0 && !decode_keys)) return fail(KVEVICT_ERR_INVALID_ARG, "null keys");
@@ -701,6 +725,7 @@ int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, cons
 
 int kvevict_read_state(kvevict_t* h, int32_t b, int32_t l, int32_t head, uint16_t* keys, float* scores,
                        float* gumbel, int32_t* positions, int32_t* n_kept, void* stream) {
+  KV_RANGE();
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   if (b < 0 || b >= h->B || l < 0 || l >= h->L || head < 0 || head >= h->H)
     return fail(KVEVICT_ERR_INVALID_ARG, "row index out of range");
@@ -730,12 +755,14 @@ int kvevict_test_stall_next_step(kvevict_t* h) {
 }
 
 int kvevict_flush(kvevict_t* h, void* stream) {
+  KV_RANGE();
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   return enqueue_flush(h, (cudaStream_t)stream);
 }
 
 int kvevict_read_values(kvevict_t* h, int32_t b, int32_t l, int32_t head, uint16_t* values,
                         int32_t* n_kept, void* stream) {
+  KV_RANGE();
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   if (int rc = with_values(h)) return rc;
   if (b < 0 || b >= h->B || l < 0 || l >= h->L || head < 0 || head >= h->H)
@@ -755,6 +782,7 @@ int kvevict_read_values(kvevict_t* h, int32_t b, int32_t l, int32_t head, uint16
 }
 
 int kvevict_check(kvevict_t* h, void* stream) {
+  KV_RANGE();
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   return check_error_word(h, (cudaStream_t)stream);
 }
@@ -776,6 +804,146 @@ int kvevict_device_bytes(const kvevict_t* h, size_t* bytes) {
   if (!h || !bytes) return fail(KVEVICT_ERR_INVALID_ARG, "null argument");
   *bytes = h->bytes + 2 * h->stage_elems * 2 + 2 * h->ev_stage_elems * 4;
   return KVEVICT_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// ---------------------------------------------------------------- snapshots
+// A snapshot is this header, the layer budgets, then the key arena, the value
+// arena (value-carrying handles), scores, Gumbel values and positions, each
+// array whole (kept rows and unused tail alike), in host byte order. It is
+// taken after a flush, so no compaction is pending in it.
+struct SnapHeader {
+  char magic[8];            // "KVEVSNP1"
+  uint32_t version;         // 1
+  uint32_t header_bytes;    // sizeof(SnapHeader)
+  int32_t batch, n_layers, n_kv_heads, head_dim, with_values, n_sink, recent, score_mode;
+  int32_t anneal_steps, stepped;
+  float tau_init, tau_end;
+  double rope_theta;
+  uint64_t seed;
+  int64_t next_pos;
+  int64_t total_rows, total_meta;
+  uint64_t payload_bytes;   // everything after the header
+};
+constexpr char kSnapMagic[8] = {'K', 'V', 'E', 'V', 'S', 'N', 'P', '1'};
+
+size_t snap_payload(const kvevict* h) {
+  const size_t keys = (size_t)h->total_rows * h->D * 2;
+  return (size_t)h->L * 4 + keys * (h->V ? 2 : 1) + (size_t)h->total_meta * 4 * 3;
+}
+
+SnapHeader snap_header(const kvevict* h) {
+  SnapHeader sh{};
+  std::memcpy(sh.magic, kSnapMagic, 8);
+  sh.version = 1;
+  sh.header_bytes = sizeof(SnapHeader);
+  sh.batch = h->B;
+  sh.n_layers = h->L;
+  sh.n_kv_heads = h->H;
+  sh.head_dim = h->D;
+  sh.with_values = h->V ? 1 : 0;
+  sh.n_sink = h->cfg.n_sink;
+  sh.recent = h->cfg.recent;
+  sh.score_mode = h->cfg.score_mode;
+  sh.anneal_steps = h->cfg.anneal_steps;
+  sh.stepped = h->stepped ? 1 : 0;
+  sh.tau_init = h->cfg.tau_init;
+  sh.tau_end = h->cfg.tau_end;
+  sh.rope_theta = h->cfg.rope_theta;
+  sh.seed = h->cfg.seed;
+  sh.next_pos = h->next_pos;
+  sh.total_rows = h->total_rows;
+  sh.total_meta = h->total_meta;
+  sh.payload_bytes = snap_payload(h);
+  return sh;
+}
+
+// The device arrays of a snapshot in file order: (device pointer, bytes).
+std::vector<std::pair<void*, size_t>> snap_arrays(kvevict* h) {
+  std::vector<std::pair<void*, size_t>> v;
+  const size_t keys = (size_t)h->total_rows * h->D * 2, meta = (size_t)h->total_meta * 4;
+  v.emplace_back(h->K, keys);
+  if (h->V) v.emplace_back(h->V, keys);
+  v.emplace_back(h->score, meta);
+  v.emplace_back(h->gum, meta);
+  v.emplace_back(h->pos, meta);
+  return v;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvevict_state_bytes(const kvevict_t* h, size_t* bytes) {
+  if (!h || !bytes) return fail(KVEVICT_ERR_INVALID_ARG, "null argument");
+  *bytes = sizeof(SnapHeader) + snap_payload(h);
+  return KVEVICT_OK;
+}
+
+int kvevict_save_state(kvevict_t* h, void* buf, size_t bytes, void* stream) {
+  KV_RANGE();
+  if (!h || !buf) return fail(KVEVICT_ERR_INVALID_ARG, "null argument");
+  const size_t need = sizeof(SnapHeader) + snap_payload(h);
+  if (bytes < need) return fail(KVEVICT_ERR_INVALID_ARG, "buffer smaller than kvevict_state_bytes");
+  cudaStream_t s = (cudaStream_t)stream;
+  int rc = enqueue_flush(h, s);   // no compaction left pending in the snapshot
+  if (rc != KVEVICT_OK) return rc;
+  unsigned char* out = static_cast<unsigned char*>(buf);
+  const SnapHeader sh = snap_header(h);
+  std::memcpy(out, &sh, sizeof sh);
+  size_t off = sizeof sh;
+  std::memcpy(out + off, h->budgets.data(), (size_t)h->L * 4);
+  off += (size_t)h->L * 4;
+  for (const auto& a : snap_arrays(h)) {
+    KV_CUDA(cudaMemcpyAsync(out + off, a.first, a.second, cudaMemcpyDeviceToHost, s));
+    off += a.second;
+  }
+  return check_error_word(h, s);   // synchronises the stream
+}
+
+int kvevict_load_state(kvevict_t* h, const void* buf, size_t bytes, void* stream) {
+  KV_RANGE();
+  if (!h || !buf) return fail(KVEVICT_ERR_INVALID_ARG, "null argument");
+  if (bytes < sizeof(SnapHeader)) return fail(KVEVICT_ERR_INVALID_ARG, "buffer too small for a snapshot header");
+  SnapHeader sh;
+  std::memcpy(&sh, buf, sizeof sh);
+  const SnapHeader mine = snap_header(h);
+  if (std::memcmp(sh.magic, kSnapMagic, 8) != 0 || sh.version != 1 || sh.header_bytes != sizeof(SnapHeader))
+    return fail(KVEVICT_ERR_INVALID_ARG, "not a kvevict snapshot (magic, version or header size)");
+  if (bytes < sizeof sh + sh.payload_bytes || sh.payload_bytes != mine.payload_bytes)
+    return fail(KVEVICT_ERR_INVALID_ARG, "snapshot size does not match this handle");
+  if (sh.batch != mine.batch || sh.n_layers != mine.n_layers || sh.n_kv_heads != mine.n_kv_heads ||
+      sh.head_dim != mine.head_dim || sh.with_values != mine.with_values || sh.total_rows != mine.total_rows ||
+      sh.total_meta != mine.total_meta)
+    return fail(KVEVICT_ERR_INVALID_ARG, "snapshot shape (B, L, H, D, values) differs from this handle");
+  if (sh.n_sink != mine.n_sink || sh.recent != mine.recent || sh.score_mode != mine.score_mode ||
+      sh.anneal_steps != mine.anneal_steps || sh.tau_init != mine.tau_init || sh.tau_end != mine.tau_end ||
+      sh.rope_theta != mine.rope_theta || sh.seed != mine.seed)
+    return fail(KVEVICT_ERR_INVALID_ARG,
+                "snapshot method parameters (sinks, recent, score mode, tau schedule, RoPE base, seed) differ");
+  if (sh.next_pos < 0 || sh.stepped < 0 || sh.stepped > 1)
+    return fail(KVEVICT_ERR_INVALID_ARG, "snapshot position out of range");
+  const unsigned char* in = static_cast<const unsigned char*>(buf);
+  size_t off = sizeof sh;
+  if (std::memcmp(in + off, h->budgets.data(), (size_t)h->L * 4) != 0)
+    return fail(KVEVICT_ERR_INVALID_ARG, "snapshot layer budgets differ from this handle's");
+  off += (size_t)h->L * 4;
+  cudaStream_t s = (cudaStream_t)stream;
+  for (const auto& a : snap_arrays(h)) {
+    KV_CUDA(cudaMemcpyAsync(a.first, in + off, a.second, cudaMemcpyHostToDevice, s));
+    off += a.second;
+  }
+  KV_CUDA(cudaMemsetAsync(h->pend, 0xFF, (size_t)h->heads * 4, s));   // flushed when saved
+  KV_CUDA(cudaMemsetAsync(h->done, 0, (size_t)h->heads * 8, s));
+  KV_CUDA(cudaMemsetAsync(h->err, 0, sizeof(int), s));
+  KV_CUDA(cudaMemsetAsync(h->ticket, 0, sizeof(unsigned long long), s));
+  h->next_pos = sh.next_pos;
+  h->stepped = sh.stepped != 0;
+  h->dsteps = 0;
+  return check_error_word(h, s);   // synchronises the stream: the caller may free buf
 }
 
 }  // extern "C"

@@ -76,3 +76,6 @@ def test_null_arguments(kvx):
     assert lib.kvevict_read_state(None, 0, 0, 0, None, None, None, None, None, None) == kvx.ERR_INVALID_ARG
     assert lib.kvevict_destroy(None) == kvx.OK
     assert "null" in kvx.last_error()
+    assert lib.kvevict_state_bytes(None, None) == kvx.ERR_INVALID_ARG
+    assert lib.kvevict_save_state(None, None, 0, None) == kvx.ERR_INVALID_ARG
+    assert lib.kvevict_load_state(None, None, 0, None) == kvx.ERR_INVALID_ARG
