@@ -9,7 +9,9 @@
  *     most the number of tokens the row has seen (each step adds one softmax,
  *     of mass 1; evicted rows take theirs with them);
  *   - both host-buffer runs give the same evicted slots and the same state
- *     bit for bit as the device-buffer path.
+ *     bit for bit as the device-buffer path;
+ *   - a snapshot of the device-path handle (kvevict_save_state) loaded into a
+ *     fresh handle reads back the same state bit for bit.
  * Exit status 0 on success. Build: gcc -std=c11 ... -lkvevict -lcudart. */
 #include <cuda_runtime.h>
 #include <math.h>
@@ -197,6 +199,36 @@ int main(void) {
         }
   }
   kvevict_t* h2 = hosts[0];
+
+  /* checkpoint: snapshot the device-path handle, load it into a fresh one */
+  size_t snap_bytes = 0;
+  CHECK(kvevict_state_bytes(h, &snap_bytes));
+  unsigned char* snap = (unsigned char*)malloc(snap_bytes);
+  if (!snap) return 1;
+  CHECK(kvevict_save_state(h, snap, snap_bytes, NULL));
+  kvevict_t* h4 = NULL;
+  CHECK(kvevict_create(&cfg, NULL, &h4));
+  CHECK(kvevict_load_state(h4, snap, snap_bytes, NULL));
+  free(snap);
+  int64_t p4 = 0;
+  CHECK(kvevict_next_pos(h4, &p4));
+  if (p4 != S + T) {
+    fprintf(stderr, "loaded next_pos %lld, expected %d\n", (long long)p4, S + T);
+    return 1;
+  }
+  for (int b = 0; b < B; ++b)
+    for (int l = 0; l < L; ++l)
+      for (int hh = 0; hh < H; ++hh) {
+        int32_t n1 = 0, n2 = 0;
+        CHECK(kvevict_read_state(h, b, l, hh, k1, s1, g1, p1, &n1, NULL));
+        CHECK(kvevict_read_state(h4, b, l, hh, k2, s2, g2, p2, &n2, NULL));
+        if (n1 != n2 || memcmp(k1, k2, (size_t)n1 * D * 2) || memcmp(s1, s2, (size_t)n1 * 4) ||
+            memcmp(g1, g2, (size_t)n1 * 4) || memcmp(p1, p2, (size_t)n1 * 4)) {
+          fprintf(stderr, "row (%d,%d,%d): loaded snapshot differs\n", b, l, hh);
+          return 1;
+        }
+      }
+  CHECK(kvevict_destroy(h4));
 
   /* an invalid call is refused with a message, and the handle keeps working */
   if (kvevict_prefill(h, dpre, S, NULL) != KVEVICT_ERR_BAD_STATE || kvevict_last_error()[0] == '\0') {
