@@ -283,7 +283,8 @@ int kvevict_load_state(kvevict_t* h, const void* buf, size_t bytes, void* stream
  * current; make that first call before any stream capture. With lazy module
  * loading the driver places the array when the library's kernels first load,
  * which can be during that first call. Errors: INVALID_ARG (null pointers,
- * head_dim not 64/128, negative or over-limit sizes), CUDA. */
+ * keys not 16-byte aligned, head_dim not 64/128, negative or over-limit
+ * sizes), CUDA. */
 int kvevict_prefill_scores_noalloc(const uint16_t* keys, int32_t heads, int32_t S,
                                    int32_t head_dim, float* colsum, void* stream);
 
