@@ -624,9 +624,11 @@ int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, cons
   const size_t per_batch = (size_t)h->L * h->H * (size_t)S * h->D;
   const size_t per_step = (size_t)BLHD(h);
   // Page-locked buffers are moved by the library's kernels through their
-  // device mapping: the prompt is staged by a copy kernel and the decode keys
-  // are read in place by the decode step. Other host memory is staged with
-  // cudaMemcpyAsync on a second stream, overlapping compute.
+  // device mapping: the prompt is staged chunk by chunk by a copy kernel on the
+  // copy stream (small enough to run beside the scorer), the decode keys are
+  // read in place by the decode step, and the evicted slots go back by the same
+  // copy kernel. Other host memory is staged with cudaMemcpyAsync on the copy
+  // stream, overlapping compute.
   const void* pre_map = S > 0 ? kvx::mapped_host(prefill_keys, (size_t)h->B * per_batch * 2) : nullptr;
   const void* dec_map = T > 0 ? kvx::mapped_host(decode_keys, (size_t)T * per_step * 2) : nullptr;
   const bool dec_inplace = dec_map && aligned16(dec_map);   // else staged by the copy kernel
