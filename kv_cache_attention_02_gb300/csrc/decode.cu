@@ -714,12 +714,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
           *reinterpret_cast<Chunk*>(vd + HALF + c * CH) = v_hi;
         }
       }
-      const int e_log_out = evict ? R_e - ((shift && R_e > e_prev) ? 1 : 0) : -1;   // slot after compaction
+      // the slot this step evicts, numbered after the previous compaction; -1 within budget
+      const int e_log = evict ? R_e - ((shift && R_e > e_prev) ? 1 : 0) : -1;
       if (tid == 0) {
         const int head = hd.head;
         gg[n] = gnew;
         pg[n] = (int32_t)hd.p;
-        const int e_log = e_log_out;
         a.pend[head] = e_log;
         if (a.evicted) {
           const int l = head / BH;
@@ -731,13 +731,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
       }
       // every consumer is done with s_log, the metadata and the reduction
       // scratch, and every write of this row's step has been issued: publish
-      // the step, free the metadata stages and the row's slot. The named
+      // the step (its count and the slot it leaves to compact, one word), free
+      // the metadata stages and the row's slot. The named
       // barrier orders every consumer's writes before thread 0's release (the
       // barrier synchronises at CTA scope, and a release is cumulative over
       // what precedes it in causality order), so no separate fence is needed
       // for a CTA that acquires the counter to see them.
       consumers_sync();
-      if (tid == 0) st_release(a.done + hd.head, pack_done(a.s0 + hd.t + 1, e_log_out));
+      if (tid == 0) st_release(a.done + hd.head, pack_done(a.s0 + hd.t + 1, e_log));
       if (lane == 0) {
         for (int k = 0; k < P.nm; ++k) mbar_arrive_cta(empty((um + k) % kStages));
         mbar_arrive_cta(rempty(q));
