@@ -640,7 +640,12 @@ int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S, cons
   const int bc = S <= 0 ? 0
                  : seq ? h->B   // sequential steps run over every row: stage the whole prompt
                        : (int)std::max<size_t>(1, std::min<size_t>(h->B, budget_elems / std::max<size_t>(per_batch, 1)));
-  const int tc = T > 0 ? (int)std::max<size_t>(1, std::min<size_t>((size_t)T, budget_elems / per_step)) : 0;
+  // decode chunk: bounded by the key staging, or, with the keys read in place,
+  // only by the evicted-slot staging (256 MiB of int32), so one launch usually
+  // runs every step
+  const size_t ev_budget = (size_t)64 << 20;
+  const size_t tc_cap = dec_inplace ? ev_budget / std::max<size_t>((size_t)BLH(h), 1) : budget_elems / per_step;
+  const int tc = T > 0 ? (int)std::max<size_t>(1, std::min<size_t>((size_t)T, tc_cap)) : 0;
   const size_t need = std::max((size_t)bc * per_batch, dec_inplace ? (size_t)0 : (size_t)tc * per_step);
   if (!h->copy_stream) {
     KV_CUDA(cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking));
