@@ -231,6 +231,23 @@ int kvevict_next_pos(const kvevict_t* h, int64_t* p);
 /* Budget of layer l as resolved at create time. */
 int kvevict_layer_budget(const kvevict_t* h, int32_t l, int32_t* budget);
 
+/* Per-layer cache statistics, host arithmetic only (page "PyramidKV ...":
+ * each layer's cache exposes layer_budget, compression_ratio and
+ * tokens_kept; page "veloxquant_mlx.quantizers.keyformer module":
+ * keyformer_fp16_bytes, full_keyformer_fp16_bytes). For layer l, with p the
+ * tokens seen (kvevict_next_pos):
+ *   tokens_kept  = min(p, budget_l), the rows each (batch, KV head) row holds;
+ *   stored_bytes = B * H * tokens_kept * D * 2 bytes of fp16 keys, doubled
+ *                  on a value-carrying handle (scores, Gumbel values and
+ *                  positions are bookkeeping, not counted, as on the
+ *                  keyformer page);
+ *   full_bytes   = the same with p tokens: what keeping every token takes;
+ *   compression_ratio = full_bytes / stored_bytes (1 while p = 0).
+ * Any output pointer may be NULL. Errors: INVALID_ARG (null handle, layer
+ * out of range). */
+int kvevict_layer_stats(const kvevict_t* h, int32_t l, int32_t* tokens_kept, uint64_t* stored_bytes,
+                        uint64_t* full_bytes, double* compression_ratio);
+
 /* Device bytes held by the handle (arena + scratch + staging). */
 int kvevict_device_bytes(const kvevict_t* h, size_t* bytes);
 

@@ -67,6 +67,7 @@ SIGNATURES = {
     "kvevict_flush": (ctypes.c_int, [P, P]),
     "kvevict_next_pos": (ctypes.c_int, [P, P]),
     "kvevict_layer_budget": (ctypes.c_int, [P, i32, P]),
+    "kvevict_layer_stats": (ctypes.c_int, [P, i32, P, P, P, P]),
     "kvevict_device_bytes": (ctypes.c_int, [P, P]),
     "kvevict_state_bytes": (ctypes.c_int, [P, P]),
     "kvevict_save_state": (ctypes.c_int, [P, P, ctypes.c_size_t, P]),
@@ -260,6 +261,14 @@ class KVEvict:
         b = i32(0)
         _check(lib().kvevict_layer_budget(self._h, l, ctypes.addressof(b)))
         return b.value
+
+    def layer_stats(self, l: int) -> dict:
+        """tokens_kept, stored_bytes, full_bytes and compression_ratio of layer l."""
+        kept, stored, full, ratio = i32(0), ctypes.c_uint64(0), ctypes.c_uint64(0), ctypes.c_double(0)
+        _check(lib().kvevict_layer_stats(self._h, l, ctypes.addressof(kept), ctypes.addressof(stored),
+                                         ctypes.addressof(full), ctypes.addressof(ratio)))
+        return {"tokens_kept": kept.value, "stored_bytes": stored.value, "full_bytes": full.value,
+                "compression_ratio": ratio.value}
 
     def device_bytes(self) -> int:
         v = ctypes.c_size_t(0)

@@ -807,6 +807,20 @@ int kvevict_layer_budget(const kvevict_t* h, int32_t l, int32_t* budget) {
   return KVEVICT_OK;
 }
 
+int kvevict_layer_stats(const kvevict_t* h, int32_t l, int32_t* tokens_kept, uint64_t* stored_bytes,
+                        uint64_t* full_bytes, double* compression_ratio) {
+  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  if (l < 0 || l >= h->L) return fail(KVEVICT_ERR_INVALID_ARG, "layer out of range");
+  const int64_t p = h->next_pos;
+  const int64_t kept = std::min<int64_t>(p, h->budgets[l]);
+  const uint64_t per_token = (uint64_t)h->B * h->H * h->D * 2 * (h->V ? 2 : 1);
+  if (tokens_kept) *tokens_kept = (int32_t)kept;
+  if (stored_bytes) *stored_bytes = per_token * (uint64_t)kept;
+  if (full_bytes) *full_bytes = per_token * (uint64_t)p;
+  if (compression_ratio) *compression_ratio = kept > 0 ? (double)p / (double)kept : 1.0;
+  return KVEVICT_OK;
+}
+
 int kvevict_device_bytes(const kvevict_t* h, size_t* bytes) {
   if (!h || !bytes) return fail(KVEVICT_ERR_INVALID_ARG, "null argument");
   *bytes = h->bytes + 2 * h->stage_elems * 2 + 2 * h->ev_stage_elems * 4;

@@ -79,3 +79,4 @@ def test_null_arguments(kvx):
     assert lib.kvevict_state_bytes(None, None) == kvx.ERR_INVALID_ARG
     assert lib.kvevict_save_state(None, None, 0, None) == kvx.ERR_INVALID_ARG
     assert lib.kvevict_load_state(None, None, 0, None) == kvx.ERR_INVALID_ARG
+    assert lib.kvevict_layer_stats(None, 0, None, None, None, None) == kvx.ERR_INVALID_ARG
