@@ -16,7 +16,8 @@
 // counter, heaviest layers first within a step; rows are independent, so a
 // row's next step starts as soon as its own previous step has been published
 // (a per-row release/acquire counter), never waiting for the whole cache to
-// finish a step. In each CTA a
+// finish a step; when there are no more rows than CTAs, each CTA keeps one
+// row for all the steps and hands them over internally. In each CTA a
 // scheduler warp claims the next row and stages its header, new key and
 // Gumbel value in shared memory; a producer warp streams the row's keys
 // through a 6-stage shared-memory ring with 1-D TMA bulk copies (16 KB tiles,
@@ -368,6 +369,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
   volatile int* abort_flag = &s_abort;
   const bool values = a.V != nullptr;
   const int BH = a.B * a.H;
+  // When every row has its own CTA, CTA r runs all of row r's steps in order
+  // and hands each step to the next inside the CTA: the consumers leave the
+  // evicted slot in the row slot's spare header word and the scheduler waits
+  // on the slot's barrier, instead of the release/acquire step word and the
+  // claim counter (a global round trip off each step's chain).
+  const bool static_rows = a.rows <= (int)gridDim.x;
 
   if (warp == kSchedulerWarp) {
     // ------------------------------------------------------- row scheduler
@@ -381,11 +388,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
       const int q = seq % kRowQ;
       if (seq >= kRowQ && !wait_watch(rempty(q), (uint32_t)((seq / kRowQ - 1) & 1), abort_flag, a.err)) break;
       unsigned long long k = 0;
-      if (lane == 0) {
-        k = atomicAdd(a.ticket, 1ull);
-        if (k == total + gridDim.x - 1) atomicExch(a.ticket, 0ull);   // the launch's last claim
+      if (static_rows) {
+        k = seq < a.T ? (unsigned long long)seq * a.rows + blockIdx.x : total;
+      } else {
+        if (lane == 0) {
+          k = atomicAdd(a.ticket, 1ull);
+          if (k == total + gridDim.x - 1) atomicExch(a.ticket, 0ull);   // the launch's last claim
+        }
+        k = __shfl_sync(0xffffffffu, k, 0);
       }
-      k = __shfl_sync(0xffffffffu, k, 0);
       unsigned char* slot = rowq + (size_t)q * G::SLOTB;
       RowHdr* hd = reinterpret_cast<RowHdr*>(slot);
       const bool claimed = k < total;
@@ -422,7 +433,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
           // it); that step's published word also carries the slot it left to
           // compact. A launch's first step takes it from the pending array
           // (written by the previous launch, the prompt, or a flush).
-          if (t > 0) {
+          if (t > 0 && static_rows) {
+            // this CTA ran step t - 1 (its sequence number seq - 1): wait for its
+            // consumers, who leave the evicted slot in the slot header's spare word
+            const int qp = (seq - 1) % kRowQ;
+            ready = wait_watch(rempty(qp), (uint32_t)(((seq - 1) / kRowQ) & 1), abort_flag, a.err);
+            hd->e_prev = ready ? *reinterpret_cast<volatile int*>(rowq + (size_t)qp * G::SLOTB + 56) : -1;
+          } else if (t > 0) {
             unsigned long long w = ld_acquire(a.done + row);
             if (done_steps(w) < a.s0 + t) {
               const uint64_t t0 = global_timer_ns();
@@ -737,8 +754,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
       // barrier synchronises at CTA scope, and a release is cumulative over
       // what precedes it in causality order), so no separate fence is needed
       // for a CTA that acquires the counter to see them.
+      if (static_rows) {
+        // this CTA's producer reads these rows with TMA at the row's next step:
+        // each writer orders its generic-proxy writes before those async-proxy
+        // reads (the producer fences again before issuing them)
+        fence_proxy_async_global();
+        if (tid == 0) *reinterpret_cast<volatile int*>(const_cast<unsigned char*>(slot) + 56) = e_log;
+      }
       consumers_sync();
-      if (tid == 0) st_release(a.done + hd.head, pack_done(a.s0 + hd.t + 1, e_log));
+      if (tid == 0 && !static_rows) st_release(a.done + hd.head, pack_done(a.s0 + hd.t + 1, e_log));
       if (lane == 0) {
         for (int k = 0; k < P.nm; ++k) mbar_arrive_cta(empty((um + k) % kStages));
         mbar_arrive_cta(rempty(q));
