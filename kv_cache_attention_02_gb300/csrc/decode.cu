@@ -110,6 +110,7 @@ struct RowPlan {
   int pos0;      // 16-byte aligned start of the moving positions
   bool move_pos;
   bool staged;   // metadata as one ring tile per array
+  bool packed;   // all three metadata arrays in one ring tile (at stride meta_stride)
 };
 
 template <int D>
@@ -124,7 +125,8 @@ __device__ __forceinline__ RowPlan row_plan(const RowHdr& h, bool values) {
   P.pos0 = (h.e_prev + 1) & ~3;
   P.move_pos = shift && h.e_prev + 1 < P.nphys;
   P.staged = (size_t)(h.capm + 4) * 4 <= (size_t)Geo<D>::TILEB;
-  P.nm = P.nphys == 0 ? 0 : P.staged ? (P.move_pos ? 3 : 2) : kStages;
+  P.packed = 3 * meta_stride(h.capm) <= (size_t)Geo<D>::TILEB;
+  P.nm = P.nphys == 0 ? 0 : P.packed ? 1 : P.staged ? (P.move_pos ? 3 : 2) : kStages;
   return P;
 }
 
@@ -470,8 +472,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
   } else if (warp == kProducerWarp) {
     // ---------------------------------------------------------- TMA producer
     // Tile sequence tg runs across rows: a row's key tiles, its value tiles,
-    // then its metadata (scores, Gumbel values, moving positions) as up to
-    // three more tiles, or, for rows too long for that, the whole ring.
+    // then its metadata (scores, Gumbel values, moving positions): one more tile
+    // holding all three arrays when they fit, else up to three tiles, or, for
+    // rows too long for that, the whole ring.
     if (lane == 0) {
       int tg = 0;
       for (int seq = 0;; ++seq) {
@@ -508,7 +511,18 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
         const int32_t* pg = a.pos + hd.mbase;
         const uint32_t mbytes = (uint32_t)(((P.nphys + 3) & ~3) * 4);
         const uint32_t pbytes = P.move_pos ? (uint32_t)(((P.nphys - P.pos0 + 3) & ~3) * 4) : 0u;
-        if (P.staged) {
+        if (P.packed) {   // short rows: all three arrays in one stage, so the row needs fewer ring slots
+          const int s = tg % kStages;
+          if (tg >= kStages && !(ok = wait_watch(empty(s), (uint32_t)((tg / kStages - 1) & 1), abort_flag, a.err)))
+            break;
+          const size_t arr = meta_stride(hd.capm);
+          unsigned char* st = ring + (size_t)s * G::TILEB;
+          mbar_expect_tx(full(s), 2 * mbytes + pbytes);
+          bulk_g2s(smem_addr(st), scg, mbytes, full(s));
+          bulk_g2s(smem_addr(st + arr), gg, mbytes, full(s));
+          if (pbytes) bulk_g2s(smem_addr(st + 2 * arr), pg + P.pos0, pbytes, full(s));
+          ++tg;
+        } else if (P.staged) {
           for (int k = 0; k < P.nm; ++k) {
             const int s = tg % kStages;
             if (tg >= kStages && !(ok = wait_watch(empty(s), (uint32_t)((tg / kStages - 1) & 1), abort_flag, a.err)))
@@ -581,11 +595,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
       int32_t* pg = a.pos + hd.mbase;
       const size_t arr = meta_stride(hd.capm);
       const int um = tg + P.ntot;   // first metadata tile
-      const float* s_sc = reinterpret_cast<const float*>(P.staged ? ring + (size_t)(um % kStages) * G::TILEB : ring);
+      const unsigned char* mtile = ring + (size_t)(um % kStages) * G::TILEB;   // the packed form's tile
+      const float* s_sc = reinterpret_cast<const float*>(P.packed ? mtile : P.staged ? ring + (size_t)(um % kStages) * G::TILEB : ring);
       const float* s_g =
-          reinterpret_cast<const float*>(P.staged ? ring + (size_t)((um + 1) % kStages) * G::TILEB : ring + arr);
+          reinterpret_cast<const float*>(P.packed ? mtile + arr : P.staged ? ring + (size_t)((um + 1) % kStages) * G::TILEB : ring + arr);
       const int32_t* s_pos =
-          reinterpret_cast<const int32_t*>(P.staged ? ring + (size_t)((um + 2) % kStages) * G::TILEB : ring + 2 * arr);
+          reinterpret_cast<const int32_t*>(P.packed ? mtile + 2 * arr : P.staged ? ring + (size_t)((um + 2) % kStages) * G::TILEB : ring + 2 * arr);
 
       float run_m = -INFINITY, run_l = 0.f;   // this thread's share of the softmax statistics
       if (tid < 32) {   // logit of the new row against itself
