@@ -102,33 +102,64 @@ __global__ void __launch_bounds__(kSThreads, 4) prefill_select_kernel(const Pref
   int16_t* newslot = reinterpret_cast<int16_t*>(flag + ((S + 15) & ~15));
   int* wsum = reinterpret_cast<int*>(newslot + ((S + 7) & ~7));
 
-  for (int t = tid; t < P2; t += kSThreads) {
-    uint64_t key = ~0ull;
-    if (t < m) {
-      const int j = a.n_sink + t;
-      const float r = fmaf(a.tau, gs[j], col[j]);
-      key = ((uint64_t)ordered_bits(r) << 32) | (uint32_t)j;
-    }
-    keys[t] = key;
+  for (int t = tid; t < m; t += kSThreads) {
+    const int j = a.n_sink + t;
+    const float r = fmaf(a.tau, gs[j], col[j]);
+    keys[t] = ((uint64_t)ordered_bits(r) << 32) | (uint32_t)j;
   }
   for (int j = tid; j < S; j += kSThreads) flag[j] = 0;
-  __syncthreads();
-  // bitonic sort, ascending by (r, slot)
-  for (int k = 2; k <= P2; k <<= 1) {
-    for (int jj = k >> 1; jj > 0; jj >>= 1) {
-      for (int t = tid; t < P2; t += kSThreads) {
-        const int ixj = t ^ jj;
-        if (ixj > t) {
-          const uint64_t x = keys[t], y = keys[ixj];
-          const bool up = (t & k) == 0;
-          if ((x > y) == up) { keys[t] = y; keys[ixj] = x; }
-        }
+  const int n_ev = S - budget;   // 1 <= n_ev < m
+  {
+    // Radix select of the n_ev smallest (r, slot) keys. The keys are distinct
+    // (the slot is in the low bits), so the n_ev-th smallest key K* is found
+    // one byte at a time from the top, and exactly the keys <= K* are evicted:
+    // the set an ascending sort's first n_ev entries would give. A slot takes
+    // at most 14 bits (S <= 16384), so bits 16..31 are zero in every key and
+    // are not visited: six passes (bytes 7..4 of r, then bytes 1, 0).
+    static_assert(kSThreads == 256, "one histogram bin per thread");
+    int* hist = wsum + 32;   // 256 bins
+    int* sel = hist + 256;   // [0] the digit, [1] keys below it
+    const int lane = tid & 31, wid = tid >> 5;
+    uint64_t prefix = 0, pmask = 0;
+    int rank = n_ev;         // 1-based rank of K* among the keys matching the prefix
+    for (int pass = 0; pass < 6; ++pass) {
+      const int shift = pass < 4 ? 56 - 8 * pass : (pass == 4 ? 8 : 0);
+      hist[tid] = 0;
+      __syncthreads();
+      for (int base = 0; base < m; base += kSThreads) {
+        const int t = base + tid;
+        const uint64_t key = t < m ? keys[t] : 0ull;
+        const bool in = t < m && (key & pmask) == prefix;
+        const int bin = in ? (int)((key >> shift) & 255) : 256 + lane;   // no dummy shares a bin
+        const unsigned peers = __match_any_sync(0xffffffffu, bin);
+        if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
       }
       __syncthreads();
+      const int v = hist[tid];
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      if (lane == 31) wsum[wid] = incl;
+      __syncthreads();
+      int excl = incl - v;
+      for (int w = 0; w < wid; ++w) excl += wsum[w];
+      if (v > 0 && excl < rank && rank <= excl + v) {   // exactly one bin holds rank
+        sel[0] = tid;
+        sel[1] = excl;
+      }
+      __syncthreads();
+      rank -= sel[1];
+      prefix |= (uint64_t)sel[0] << shift;
+      pmask |= (uint64_t)0xFF << shift;
+      if (pass == 3) pmask |= 0xFFFF0000ull;
+      __syncthreads();   // hist, wsum and sel are rewritten by the next pass
     }
+    for (int t = tid; t < m; t += kSThreads)
+      if (keys[t] <= prefix) flag[(uint32_t)keys[t]] = 1;
   }
-  const int n_ev = S - budget;
-  for (int t = tid; t < n_ev; t += kSThreads) flag[(uint32_t)keys[t]] = 1;
   __syncthreads();
 
   // exclusive scan of survivors -> new slot (each thread owns a contiguous segment)
@@ -290,7 +321,8 @@ __global__ void __launch_bounds__(256) prefill_lastrow_kernel(const PrefillScore
 size_t prefill_select_smem(int S) {
   int P2 = 1;
   while (P2 < S) P2 <<= 1;
-  return (size_t)P2 * 8 + ((S + 15) & ~15) + ((S + 7) & ~7) * 2 + 32 * sizeof(int) + 64;
+  // keys, flags, new slots, the scan's warp sums, the select's histogram and result
+  return (size_t)P2 * 8 + ((S + 15) & ~15) + ((S + 7) & ~7) * 2 + (32 + 256 + 4) * sizeof(int) + 64;
 }
 
 cudaError_t prefill_setup(int D, int max_prefill) {
