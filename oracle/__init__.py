@@ -81,6 +81,7 @@ def _bind(handle):
         "orc_budgets": (ctypes.c_int, [i32, i32, i32, f64, P]),
         "orc_splitmix64": (u64, [u64]),
         "orc_gumbel_hash": (u64, [u64, i64, i64, i64]),
+        "orc_gumbel_of_hash": (ctypes.c_float, [u64]),
         "orc_gumbel": (ctypes.c_float, [u64, i64, i64, i64]),
         "orc_gumbel_many": (None, [u64, i64, i64, i64, i64, P]),
         "orc_tau": (f64, [f64, f64, i64, i64]),
@@ -94,6 +95,9 @@ def _bind(handle):
         "orc_regularised": (None, [i32, P, P, f64, P]),
         "orc_argmin": (i32, [i32, P, i32, i32]),
         "orc_evict": (i32, [i32, i32, P, P, P, P, i32, f64]),
+        "orc_values_append": (None, [i32, i32, P, P]),
+        "orc_values_evict": (i32, [i32, i32, P, i32]),
+        "orc_values_prefill_apply": (i32, [i32, i32, P, P, P]),
         "orc_prefill_colsum": (None, [i32, i32, P, P]),
         "orc_prefill_select": (i32, [i32, i32, i32, i32, P, P]),
         "orc_prefill_lastrow": (None, [i32, i32, P, P]),
@@ -127,6 +131,11 @@ def splitmix64(x: int) -> int:
 
 def gumbel_hash(seed: int, layer: int, head: int, pos: int) -> int:
     return int(lib().orc_gumbel_hash(seed, layer, head, pos))
+
+
+def gumbel_of_hash(h: int) -> float:
+    """The frozen Gumbel value a 64-bit hash maps to (float32, as a Python float)."""
+    return float(lib().orc_gumbel_of_hash(h & (2**64 - 1)))
 
 
 def gumbel(seed: int, layer: int, head: int, p0: int, count: int = 1) -> np.ndarray:
@@ -216,10 +225,12 @@ class OracleHead:
     test can check the oracle's own choice (``select``) before applying one.
     """
 
-    def __init__(self, prm: HeadParams, extra_rows: int = 0):
+    def __init__(self, prm: HeadParams, extra_rows: int = 0, values: bool = False):
         self.prm = prm
         cap = prm.budget + 1 + extra_rows
         self.K = np.zeros((cap, prm.D), dtype=np.uint16)
+        # value rows (keyformer page, KeyformerState.values), or None: keys only
+        self.V = np.zeros((cap, prm.D), dtype=np.uint16) if values else None
         self.score = np.zeros(cap, dtype=np.float64)
         self.g = np.zeros(cap, dtype=np.float32)
         self.pos = np.zeros(cap, dtype=np.int32)
@@ -246,32 +257,42 @@ class OracleHead:
             raise ValueError("not enough evictable rows")
         return mask
 
-    def prefill_apply(self, keys, colsum, g, mask):
+    def prefill_apply(self, keys, colsum, g, mask, values=None):
         keys = np.ascontiguousarray(keys, dtype=np.uint16)
         S = keys.shape[0]
         kept = S - int(mask.sum())
         if kept > self.K.shape[0]:
             raise ValueError("prefill keeps more rows than the state holds")
+        mask = np.ascontiguousarray(mask, np.uint8)
         self.n = lib().orc_prefill_apply(S, self.prm.D, _p(keys),
                                          _p(np.ascontiguousarray(colsum, np.float64)),
                                          _p(np.ascontiguousarray(g, np.float32)),
-                                         _p(np.ascontiguousarray(mask, np.uint8)), self.prm.theta,
+                                         _p(mask), self.prm.theta,
                                          _p(self.K), _p(self.score), _p(self.g), _p(self.pos))
+        if self.V is not None:
+            vals = np.ascontiguousarray(values, dtype=np.uint16)
+            assert vals.shape == keys.shape
+            lib().orc_values_prefill_apply(S, self.prm.D, _p(vals), _p(mask), _p(self.V))
         self.next_pos = S
 
-    def prefill(self, keys: np.ndarray) -> np.ndarray:
+    def prefill(self, keys: np.ndarray, values: np.ndarray | None = None) -> np.ndarray:
         if self.prm.prefill_mode == 1:     # one step per prompt token
-            return np.array([self.step(k) for k in keys], dtype=np.int32)
+            return np.array([self.step(k, None if values is None else values[t])
+                             for t, k in enumerate(keys)], dtype=np.int32)
         colsum, g, r = self.prefill_scores(keys)
         mask = self.prefill_select(r)
-        self.prefill_apply(keys, colsum, g, mask)
+        self.prefill_apply(keys, colsum, g, mask, values)
         return mask
 
     # decode ----------------------------------------------------------------
-    def accumulate(self, k_new: np.ndarray) -> int:
+    def accumulate(self, k_new: np.ndarray, v_new: np.ndarray | None = None) -> int:
         p = self.next_pos
         gn = float(gumbel(self.prm.seed, self.prm.layer, self.prm.head, p, 1)[0])
         k = np.ascontiguousarray(k_new, dtype=np.uint16)
+        if self.V is not None:
+            v = np.ascontiguousarray(v_new, dtype=np.uint16)
+            assert v.shape == k.shape
+            lib().orc_values_append(self.prm.D, self.n, _p(self.V), _p(v))
         self.n = lib().orc_step_accumulate(self.prm.D, self.n, _p(self.K), _p(self.score),
                                            _p(self.g), _p(self.pos), _p(k), p, gn, self.prm.mode)
         self.next_pos = p + 1
@@ -292,12 +313,14 @@ class OracleHead:
     def evict(self, e: int):
         if not (self.prm.n_sink <= e < self.n - self.prm.recent):
             raise ValueError(f"slot {e} is not evictable")
+        if self.V is not None:
+            lib().orc_values_evict(self.prm.D, self.n, _p(self.V), e)
         self.n = lib().orc_evict(self.prm.D, self.n, _p(self.K), _p(self.score), _p(self.g),
                                  _p(self.pos), e, self.prm.theta)
 
-    def step(self, k_new: np.ndarray) -> int:
+    def step(self, k_new: np.ndarray, v_new: np.ndarray | None = None) -> int:
         """Append, accumulate and, when over budget, evict the oracle's own pick."""
-        self.accumulate(k_new)
+        self.accumulate(k_new, v_new)
         if self.over_budget():
             e = self.select()
             self.evict(e)
@@ -307,6 +330,10 @@ class OracleHead:
     def state(self):
         n = self.n
         return (self.K[:n].copy(), self.score[:n].copy(), self.g[:n].copy(), self.pos[:n].copy())
+
+    def values(self) -> np.ndarray:
+        """The kept value rows [n, D] in slot order (a value-carrying head only)."""
+        return self.V[: self.n].copy()
 
 
 def run_heads(params: list[HeadParams], prefill_keys: np.ndarray, decode_keys: np.ndarray,

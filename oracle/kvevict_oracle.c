@@ -77,11 +77,15 @@ uint64_t orc_gumbel_hash(uint64_t seed, int64_t layer, int64_t head, int64_t pos
   return h;
 }
 
-float orc_gumbel(uint64_t seed, int64_t layer, int64_t head, int64_t pos) {
-  uint64_t k = orc_gumbel_hash(seed, layer, head, pos) >> 12;      /* 52 bits */
+float orc_gumbel_of_hash(uint64_t h) {
+  uint64_t k = h >> 12;                                            /* top 52 bits */
   double u = (double)(2 * k + 1) * 0x1p-53;                        /* (0,1) */
   double g = -log(-log(u));
   return (float)g;
+}
+
+float orc_gumbel(uint64_t seed, int64_t layer, int64_t head, int64_t pos) {
+  return orc_gumbel_of_hash(orc_gumbel_hash(seed, layer, head, pos));
 }
 
 void orc_gumbel_many(uint64_t seed, int64_t layer, int64_t head, int64_t p0, int64_t count, float* out) {
@@ -278,6 +282,36 @@ int32_t orc_evict(int32_t D, int32_t n, uint16_t* K, double* score, float* g, in
   int32_t r = evict_with_consts(D, n, K, score, g, pos, e, c, s);
   free(c);
   return r;
+}
+
+/* ---------------------------------------------------------------------------
+ * Value rows. Keyformer page, KeyformerState.values (one fp16 value row per
+ * kept token, [n_kept, D]), keyformer_update steps 2-3 (a token is appended
+ * with its key and value; survivors after the evicted token shift down by one)
+ * and keyformer_get_kv (keys and values are returned together). A value row
+ * carries no position, so it is only moved: the RoPE remap of step 3 applies
+ * to keys alone.
+ * ------------------------------------------------------------------------- */
+void orc_values_append(int32_t D, int32_t n, uint16_t* V, const uint16_t* v_new) {
+  memcpy(V + (size_t)n * D, v_new, sizeof(uint16_t) * (size_t)D);
+}
+
+int32_t orc_values_evict(int32_t D, int32_t n, uint16_t* V, int32_t e) {
+  for (int32_t j = e + 1; j < n; ++j)
+    memcpy(V + (size_t)(j - 1) * D, V + (size_t)j * D, sizeof(uint16_t) * (size_t)D);
+  return n - 1;
+}
+
+/* The prompt's value rows after a bulk eviction: the survivors' rows in order. */
+int32_t orc_values_prefill_apply(int32_t S, int32_t D, const uint16_t* values, const uint8_t* mask,
+                                 uint16_t* V) {
+  int32_t n = 0;
+  for (int32_t j = 0; j < S; ++j) {
+    if (mask[j]) continue;
+    memcpy(V + (size_t)n * D, values + (size_t)j * D, sizeof(uint16_t) * (size_t)D);
+    ++n;
+  }
+  return n;
 }
 
 /* ---------------------------------------------------------------------------

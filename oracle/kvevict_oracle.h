@@ -22,9 +22,12 @@
  * keyformer page, KeyformerState.gumbel).
  *
  * Parity pins live in tests/test_oracle_*.py. One function has no pin from
- * the pages: the Gumbel hash (the pages name no formula), so orc_gumbel is
- * "parity unpinned" against the pages; it is pinned only to the published
- * SplitMix64 reference outputs and to the Gumbel distribution's moments.
+ * the pages: the way orc_gumbel_hash chains SplitMix64 over (seed, layer,
+ * head, position) (the pages name no formula) is "parity unpinned". What can
+ * be pinned is: SplitMix64 itself (published reference outputs), the map
+ * from a hash to u and g (its end points and monotonicity, from the
+ * mathematics) and the Gumbel law of the values (moments, KS test). A table
+ * of hashes and values in tests/golden/ is a regression fixture, not a pin.
  */
 #ifndef KVEVICT_ORACLE_H
 #define KVEVICT_ORACLE_H
@@ -41,6 +44,8 @@ int orc_budgets(int32_t n_layers, int32_t avg_budget, int32_t n_sink, double bet
 uint64_t orc_splitmix64(uint64_t x);
 /* Hash of (seed, layer, head, position) and the frozen Gumbel value. */
 uint64_t orc_gumbel_hash(uint64_t seed, int64_t layer, int64_t head, int64_t pos);
+/* The Gumbel value of a hash: k = top 52 bits, u = (2k+1)/2^53, -log(-log u) as f32. */
+float orc_gumbel_of_hash(uint64_t h);
 float orc_gumbel(uint64_t seed, int64_t layer, int64_t head, int64_t pos);
 /* Gumbel values for positions p0 .. p0+count-1 of one (layer, head). */
 void orc_gumbel_many(uint64_t seed, int64_t layer, int64_t head, int64_t p0, int64_t count, float* out);
@@ -78,6 +83,14 @@ int32_t orc_argmin(int32_t n, const double* r, int32_t n_sink, int32_t recent);
  * each moved key re-rotated by -1 position. Returns n-1. */
 int32_t orc_evict(int32_t D, int32_t n, uint16_t* K, double* score, float* g, int32_t* pos,
                   int32_t e, double theta);
+
+/* Value rows (fp16 bits [rows, D]) move with their keys and are never rotated.
+ * append: V[n] = v_new. evict: rows after e move down one slot; returns n-1.
+ * prefill_apply: the unmasked prompt value rows in order; returns the count. */
+void orc_values_append(int32_t D, int32_t n, uint16_t* V, const uint16_t* v_new);
+int32_t orc_values_evict(int32_t D, int32_t n, uint16_t* V, int32_t e);
+int32_t orc_values_prefill_apply(int32_t S, int32_t D, const uint16_t* values, const uint8_t* mask,
+                                 uint16_t* V);
 
 /* Prefill scoring: column sums of the causal softmax(K K^T / sqrt(D)), the
  * diagonal included. keys [S, D] fp16 bits, out colsum [S]. */

@@ -17,7 +17,7 @@ SRC = os.path.join(ROOT, "oracle", "kvevict_oracle.c")
 HDR = os.path.join(ROOT, "oracle", "kvevict_oracle.h")
 PIN_FILES = [os.path.join(ROOT, "tests", f) for f in (
     "test_oracle_schedule.py", "test_oracle_hash.py", "test_oracle_fp16_rope.py",
-    "test_oracle_step.py")]
+    "test_oracle_step.py", "test_oracle_values.py")]
 
 # name: (text in the source, planted replacement, count of replacements or 0 = all)
 MUTATIONS = {
@@ -44,6 +44,15 @@ MUTATIONS = {
                                  "rest >= 0x1000u"),
     "taper_slope": ("1.0 - 2.0 * (double)l", "1.0 - 1.0 * (double)l"),
     "prompt_select_takes_highest": ("while (b >= 0 && r[idx[b]] > r[v])", "while (b >= 0 && r[idx[b]] < r[v])"),
+    "gumbel_u_from_53_bits": ("uint64_t k = h >> 12;", "uint64_t k = h >> 11;"),
+    "gumbel_u_offset_dropped": ("double u = (double)(2 * k + 1) * 0x1p-53;",
+                                "double u = (double)(2 * k) * 0x1p-53;"),
+    "values_shift_up": ("memcpy(V + (size_t)(j - 1) * D, V + (size_t)j * D,",
+                        "memcpy(V + (size_t)j * D, V + (size_t)(j - 1) * D,"),
+    "values_not_moved": ("for (int32_t j = e + 1; j < n; ++j)\n    memcpy(V",
+                         "for (int32_t j = n; j < n; ++j)\n    memcpy(V"),
+    "prompt_values_from_kept_slot": ("memcpy(V + (size_t)n * D, values + (size_t)j * D,",
+                                     "memcpy(V + (size_t)n * D, values + (size_t)n * D,"),
 }
 
 
