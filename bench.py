@@ -70,9 +70,23 @@ def workload_of(args):
     return wl.scaled(**kw) if kw else wl
 
 
+def tau_text(wl):
+    """The temperature schedule as the run applies it: tau anneals over absolute
+    positions 0..anneal_steps, prompt positions included, so a prompt at least
+    that long leaves every decode step at tau_end."""
+    if wl.tau_init == wl.tau_end or not wl.anneal_steps:
+        return f"{wl.tau_init:g} (constant)"
+    span = f"{wl.tau_init:g}->{wl.tau_end:g} over positions 0..{wl.anneal_steps}"
+    if wl.prefill >= wl.anneal_steps:
+        return span + f"; the {wl.prefill}-token prompt covers the ramp, every decode step runs at {wl.tau_end:g}"
+    t0 = wl.tau_init + wl.prefill * (wl.tau_end - wl.tau_init) / wl.anneal_steps
+    last = wl.prefill + wl.decode - 1
+    t1 = wl.tau_init + min(last, wl.anneal_steps) * (wl.tau_end - wl.tau_init) / wl.anneal_steps
+    return span + f"; decode runs from {t0:g} to {t1:g}"
+
+
 def config_of(wl, budgets):
-    tau = "0" if wl.tau_init == 0 and wl.tau_end == 0 else (
-        f"{wl.tau_init:g}->{wl.tau_end:g} over {wl.anneal_steps}" if wl.anneal_steps else f"{wl.tau_init:g}")
+    tau = tau_text(wl)
     return {"workload": wl.name, "batch": wl.batch, "layers": wl.n_layers, "kv_heads": wl.n_kv_heads,
             "head_dim": wl.head_dim, "avg_budget": wl.avg_budget, "pyramid_beta": wl.beta,
             "budgets": f"{budgets[0]}..{budgets[-1]}", "n_sink": wl.n_sink, "tau": tau,
@@ -80,23 +94,24 @@ def config_of(wl, budgets):
             "late_riser": wl.late_riser}
 
 
-def profiled_traffic(wl, kernel_src):
-    """DRAM bytes (read + write) of one decode launch on this workload, from the
-    committed ncu launch list, or None when the kernel source has changed since
-    the counters were taken or the workload differs."""
+def profiled_traffic(wl, kernel_src, bytes_per_launch):
+    """DRAM bytes (read + write) of one decode launch on this workload, scaled
+    from the committed small-case ncu capture (profiles/decode_step_small.md):
+    that launch's DRAM bytes over its algorithmic bytes, times this launch's
+    algorithmic bytes. None when decode.cu has changed since the counters were
+    taken, or when the capture was of another workload."""
     import hashlib
     try:
-        with open(os.path.join(ROOT, "profiles", "large_context_launch_list.md")) as f:
-            lines = [ln.split() for ln in f if ln.startswith("traffic ")]
+        with open(os.path.join(ROOT, "profiles", "decode_step_small.md")) as f:
+            lines = [ln.split() for ln in f if ln.startswith("traffic_ratio ")]
         with open(kernel_src, "rb") as f:
             sha = hashlib.sha256(f.read()).hexdigest()
     except OSError:
         return None
     for ln in lines:
-        kv = dict(x.split("=", 1) for x in ln[3:] if "=" in x)
-        if (ln[2] == wl.name and wl is workloads.ALL.get(wl.name) and int(kv.get("steps", -1)) == wl.decode
-                and kv.get("decode_cu_sha256") == sha):
-            return int(kv["bytes"])
+        kv = dict(x.split("=", 1) for x in ln[1:] if "=" in x)
+        if kv.get("workload") == wl.name and kv.get("decode_cu_sha256") == sha:
+            return int(round(int(kv["dram_bytes"]) / int(kv["algorithmic_bytes"]) * bytes_per_launch))
     return None
 
 
@@ -417,7 +432,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": profiled_traffic(wl, os.path.join(ROOT, "kv_cache_attention_02_gb300", "csrc",
-                                                                  "decode.cu")),
+                                                                  "decode.cu"), step_bytes),
                      "kernel": "decode_step_kernel<128>" if D == 128 else "decode_step_kernel<64>",
                      "bytes_per_launch": step_bytes, "launch_us": decode_ms * 1e3,
                      "steps_per_launch": T, "us_per_step": launch_ms * 1e3,

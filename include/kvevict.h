@@ -78,7 +78,21 @@ typedef struct kvevict_config {
   int32_t with_values;    /* 1: the cache also holds value rows (fp16 [.., D]); they move with
                              their keys and are never rotated (keyformer page,
                              KeyformerState.values); 0: keys only */
+  int32_t decode_kernel;  /* KVEVICT_DECODE_AUTO (0), KVEVICT_DECODE_STREAM or
+                             KVEVICT_DECODE_RESIDENT: which kernel runs the decode steps */
 } kvevict_config;
+
+/* Decode kernels; both compute the same steps and agree with each other up to
+ * the order of floating-point sums. STREAM: every step streams each row's
+ * keys from device memory through shared memory, any row length. RESIDENT: a
+ * call of several steps keeps each row in one CTA's shared memory for all of
+ * them (rows up to 1023 keys, key-only handles; the rows of a large cache run
+ * in waves). AUTO takes RESIDENT for key-only handles whose rows fit and for
+ * calls of at least 4 steps, STREAM otherwise; asking for RESIDENT on a handle
+ * whose rows do not fit, or that carries values, is INVALID_ARG at create. */
+#define KVEVICT_DECODE_AUTO 0
+#define KVEVICT_DECODE_STREAM 1
+#define KVEVICT_DECODE_RESIDENT 2
 
 /* Prompt modes. BULK: score the whole prompt, then a row over budget evicts its
  * lowest (score + tau(S-1) * g, slot) rows at once. SEQUENTIAL: every prompt
@@ -115,7 +129,11 @@ int kvevict_budgets(int32_t n_layers, int32_t avg_budget, int32_t n_sink, double
  * null pointers, sizes out of range), OOM, CUDA. *out is set only on success. */
 int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out);
 
-/* Free the handle and its device memory (synchronises the device first). */
+/* Free the handle and its device memory (synchronises the device first).
+ * The pages keep a cache's state in a KeyformerState object that lives as long
+ * as its owner holds it (page "veloxquant_mlx.quantizers.keyformer module",
+ * KeyformerState); this ends the life of the device arena holding it here.
+ * Errors: none (a null handle is ignored). */
 int kvevict_destroy(kvevict_t* h);
 
 /* Return the handle to the empty state at position 0 (the arena is reused). */
@@ -161,7 +179,12 @@ int kvevict_decode_kv(kvevict_t* h, const uint16_t* keys, const uint16_t* values
 int kvevict_read_values(kvevict_t* h, int32_t b, int32_t l, int32_t head, uint16_t* values,
                         int32_t* n_kept, void* stream);
 
-/* One decode step for every row at position p = kvevict_next_pos().
+/* One decode step for every row at position p = kvevict_next_pos(): the
+ * three steps of keyformer_update for one incoming token (page
+ * "veloxquant_mlx.quantizers.keyformer module"), applied to every (batch,
+ * layer, KV head) row at once as keyformer_update_batched applies them to
+ * every (batch, head) row of a layer, with each layer's own budget (page
+ * "PyramidKV ...", "How it works").
  * k_new: device fp16 [B, L, H, D], RoPE-rotated at p. evicted: device int32
  * [B, L, H] or NULL; receives the evicted slot (index into the rows after the
  * append, 0..n) or -1 when the row was within budget. One fused kernel launch.
@@ -195,7 +218,10 @@ int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S,
                      const uint16_t* decode_keys, int32_t T, int32_t* evicted, void* stream);
 /* (key-only handles; a with_values handle returns INVALID_ARG) */
 
-/* Apply the compaction the last decode step decided (the step kernel leaves
+/* Apply the compaction the last decode step decided: the second half of
+ * keyformer_update step 3 (page "veloxquant_mlx.quantizers.keyformer module":
+ * survivors after the evicted token shift down by one and are re-rotated),
+ * which this library defers (the step kernel leaves
  * the evicted row in place and the next step or this call removes it while
  * re-rotating the rows that move). kvevict_read_state calls it itself; a
  * caller that reads the device arena by other means, or that wants a step's
@@ -203,7 +229,10 @@ int kvevict_run_host(kvevict_t* h, const uint16_t* prefill_keys, int32_t S,
  * kernel launch; a no-op for rows with nothing pending. Errors: CUDA. */
 int kvevict_flush(kvevict_t* h, void* stream);
 
-/* Copy one row's state to host memory (synchronises the stream). Rows
+/* Copy one row's state to host memory (synchronises the stream): the keys
+ * keyformer_get_kv returns and the KeyformerState fields scores, gumbel and
+ * positions (page "veloxquant_mlx.quantizers.keyformer module"; values:
+ * kvevict_read_values). Rows
  * are given in slot order: keys [n, D] fp16 bits, scores [n], gumbel [n],
  * positions [n] (the original absolute position of each kept key), n =
  * *n_kept = min(next_pos, budget of layer l). Buffers need room for
@@ -218,14 +247,21 @@ int kvevict_read_state(kvevict_t* h, int32_t b, int32_t l, int32_t head, uint16_
  * word and the state, after which the handle works as a new one. */
 int kvevict_check(kvevict_t* h, void* stream);
 
-/* Test hook for the failure path, with no counterpart on the pages: in the
- * next decode launch, the first CTA's copy of its first key tile is never
- * issued, so a wait on it runs out (1 s) and the kernel sets the error word
- * (wait timeout) and returns; nothing faults or hangs. One-shot. Errors:
- * INVALID_ARG (null handle). */
+/* Test hook for the failure path, with no counterpart on the pages. With a
+ * handle: in its next decode launch, the first CTA's copy of its first key
+ * tile is never issued, so a wait on it runs out (1 s) and the kernel sets the
+ * handle's error word (wait timeout) and returns. With h = NULL: the next
+ * launch of the tensor-core prompt scorer in this process (kvevict_prefill of
+ * any handle in a cumulative score mode, or kvevict_prefill_scores_noalloc)
+ * never issues its first CTA's query-tile copy, with the same outcome: a
+ * handle then reports DEVICE_CHECK, the allocation-free call writes NaN
+ * scores. Nothing faults or hangs. One-shot. Errors: none. */
 int kvevict_test_stall_next_step(kvevict_t* h);
 
-/* Position the next decode key will occupy (= tokens absorbed so far). */
+/* Position the next decode key will occupy (= tokens absorbed so far): the
+ * KeyformerState.next_pos counter, one value shared by every row (page
+ * "veloxquant_mlx.quantizers.keyformer module", KeyformerState and
+ * keyformer_update_batched). *p: host int64. Errors: INVALID_ARG (null). */
 int kvevict_next_pos(const kvevict_t* h, int64_t* p);
 
 /* Budget of layer l as resolved at create time. */
@@ -295,13 +331,21 @@ int kvevict_load_state(kvevict_t* h, const void* buf, size_t bytes, void* stream
  * needs to start at zero, since a call reads only entries it wrote itself
  * (padding entries it reads are masked out). Calls whose work overlaps on the
  * GPU (other streams, other threads) race on the array: serialise them.
- * The first call on each device (and head_dim) looks up the array's device
- * address and sets the kernels' shared-memory attribute, with that device
- * current; make that first call before any stream capture. With lazy module
- * loading the driver places the array when the library's kernels first load,
- * which can be during that first call. Errors: INVALID_ARG (null pointers,
- * keys not 16-byte aligned, head_dim not 64/128, negative or over-limit
- * sizes), CUDA. */
+ * A failure on the GPU cannot reach the return code, which comes back before
+ * the GPU runs the call: if one of the scorer's bounded waits runs out (1 s),
+ * the call writes NaN to every entry of colsum instead of scores, so a caller
+ * that must know checks colsum for NaN after the stream has passed the call.
+ * (A device error word beside the array records it; each call clears the word
+ * first with cudaMemsetAsync, which allocates nothing.)
+ * The first call on each device (and head_dim) looks up the device addresses
+ * of the array and the error word, the device's multiprocessor count, and sets
+ * the kernels' shared-memory attribute, with that device current; make that
+ * first call before any stream capture. The addresses are kept for the life of
+ * the process: do not reset the device (cudaDeviceReset) after the first call.
+ * With lazy module loading the driver places the array when the library's
+ * kernels first load, which can be during that first call. Errors:
+ * INVALID_ARG (null pointers, keys not 16-byte aligned, head_dim not 64/128,
+ * negative or over-limit sizes), CUDA. */
 int kvevict_prefill_scores_noalloc(const uint16_t* keys, int32_t heads, int32_t S,
                                    int32_t head_dim, float* colsum, void* stream);
 

@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libkvevict.so")
 OK, ERR_INVALID_ARG, ERR_BAD_STATE, ERR_CUDA, ERR_OOM, ERR_DEVICE_CHECK = 0, -1, -2, -3, -4, -5
 SCORE_CUMULATIVE, SCORE_CURRENT = 0, 1
 PREFILL_BULK, PREFILL_SEQUENTIAL = 0, 1
+DECODE_AUTO, DECODE_STREAM, DECODE_RESIDENT = 0, 1, 2
 MAX_LAYERS = 256
 MAX_PREFILL = 16384
 
@@ -35,7 +36,7 @@ class Config(ctypes.Structure):
                 ("avg_budget", i32), ("pyramid_beta", f64), ("layer_budgets", P), ("n_sink", i32),
                 ("tau_init", f32), ("tau_end", f32), ("anneal_steps", i32), ("rope_theta", f64),
                 ("seed", u64), ("max_prefill", i32), ("recent", i32), ("score_mode", i32),
-                ("prefill_mode", i32), ("with_values", i32)]
+                ("prefill_mode", i32), ("with_values", i32), ("decode_kernel", i32)]
 
 
 class KVEvictError(RuntimeError):
@@ -146,14 +147,16 @@ class KVEvict:
                  n_sink: int = 4, tau_init: float = 0.0, tau_end: float = 0.0,
                  anneal_steps: int = 0, rope_theta: float = 10000.0, seed: int = 0,
                  max_prefill: int = 0, recent: int = 0, score_mode: int = SCORE_CUMULATIVE,
-                 prefill_mode: int = PREFILL_BULK, with_values: bool = False, stream=None):
+                 prefill_mode: int = PREFILL_BULK, with_values: bool = False,
+                 decode_kernel: int = DECODE_AUTO, stream=None):
         self._lb = None
         if layer_budgets is not None:
             self._lb = (i32 * n_layers)(*layer_budgets)
         self.cfg = Config(batch, n_layers, n_kv_heads, head_dim, avg_budget, pyramid_beta,
                           ctypes.addressof(self._lb) if self._lb is not None else None, n_sink,
                           tau_init, tau_end, anneal_steps, rope_theta, seed & (2 ** 64 - 1),
-                          max_prefill, recent, score_mode, prefill_mode, int(bool(with_values)))
+                          max_prefill, recent, score_mode, prefill_mode, int(bool(with_values)),
+                          decode_kernel)
         self._h = P()
         _check(lib().kvevict_create(ctypes.addressof(self.cfg), _stream(stream),
                                     ctypes.addressof(self._h)))
@@ -295,7 +298,7 @@ class KVEvict:
         _check(lib().kvevict_load_state(self._h, buf.ctypes.data, buf.size, _stream(stream)))
 
 
-def from_workload(wl, stream=None, with_values=False) -> KVEvict:
+def from_workload(wl, stream=None, with_values=False, decode_kernel=DECODE_AUTO) -> KVEvict:
     """Handle for a ``workloads.Workload`` configuration."""
     return KVEvict(batch=wl.batch, n_layers=wl.n_layers, n_kv_heads=wl.n_kv_heads,
                    head_dim=wl.head_dim, avg_budget=wl.avg_budget, pyramid_beta=wl.beta,
@@ -304,4 +307,4 @@ def from_workload(wl, stream=None, with_values=False) -> KVEvict:
                    max_prefill=wl.prefill, recent=getattr(wl, "recent", 0),
                    score_mode=getattr(wl, "score_mode", SCORE_CUMULATIVE),
                    prefill_mode=getattr(wl, "prefill_mode", PREFILL_BULK),
-                   with_values=with_values, stream=stream)
+                   with_values=with_values, decode_kernel=decode_kernel, stream=stream)

@@ -1,0 +1,430 @@
+// decode_resident.cu -- the decode step with each cache row held in shared
+// memory for a whole multi-step call.
+//
+// It computes exactly what decode_step_kernel computes (page
+// "veloxquant_mlx.quantizers.keyformer module", keyformer_update steps 1-3;
+// page "PyramidKV -- Layer-Adaptive Budget Attention-Mass Eviction", "How it
+// works"): per step, append the new key, softmax(K k / sqrt(D)) over every
+// row including the new one, scores += attn (or = attn, current-step mode),
+// and over budget evict the lowest score + tau * gumbel among the rows that
+// are neither sinks nor in the recent window (lowest slot on ties); the rows
+// after it move down one slot, keys re-rotated by -1 position in fp32.
+//
+// Design (GB300): when a row's keys and metadata fit in one CTA's shared
+// memory and a call runs several steps, one CTA takes one row for every step
+// of the call. It loads the row once (a 1-D TMA bulk copy of its keys), runs
+// the T steps out of shared memory, and writes the row back once, so a step
+// costs no HBM or L2 round trip: the few-row shapes, whose steps are a chain
+// of such round trips in the streaming kernel, run at the speed of one SM's
+// shared memory instead. A helper warp runs ahead of the step: it reads the
+// next steps' keys (several in flight), computes their frozen Gumbel values
+// (fp64 logs, eight steps at once on eight lanes) and temperatures, and hands
+// them over through a ring of shared-memory slots. The eight consumer warps
+// keep the physical key rows in place and a logical-slot -> physical-row map:
+// an eviction shifts the map and the per-slot scores, Gumbel values and
+// positions (a few words per row), the evicted row's storage takes the next
+// step's new key, and every row that moved is re-rotated in place by the
+// threads that read it in the next step's dot products (the deferred
+// compaction of the streaming kernel, without the move). The call ends by
+// writing the row back in the arena's layout, with the last step's
+// compaction left pending exactly as the streaming kernel leaves it.
+//
+// Rows are independent, so a grid with more rows than fit on the GPU at once
+// runs in waves; nothing waits across CTAs.
+#include "decode_common.cuh"
+
+namespace kvx {
+namespace {
+
+constexpr int kHelperWarp = kConsumerWarps;   // stages each step's inputs
+constexpr int kRThreads = kConsumers + 32;
+constexpr int kQ = 16;                        // input slots (steps the helper may run ahead)
+constexpr int kGroup = 8;                     // steps the helper prepares at once
+constexpr int kMaxPerThread = 4;              // logical slots per consumer thread in the shift pass
+constexpr int kResidentMaxCap = kConsumers * kMaxPerThread;   // 1024 rows
+
+// One step's inputs as the helper leaves them in a slot; the new key follows.
+struct StepIn {
+  int64_t p;    // absolute position of the incoming key
+  float gnew;   // its frozen Gumbel value
+  float tau;    // tau(p)
+};
+static_assert(sizeof(StepIn) == 16, "step input header");
+
+struct ResLayout {
+  size_t keys, score, gum, pos, perm, logit, queue, bars, redf, redi, total;
+};
+
+template <int D>
+__host__ __device__ inline size_t res_slot_bytes() { return sizeof(StepIn) + (size_t)D * 2; }
+
+// cap: physical key rows (the largest budget + 1, rounded up to 4)
+template <int D>
+__host__ __device__ inline ResLayout resident_layout(int cap) {
+  ResLayout L{};
+  const size_t c4 = ((size_t)cap + 3) / 4 * 4;
+  size_t o = 0;
+  L.keys = o;  o += c4 * D * 2;
+  L.score = o; o += c4 * 4;
+  L.gum = o;   o += c4 * 4;
+  L.pos = o;   o += c4 * 4;
+  L.perm = o;  o += c4 * 4;
+  L.logit = o; o += (c4 + 4) * 4;
+  o = (o + 15) / 16 * 16;
+  L.queue = o; o += (size_t)kQ * res_slot_bytes<D>();
+  o = (o + 7) / 8 * 8;
+  L.bars = o;  o += (size_t)8 * (2 * kQ + 1);
+  L.redf = o;  o += 64 * 4;
+  L.redi = o;  o += 64 * 4;
+  L.total = o;
+  return L;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const DecodeArgs a) {
+  using G = Geo<D>;
+  using Chunk = typename G::Chunk;
+  using Word = typename G::Word;
+  constexpr int CH = G::CH, HALF = G::HALF, ROWB = G::ROWB;
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const ResLayout SL = resident_layout<D>(a.capm_max);
+  __half* Ks = reinterpret_cast<__half*>(smem + SL.keys);
+  float* sc = reinterpret_cast<float*>(smem + SL.score);
+  float* gm = reinterpret_cast<float*>(smem + SL.gum);
+  int* ps = reinterpret_cast<int*>(smem + SL.pos);
+  int* pm = reinterpret_cast<int*>(smem + SL.perm);
+  float* lg = reinterpret_cast<float*>(smem + SL.logit);
+  unsigned char* queue = smem + SL.queue;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SL.bars);
+  float* redf = reinterpret_cast<float*>(smem + SL.redf);
+  int* redi = reinterpret_cast<int*>(smem + SL.redi);
+  __shared__ int s_abort;
+  auto kfull = [&](int q) { return smem_addr(&bars[q]); };
+  auto kempty = [&](int q) { return smem_addr(&bars[kQ + q]); };
+  const uint32_t loaded = smem_addr(&bars[2 * kQ]);
+
+  if (tid == 0) {
+    for (int q = 0; q < kQ; ++q) {
+      mbar_init(kfull(q), 32);               // every helper lane
+      mbar_init(kempty(q), kConsumerWarps);  // each consumer warp
+    }
+    mbar_init(loaded, 1);
+    fence_mbar_init();
+    s_abort = 0;
+  }
+  __syncthreads();
+  volatile int* abort_flag = &s_abort;
+
+  const int row = blockIdx.x;   // layer-major cache row
+  const int BH = a.B * a.H;
+  const int l = row / BH;
+  const int rem = row - l * BH;
+  const int b = rem / a.H;
+  const int hh = rem - b * a.H;
+  const LayerInfo li = a.layers[l];
+  const int budget = li.budget;
+  const int64_t in_off = (((int64_t)b * a.L + l) * a.H + hh);
+
+  if (warp == kHelperWarp) {
+    // ------------------------------------------------------------ helper
+    // Eight steps at a time: their keys are read together (eight loads in
+    // flight per lane) and lanes 0..7 take one step's Gumbel value each.
+    for (int t0 = 0; t0 < a.T; t0 += kGroup) {
+      const int cnt = min(kGroup, a.T - t0);
+      Word w[kGroup];
+#pragma unroll
+      for (int u = 0; u < kGroup; ++u)
+        if (u < cnt)
+          w[u] = reinterpret_cast<const Word*>(a.k_new + (int64_t)(t0 + u) * a.k_step + in_off * a.k_stride)[lane];
+      float gv = 0.f, tv = 0.f;
+      if (lane < cnt) {
+        gv = gumbel_at(a.seed, l, hh, a.p0 + t0 + lane);
+        tv = tau_at(a, a.p0 + t0 + lane);
+      }
+      bool ok = true;
+#pragma unroll
+      for (int u = 0; u < kGroup; ++u) {
+        const float g_u = __shfl_sync(0xffffffffu, gv, u);
+        const float t_u = __shfl_sync(0xffffffffu, tv, u);
+        if (u >= cnt || !ok) continue;
+        const int t = t0 + u;
+        const int q = t % kQ;
+        if (t >= kQ) ok = wait_watch(kempty(q), (uint32_t)((t / kQ - 1) & 1), abort_flag, a.err);
+        ok = __all_sync(0xffffffffu, ok);   // the lanes leave together
+        if (!ok) continue;
+        unsigned char* slot = queue + (size_t)q * res_slot_bytes<D>();
+        reinterpret_cast<Word*>(slot + sizeof(StepIn))[lane] = w[u];
+        if (lane == 0) {
+          StepIn* si = reinterpret_cast<StepIn*>(slot);
+          si->p = a.p0 + t;
+          si->gnew = g_u;
+          si->tau = t_u;
+        }
+        __syncwarp();
+        mbar_arrive_cta(kfull(q));
+      }
+      if (!ok) break;
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int c = tid & (kTPR - 1);   // chunk index within a row
+  const int rg = tid >> 3;          // row within a pass
+  const int64_t kbase = li.row_base + (int64_t)rem * li.cap;
+  const int64_t mbase = li.meta_base + (int64_t)rem * li.capm;
+  __half* Kg = a.K + kbase * D;
+  float* scg = a.score + mbase;
+  float* gg = a.gum + mbase;
+  int32_t* pg = a.pos + mbase;
+
+  // the row as the arena holds it: n kept rows, plus the slot e0 the last
+  // step evicted and left in place (rows after it not yet moved or rotated)
+  int n = (int)(a.p0 < (int64_t)budget ? a.p0 : (int64_t)budget);
+  const int e0 = __ldcg(a.pend + row);
+  const int nphys = n + (e0 >= 0 ? 1 : 0);
+  if (tid == 0) {
+    const bool stall = a.stall && blockIdx.x == 0;   // test hook: a barrier nothing completes
+    const uint32_t lo_rows = (uint32_t)(e0 >= 0 ? e0 : nphys);
+    const uint32_t hi_rows = (uint32_t)(e0 >= 0 ? nphys - e0 - 1 : 0);
+    const uint32_t bytes = (lo_rows + hi_rows) * ROWB;
+    if (!stall) {   // one arrival, completing once the copies' bytes have landed
+      mbar_expect_tx(loaded, bytes);
+      if (lo_rows) bulk_g2s(smem_addr(Ks), Kg, lo_rows * ROWB, loaded);
+      if (hi_rows) bulk_g2s(smem_addr(Ks + (size_t)e0 * D), Kg + (size_t)(e0 + 1) * D, hi_rows * ROWB, loaded);
+    }
+  }
+  for (int j = tid; j < n; j += kConsumers) {
+    const int src = (e0 >= 0 && j >= e0) ? j + 1 : j;
+    sc[j] = scg[src];
+    gm[j] = gg[src];
+    ps[j] = pg[src];
+    pm[j] = j;
+  }
+  float2 rc[CH / 2], rs[CH / 2];   // shift-by-one RoPE constants of this thread's pairs
+#pragma unroll
+  for (int k = 0; k < CH / 2; ++k) {
+    rc[k] = make_float2(a.rope_c[c * CH + 2 * k], a.rope_c[c * CH + 2 * k + 1]);
+    rs[k] = make_float2(a.rope_s[c * CH + 2 * k], a.rope_s[c * CH + 2 * k + 1]);
+  }
+  const bool got_row = wait_watch(loaded, 0, abort_flag, a.err);
+  bool aborted = consumers_any(!got_row || *abort_flag);   // also publishes the metadata
+
+  int e_prev = e0;     // logical rows >= e_prev still owe their -1 rotation
+  int fr = n;          // the physical row the next new key goes to
+  int t = 0;
+  for (; t < a.T && !aborted; ++t) {
+    const int q = t % kQ;
+    const bool got = wait_watch(kfull(q), (uint32_t)((t / kQ) & 1), abort_flag, a.err);
+    if ((aborted = consumers_any(!got || *abort_flag))) break;
+    const unsigned char* slot = queue + (size_t)q * res_slot_bytes<D>();
+    const StepIn si = *reinterpret_cast<const StepIn*>(slot);
+    const unsigned char* qs = slot + sizeof(StepIn);
+    const Chunk q_lo = *reinterpret_cast<const Chunk*>(qs + c * CH * 2);
+    const Chunk q_hi = *reinterpret_cast<const Chunk*>(qs + (HALF + c * CH) * 2);
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cta(kempty(q));   // the slot's contents are in registers
+    if (tid < kTPR) {                            // the new key's storage for the coming steps
+      __half* dst = Ks + (size_t)fr * D;
+      *reinterpret_cast<Chunk*>(dst + c * CH) = q_lo;
+      *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = q_hi;
+    }
+    // Rows are visited in the streaming kernel's numbering: "physical" index R
+    // runs over the kept rows with the slot the last step evicted still in
+    // place (dead, skipped) and the new row last, so every thread takes the
+    // same rows in the same order as there and the results agree bit for bit.
+    const bool shift = e_prev >= 0;
+    const int nphys = n + (shift ? 1 : 0);
+    const int NR = nphys + 1;
+    const bool evict = n + 1 > budget;
+
+    // ------------------------------------------------ logits (and pending rotations)
+    float run_m = -INFINITY, run_l = 0.f;
+    if (tid < 32) {   // the new row against itself
+      float d = dot_chunks<CH>(q_lo, q_hi, q_lo, q_hi);
+      d += __shfl_xor_sync(0xffffffffu, d, 1);
+      d += __shfl_xor_sync(0xffffffffu, d, 2);
+      d += __shfl_xor_sync(0xffffffffu, d, 4);
+      if (tid == 0) {
+        lg[nphys] = d * a.scale2;
+        run_m = d * a.scale2;
+        run_l = 1.f;
+      }
+    }
+    for (int r0 = 0; r0 < nphys; r0 += 2 * kRowsPerPass) {
+      Chunk lo[2], hi[2];
+      bool live[2];
+      int Rr[2], ph[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {   // both rows' loads first
+        Rr[u] = r0 + u * kRowsPerPass + rg;
+        live[u] = Rr[u] < nphys && Rr[u] != e_prev;
+        ph[u] = live[u] ? pm[(shift && Rr[u] > e_prev) ? Rr[u] - 1 : Rr[u]] : 0;
+        const __half* src = Ks + (size_t)ph[u] * D;
+        lo[u] = *reinterpret_cast<const Chunk*>(src + c * CH);
+        hi[u] = *reinterpret_cast<const Chunk*>(src + HALF + c * CH);
+      }
+      float dot[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (live[u] && shift && Rr[u] > e_prev) {   // moved last step: re-rotate in place
+          float2 fa[CH / 2], fb[CH / 2];
+          unpack2<CH>(lo[u], fa);
+          unpack2<CH>(hi[u], fb);
+          rotate2<CH>(fa, fb, rc, rs);
+          lo[u] = pack2<CH>(fa);
+          hi[u] = pack2<CH>(fb);
+          __half* dst = Ks + (size_t)ph[u] * D;
+          *reinterpret_cast<Chunk*>(dst + c * CH) = lo[u];
+          *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = hi[u];
+        }
+        dot[u] = live[u] ? dot_chunks<CH>(lo[u], hi[u], q_lo, q_hi) : 0.f;
+      }
+      {
+        // reduce-scatter of the two rows' partial sums over the 8 threads of
+        // a row group (as in the streaming kernel)
+        const bool odd = (c & 1) != 0;
+        float mine = odd ? dot[1] : dot[0];
+        mine += __shfl_xor_sync(0xffffffffu, odd ? dot[0] : dot[1], 1);
+        mine += __shfl_xor_sync(0xffffffffu, mine, 2);
+        mine += __shfl_xor_sync(0xffffffffu, mine, 4);
+        const bool lv = odd ? live[1] : live[0];
+        const int Rw = odd ? Rr[1] : Rr[0];
+        if (lv && c < 2) {
+          const float sv = mine * a.scale2;   // base-2 logit
+          lg[Rw] = sv;
+          if (sv > run_m) {
+            run_l = run_l * ex2(run_m - sv) + 1.f;
+            run_m = sv;
+          } else {
+            run_l += ex2(sv - run_m);
+          }
+        }
+      }
+    }
+
+    // ------------------------------------------------ softmax, scores, selection
+    block_lse(run_m, run_l, redf);
+    const float m = run_m;
+    const float inv_l = 1.f / run_l;
+    float best_r = INFINITY;
+    int best_R = INT_MAX;
+    for (int R = tid; R < NR; R += kConsumers) {
+      if (R == e_prev) continue;
+      const int j = (shift && R > e_prev) ? R - 1 : R;                 // logical slot (the new row: n)
+      const float attn = ex2(lg[R] - m) * inv_l;
+      const float ns = a.mode ? attn : (j < n ? sc[j] : 0.f) + attn;   // current-step or cumulative
+      lg[R] = ns;
+      if (evict && R >= a.n_sink && j < n + 1 - a.recent) {
+        const float gv = j < n ? gm[j] : si.gnew;
+        const float r = fmaf(si.tau, gv, ns);
+        if (r < best_r) { best_r = r; best_R = R; }
+      }
+    }
+    int e = -1;   // the evicted slot, numbered over the n + 1 rows after the append
+    if (evict) {
+      const int R_e = block_argmin(best_r, best_R, redf, redi);   // its barrier also publishes lg
+      e = (shift && R_e > e_prev) ? R_e - 1 : R_e;
+    } else {
+      consumers_sync();
+    }
+    if (tid == 0) {
+      if (a.evicted) a.evicted[(int64_t)t * a.ev_step + in_off] = e;
+      if (evict && (e < a.n_sink || e >= n + 1 - a.recent)) atomicOr(a.err, kErrBadIndex);
+    }
+
+    // ------------------------------------------------ compaction of the slot arrays
+    // Slot j of the kept rows takes logical slot src = j (+1 from the evicted
+    // slot on); read everything first, then write, so no thread reads a slot
+    // another has already overwritten.
+    const int NK = evict ? n : n + 1;
+    const int fr_next = !evict ? n + 1 : (e < n ? pm[e] : fr);
+    float vs[kMaxPerThread], vg[kMaxPerThread];
+    int vp[kMaxPerThread], vm[kMaxPerThread];
+#pragma unroll
+    for (int k = 0; k < kMaxPerThread; ++k) {
+      const int j = tid + k * kConsumers;
+      if (j < NK) {
+        const int src = (evict && j >= e) ? j + 1 : j;
+        const bool old = src < n;
+        vs[k] = lg[(shift && src >= e_prev) ? src + 1 : src];
+        vg[k] = old ? gm[src] : si.gnew;
+        vp[k] = old ? ps[src] : (int)si.p;
+        vm[k] = old ? pm[src] : fr;
+      }
+    }
+    consumers_sync();
+#pragma unroll
+    for (int k = 0; k < kMaxPerThread; ++k) {
+      const int j = tid + k * kConsumers;
+      if (j < NK) {
+        sc[j] = vs[k];
+        gm[j] = vg[k];
+        ps[j] = vp[k];
+        pm[j] = vm[k];
+      }
+    }
+    consumers_sync();
+    fr = fr_next;
+    n = NK;
+    e_prev = evict ? e : -1;
+  }
+
+  if (aborted) {
+    if (tid == 0) (void)mbar_wait_bounded(loaded, 0, 10000000ull);   // no copy may still be landing
+    return;
+  }
+
+  // ------------------------------------------------------------ write-back
+  // The arena's layout after a step: the slot the last step evicted stays in
+  // place, dead, and the rows after it keep their slots and their
+  // un-re-rotated keys; the next step (or a flush) applies that compaction.
+  const int gshift = e_prev;   // -1: nothing pending
+  for (int j0 = 0; j0 < n; j0 += kRowsPerPass) {
+    const int j = j0 + rg;
+    if (j < n) {
+      const int gs = (gshift >= 0 && j >= gshift) ? j + 1 : j;
+      const __half* src = Ks + (size_t)pm[j] * D;
+      __half* dst = Kg + (size_t)gs * D;
+      *reinterpret_cast<Chunk*>(dst + c * CH) = *reinterpret_cast<const Chunk*>(src + c * CH);
+      *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = *reinterpret_cast<const Chunk*>(src + HALF + c * CH);
+    }
+  }
+  for (int j = tid; j < n; j += kConsumers) {
+    const int gs = (gshift >= 0 && j >= gshift) ? j + 1 : j;
+    scg[gs] = sc[j];
+    gg[gs] = gm[j];
+    pg[gs] = ps[j];
+  }
+  if (tid == 0) {
+    a.pend[row] = gshift;
+    a.done[row] = ((unsigned long long)(unsigned)(a.s0 + a.T) << 32) | (unsigned)(gshift + 1);
+  }
+}
+
+}  // namespace
+
+size_t resident_step_smem(int D, int capm_max) {
+  if (capm_max > kResidentMaxCap) return (size_t)-1;
+  return D == 64 ? resident_layout<64>(capm_max).total : resident_layout<128>(capm_max).total;
+}
+
+cudaError_t resident_step_setup(int D, size_t smem) {
+  if (D == 64)
+    return cudaFuncSetAttribute(resident_step_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return cudaFuncSetAttribute(resident_step_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+cudaError_t launch_resident_step(const DecodeArgs& a, int D, size_t smem, cudaStream_t s) {
+  if (a.rows <= 0 || a.T <= 0) return cudaSuccess;
+  if (D == 64)
+    resident_step_kernel<64><<<a.rows, kRThreads, smem, s>>>(a);
+  else
+    resident_step_kernel<128><<<a.rows, kRThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kvx

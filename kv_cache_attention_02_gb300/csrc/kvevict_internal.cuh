@@ -98,7 +98,12 @@ struct PrefillScoreArgs {
   int heads;
   float scale2;            // log2(e) / sqrt(D)
   int* err;                // error word for bounded waits, or null
+  int stall;               // test hook: pass 1's first CTA never issues its query tile's copy
 };
+
+// Test hook (kvevict_test_stall_next_step with a null handle): the next prompt
+// scorer launch in the process takes stall = 1; returns whether one was armed.
+bool take_scorer_stall();
 
 struct PrefillSelectArgs {
   const __half* keys;      // [heads, S_buf, D] for the heads of this launch; the first S rows used
@@ -134,6 +139,12 @@ size_t decode_step_smem(int D, int capm_max);
 cudaError_t decode_step_ctas_per_sm(int D, size_t smem, int* ctas);
 cudaError_t launch_decode_step(const DecodeArgs& a, int D, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_flush(const FlushArgs& a, int D, int heads, cudaStream_t s);
+// The shared-memory-resident decode step (decode_resident.cu): one CTA per row
+// for every step of the call. resident_step_smem returns (size_t)-1 when a
+// row of capm_max slots does not fit its layout.
+size_t resident_step_smem(int D, int capm_max);
+cudaError_t resident_step_setup(int D, size_t smem);
+cudaError_t launch_resident_step(const DecodeArgs& a, int D, size_t smem, cudaStream_t s);
 
 // Page-locked host memory (staging.cu). mapped_host: the device address of the
 // host buffer [p, p + bytes) when both its ends are page-locked and mapped into
@@ -154,7 +165,8 @@ cudaError_t launch_prefill_tc(const PrefillScoreArgs& a, int D, cudaStream_t s);
 size_t prefill_select_smem(int S);
 // The prompt's Gumbel values depend on (layer, head, position) only, not on the
 // batch row: out[(l*H + h)*Sp + j] = g(seed, l, h, j) for j < S.
-cudaError_t launch_gumbel_table(uint64_t seed, int L, int H, int S, int Sp, float* out, cudaStream_t s);
+cudaError_t launch_gumbel_table(uint64_t seed, int L, int H, int S, int Sp, float* out, int sms,
+                                cudaStream_t s);
 cudaError_t launch_prefill_select(const PrefillSelectArgs& a, int D, int heads, cudaStream_t s);
 
 // ---------------------------------------------------------------- device helpers

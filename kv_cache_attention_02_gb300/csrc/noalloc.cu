@@ -13,11 +13,17 @@
 // loads this library, for as long as the process lives. Every call shares it:
 // calls whose work overlaps on the GPU (different streams, or other threads)
 // race on it and must be serialised by the caller.
+//
+// A bounded wait in the scorer that runs out (1 s) cannot be reported through
+// the return code, which the call gives before the GPU runs. The scorer sets a
+// file-scope error word instead, which each call clears first, and the last
+// kernel of the call then writes NaN to every output instead of the scores.
 #include "kvevict.h"
 #include "kvevict_internal.cuh"
 
 #include <nvtx3/nvToolsExt.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 #include <string>
@@ -34,25 +40,36 @@ constexpr int kMaxDevices = 64;
 // Working memory of the allocation-free scorer: [2, heads, Sp] floats (the
 // row log-sum-exps, then the padded column sums).
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+// Error word of the allocation-free scorer's bounded waits (cleared by each call).
+static __device__ __align__(256) int g_noalloc_err;
+
+struct DeviceSetup {
+  float* scratch = nullptr;   // device address of g_noalloc_scratch
+  int* err = nullptr;         // device address of g_noalloc_err
+  int sms = 0;                // multiprocessors, to size the gather's grid
+  bool tc_ready[2] = {false, false};   // scorer's shared-memory attribute set (D = 64, 128)
+};
 
 std::mutex g_setup_mu;
-float* g_scratch_ptr[kMaxDevices] = {};
-bool g_setup_done[kMaxDevices][2] = {};
+DeviceSetup g_setup[kMaxDevices];
 
-// Copy the padded column sums [heads, Sp] to the caller's [heads, S].
-__global__ void gather_colsum_kernel(const float* src, int Sp, float* dst, int S, int64_t total) {
+// Copy the padded column sums [heads, Sp] to the caller's [heads, S]; if a
+// bounded wait of this call's scorer ran out, write NaN instead.
+__global__ void gather_colsum_kernel(const float* src, int Sp, float* dst, int S, int64_t total,
+                                     const int* err) {
+  const bool failed = *reinterpret_cast<const volatile int*>(err) != 0;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t h = i / S;
     const int64_t j = i - h * S;
-    dst[i] = src[h * Sp + j];
+    dst[i] = failed ? __int_as_float(0x7fc00000) : src[h * Sp + j];
   }
 }
 
 // Once per device (and head_dim), with that device current: resolve the
-// device address of the scratch array and set the scoring kernels' shared
-// memory attribute.
-int setup_device(int D, float** scratch) {
+// device addresses of the scratch array and the error word, read the SM count
+// and set the scoring kernels' shared-memory attribute.
+int setup_device(int D, DeviceSetup* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) {
@@ -64,25 +81,32 @@ int setup_device(int D, float** scratch) {
     return KVEVICT_ERR_INVALID_ARG;
   }
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (!g_scratch_ptr[dev]) {
+  DeviceSetup& st = g_setup[dev];
+  if (!st.scratch) {
     void* p = nullptr;
+    void* q = nullptr;
+    int sms = 0;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&q, g_noalloc_err);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) {
-      kvx::set_last_error(std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+      kvx::set_last_error(std::string("device set-up: ") + cudaGetErrorString(e));
       return KVEVICT_ERR_CUDA;
     }
-    g_scratch_ptr[dev] = static_cast<float*>(p);
+    st.err = static_cast<int*>(q);
+    st.sms = sms > 0 ? sms : 1;
+    st.scratch = static_cast<float*>(p);
   }
   const int di = D == 64 ? 0 : 1;
-  if (!g_setup_done[dev][di]) {
+  if (!st.tc_ready[di]) {
     e = kvx::prefill_tc_setup(D);
     if (e != cudaSuccess) {
       kvx::set_last_error(std::string("prefill_tc_setup: ") + cudaGetErrorString(e));
       return KVEVICT_ERR_CUDA;
     }
-    g_setup_done[dev][di] = true;
+    st.tc_ready[di] = true;
   }
-  *scratch = g_scratch_ptr[dev];
+  *out = st;
   return KVEVICT_OK;
 }
 
@@ -114,26 +138,27 @@ int prefill_scores_noalloc(const uint16_t* keys, int32_t heads, int32_t S, int32
     kvx::set_last_error("heads * round_up(S, 128) exceeds the fixed scratch of 2,097,152 floats per pass");
     return KVEVICT_ERR_INVALID_ARG;
   }
-  float* scratch = nullptr;
-  const int rc = setup_device(head_dim, &scratch);
+  DeviceSetup dev;
+  const int rc = setup_device(head_dim, &dev);
   if (rc != KVEVICT_OK) return rc;
   cudaStream_t s = (cudaStream_t)stream;
   kvx::PrefillScoreArgs a{};
   a.keys = reinterpret_cast<const __half*>(keys);
-  a.lse2 = scratch;
-  a.colsum = scratch + (size_t)heads * Sp;
+  a.lse2 = dev.scratch;
+  a.colsum = dev.scratch + (size_t)heads * Sp;
   a.S = S;
   a.S_buf = S;
   a.Sp = (int)Sp;
   a.heads = heads;
   a.scale2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
-  a.err = nullptr;
-  cudaError_t e = kvx::launch_prefill_tc(a, head_dim, s);
+  a.err = dev.err;
+  a.stall = kvx::take_scorer_stall() ? 1 : 0;
+  cudaError_t e = cudaMemsetAsync(dev.err, 0, sizeof(int), s);   // writes, allocates nothing
+  if (e == cudaSuccess) e = kvx::launch_prefill_tc(a, head_dim, s);
   if (e == cudaSuccess) {
     const int64_t total = (int64_t)heads * S;
-    int64_t blocks = (total + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
-    gather_colsum_kernel<<<(unsigned)blocks, 256, 0, s>>>(a.colsum, (int)Sp, colsum, S, total);
+    const int64_t blocks = std::min<int64_t>((total + 255) / 256, (int64_t)dev.sms * 16);
+    gather_colsum_kernel<<<(unsigned)blocks, 256, 0, s>>>(a.colsum, (int)Sp, colsum, S, total, dev.err);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) {

@@ -95,10 +95,9 @@ __global__ void __launch_bounds__(kSThreads, 4) prefill_select_kernel(const Pref
   }
 
   const int m = S - a.n_sink - a.recent;   // evictable rows: not a sink, not in the recent window
-  int P2 = 1;
-  while (P2 < m) P2 <<= 1;
+  // m <= S keys; an even count keeps the next region 16-byte aligned
   uint64_t* keys = reinterpret_cast<uint64_t*>(smem);
-  unsigned char* flag = smem + (size_t)P2 * 8;
+  unsigned char* flag = smem + (size_t)((S + 1) & ~1) * 8;
   int16_t* newslot = reinterpret_cast<int16_t*>(flag + ((S + 15) & ~15));
   int* wsum = reinterpret_cast<int*>(newslot + ((S + 7) & ~7));
 
@@ -319,10 +318,8 @@ __global__ void __launch_bounds__(256) prefill_lastrow_kernel(const PrefillScore
 }  // namespace
 
 size_t prefill_select_smem(int S) {
-  int P2 = 1;
-  while (P2 < S) P2 <<= 1;
   // keys, flags, new slots, the scan's warp sums, the select's histogram and result
-  return (size_t)P2 * 8 + ((S + 15) & ~15) + ((S + 7) & ~7) * 2 + (32 + 256 + 4) * sizeof(int) + 64;
+  return (size_t)((S + 1) & ~1) * 8 + ((S + 15) & ~15) + ((S + 7) & ~7) * 2 + (32 + 256 + 4) * sizeof(int) + 64;
 }
 
 cudaError_t prefill_setup(int D, int max_prefill) {
@@ -350,10 +347,11 @@ cudaError_t launch_prefill_lastrow(const PrefillScoreArgs& a, int D, cudaStream_
   return cudaGetLastError();
 }
 
-cudaError_t launch_gumbel_table(uint64_t seed, int L, int H, int S, int Sp, float* out, cudaStream_t s) {
+cudaError_t launch_gumbel_table(uint64_t seed, int L, int H, int S, int Sp, float* out, int sms,
+                                cudaStream_t s) {
   const int64_t n = (int64_t)L * H * S;
   if (n <= 0) return cudaSuccess;
-  const int blocks = (int)std::min<int64_t>((n + 255) / 256, 152 * 16);
+  const int blocks = (int)std::min<int64_t>((n + 255) / 256, (int64_t)std::max(sms, 1) * 16);
   gumbel_table_kernel<<<blocks, 256, 0, s>>>(seed, H, S, Sp, n, out);
   return cudaGetLastError();
 }

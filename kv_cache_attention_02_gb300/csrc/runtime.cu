@@ -7,6 +7,7 @@
 
 #include <nvtx3/nvToolsExt.h>
 
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdio>
@@ -87,6 +88,11 @@ cudaError_t dalloc(T** p, size_t count) {
 
 namespace kvx {
 void set_last_error(const std::string& msg) { g_last_error = msg; }
+
+namespace {
+std::atomic<bool> g_stall_next_scorer{false};   // kvevict_test_stall_next_step(NULL)
+}
+bool take_scorer_stall() { return g_stall_next_scorer.exchange(false); }
 }  // namespace kvx
 
 struct kvevict {
@@ -115,6 +121,8 @@ struct kvevict {
   int64_t Sp_max = 0;
   size_t decode_smem = 0;
   int decode_grid = 0;      // persistent decode CTAs
+  size_t resident_smem = 0; // the resident decode step's shared memory
+  bool resident_ok = false; // rows fit the resident decode step (key-only handle)
   int sms = 0;              // SMs on the device
   int64_t next_pos = 0;
   bool stepped = false;
@@ -133,6 +141,10 @@ struct kvevict {
 };
 
 namespace {
+
+// Shortest call the automatic choice gives the resident decode step (it reads
+// and writes each row once per call, the streaming step once per step).
+constexpr int kResidentMinSteps = 4;
 
 int64_t BLHD(const kvevict* h) { return (int64_t)h->B * h->L * h->H * h->D; }
 int64_t BLH(const kvevict* h) { return (int64_t)h->B * h->L * h->H; }
@@ -181,7 +193,11 @@ int enqueue_steps(kvevict* h, const uint16_t* keys, const uint16_t* values, int6
   a.seed = h->cfg.seed;
   a.stall = h->stall_next ? 1 : 0;
   h->stall_next = false;
-  KV_CUDA(kvx::launch_decode_step(a, h->D, h->decode_grid, h->decode_smem, s));
+  const int kind = h->cfg.decode_kernel;
+  if (h->resident_ok && kind != KVEVICT_DECODE_STREAM && (kind == KVEVICT_DECODE_RESIDENT || T >= kResidentMinSteps))
+    KV_CUDA(kvx::launch_resident_step(a, h->D, h->resident_smem, s));
+  else
+    KV_CUDA(kvx::launch_decode_step(a, h->D, h->decode_grid, h->decode_smem, s));
   h->dsteps += T;
   return KVEVICT_OK;
 }
@@ -202,10 +218,12 @@ int enqueue_prompt_scores(kvevict* h, const uint16_t* keys, const uint16_t* valu
   sa.heads = heads;
   sa.scale2 = (float)(1.4426950408889634 / std::sqrt((double)h->D));
   sa.err = h->err;
-  if (h->cfg.score_mode == KVEVICT_SCORE_CURRENT)
+  if (h->cfg.score_mode == KVEVICT_SCORE_CURRENT) {
     KV_CUDA(kvx::launch_prefill_lastrow(sa, h->D, s));
-  else
+  } else {
+    sa.stall = kvx::take_scorer_stall() ? 1 : 0;
     KV_CUDA(kvx::launch_prefill_tc(sa, h->D, s));
+  }
   kvx::PrefillSelectArgs pa{};
   pa.keys = sa.keys;
   pa.values = reinterpret_cast<const __half*>(values);
@@ -238,7 +256,7 @@ int enqueue_prompt_scores(kvevict* h, const uint16_t* keys, const uint16_t* valu
 
 int enqueue_gumbel_table(kvevict* h, int32_t S, cudaStream_t s) {
   const int Sp = (S + kvx::kPrefillRowPad - 1) / kvx::kPrefillRowPad * kvx::kPrefillRowPad;
-  KV_CUDA(kvx::launch_gumbel_table(h->cfg.seed, h->L, h->H, S, Sp, h->gtab, s));
+  KV_CUDA(kvx::launch_gumbel_table(h->cfg.seed, h->L, h->H, S, Sp, h->gtab, h->sms, s));
   return KVEVICT_OK;
 }
 
@@ -353,6 +371,9 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
     return fail(KVEVICT_ERR_INVALID_ARG, "prefill_mode must be KVEVICT_PREFILL_BULK or KVEVICT_PREFILL_SEQUENTIAL");
   if (c.score_mode != KVEVICT_SCORE_CUMULATIVE && c.score_mode != KVEVICT_SCORE_CURRENT)
     return fail(KVEVICT_ERR_INVALID_ARG, "score_mode must be KVEVICT_SCORE_CUMULATIVE or KVEVICT_SCORE_CURRENT");
+  if (c.decode_kernel != KVEVICT_DECODE_AUTO && c.decode_kernel != KVEVICT_DECODE_STREAM &&
+      c.decode_kernel != KVEVICT_DECODE_RESIDENT)
+    return fail(KVEVICT_ERR_INVALID_ARG, "decode_kernel must be KVEVICT_DECODE_AUTO, _STREAM or _RESIDENT");
 
   std::vector<int32_t> budgets(c.n_layers);
   if (c.layer_budgets) {
@@ -423,8 +444,14 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
         kvx::prefill_select_smem(std::max(1, c.max_prefill)) + 1024 > (size_t)optin ||
         kvx::prefill_tc_smem(h->D) + 1024 > (size_t)optin)
       return bail(fail(KVEVICT_ERR_INVALID_ARG, "layer budget or max_prefill too large for shared memory"));
+    h->resident_smem = kvx::resident_step_smem(h->D, h->capm_max);
+    h->resident_ok = !c.with_values && h->resident_smem != (size_t)-1 && h->resident_smem + 1024 <= (size_t)optin;
+    if (c.decode_kernel == KVEVICT_DECODE_RESIDENT && !h->resident_ok)
+      return bail(fail(KVEVICT_ERR_INVALID_ARG,
+                       "the resident decode kernel needs a key-only handle whose rows fit in shared memory"));
   }
   KV_CUDA_CREATE(kvx::decode_step_setup(h->D, h->decode_smem));
+  if (h->resident_ok) KV_CUDA_CREATE(kvx::resident_step_setup(h->D, h->resident_smem));
   {
     int per_sm = 0, sms = 0;
     KV_CUDA_CREATE(kvx::decode_step_ctas_per_sm(h->D, h->decode_smem, &per_sm));
@@ -756,7 +783,10 @@ int kvevict_read_state(kvevict_t* h, int32_t b, int32_t l, int32_t head, uint16_
 }
 
 int kvevict_test_stall_next_step(kvevict_t* h) {
-  if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
+  if (!h) {
+    kvx::g_stall_next_scorer.store(true);
+    return KVEVICT_OK;
+  }
   h->stall_next = true;
   return KVEVICT_OK;
 }

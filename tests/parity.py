@@ -17,9 +17,17 @@ oracle state so the two stay comparable for the rest of the run. The oracle
 itself never reads CUDA output: the choice is made here, after checking it
 against the oracle's own tie set.
 
-"Relative" uses the magnitude of the terms that form r = score + tau*g, so a
-near-cancellation of score against tau*g is still judged against the rounding
-those terms carry.
+"Relative" is relative to |r| (the plain reading): the CUDA path may pick
+another row only when it lies within TIE_REL * |r| of the oracle's lowest.
+For information a wider set is counted as well, whose tolerance scales with
+the magnitude of the terms forming r = score + tau*g (|r| + |score| +
+|tau*g|, the rounding a near-cancellation of score against tau*g carries):
+``ties`` counts the steps that are ties under that wider rule, ``ties_plain``
+those that are ties under the plain rule, and a divergence that only the
+wider rule would admit is a failure (``tie_divergences_wide_only`` stays 0).
+
+Value rows (a value-carrying cache) are compared bit for bit: they are moved,
+never computed.
 """
 from __future__ import annotations
 
@@ -29,7 +37,6 @@ import numpy as np
 
 TIE_REL = 1e-5
 SCORE_RTOL = 1e-4
-SCORE_ATOL = 1e-6
 
 
 @dataclass
@@ -39,9 +46,12 @@ class RowReport:
     evicted_first: int = 0        # evictions of the first candidate slot (n_sink)
     evicted_last: int = 0         # evictions of the last candidate slot (the new row when recent = 0)
     evicted_mid: int = 0          # evictions strictly between them
-    ties: int = 0                 # steps whose two lowest r are within TIE_REL
+    ties: int = 0                 # steps whose two lowest r are within TIE_REL (wide rule)
+    ties_plain: int = 0           # ... of which also within TIE_REL * |r| (plain rule)
     tie_divergences: int = 0      # ties where the CUDA path picked another tied row
+    tie_divergences_wide_only: int = 0   # ... at a step that is a tie under the wide rule only
     prefill_tie: bool = False
+    prefill_tie_wide_only: bool = False
     gumbel_ulp_outliers: int = 0
     max_key_ulp: int = 0
     max_score_rel: float = 0.0
@@ -55,7 +65,9 @@ def _scale(head, j: int, tau: float) -> float:
     return abs(head.r[j]) + abs(head.score[j]) + abs(tau * float(head.g[j]))
 
 
-def _tie_set(head, tau: float, n_sink: int, recent: int = 0) -> tuple[list[int], float]:
+def _tie_set(head, tau: float, n_sink: int, recent: int = 0, plain: bool = False) -> tuple[list[int], float]:
+    """Rows whose r is within the tie tolerance of the lowest (lowest first).
+    plain: the tolerance is TIE_REL * |r| instead of the wide rule's scale."""
     n = head.n
     r = head.r[:n]
     cand = np.arange(n_sink, n - recent)
@@ -65,7 +77,10 @@ def _tie_set(head, tau: float, n_sink: int, recent: int = 0) -> tuple[list[int],
     gap = np.inf
     for j in order[1:]:
         j = int(j)
-        tol = TIE_REL * max(_scale(head, best, tau), _scale(head, j, tau))
+        if plain:
+            tol = TIE_REL * max(abs(r[best]), abs(r[j]))
+        else:
+            tol = TIE_REL * max(_scale(head, best, tau), _scale(head, j, tau))
         d = r[j] - r[best]
         if len(ties) == 1:
             gap = d
@@ -85,8 +100,13 @@ def ulp_diff_f16(a: np.ndarray, b: np.ndarray) -> np.ndarray:
 
 
 def compare_state(rep: RowReport, where: str, orc_state, gpu_state):
-    oK, osc, og, opos = orc_state
-    gK, gsc, gg, gpos = gpu_state
+    """States are (keys, scores, gumbel, positions) or, on a value-carrying
+    cache, (keys, scores, gumbel, positions, values)."""
+    oK, osc, og, opos = orc_state[:4]
+    gK, gsc, gg, gpos = gpu_state[:4]
+    if len(orc_state) != len(gpu_state):
+        rep.failures.append(f"{where}: one side carries value rows, the other does not")
+        return
     if len(opos) != len(gpos):
         rep.failures.append(f"{where}: kept {len(gpos)} rows, oracle {len(opos)}")
         return
@@ -103,19 +123,28 @@ def compare_state(rep: RowReport, where: str, orc_state, gpu_state):
         err = np.abs(gsc.astype(np.float64) - osc)
         rep.max_score_rel = max(rep.max_score_rel,
                                 float((err / np.maximum(np.abs(osc), 1e-12)).max()))
-        bad = err > SCORE_RTOL * np.abs(osc) + SCORE_ATOL
+        bad = err > SCORE_RTOL * np.abs(osc)
         if bad.any():
             j = int(np.nonzero(bad)[0][0])
             rep.failures.append(f"{where}: score slot {j}: gpu {gsc[j]!r} oracle {osc[j]!r}")
         gdiff = np.abs(og.view(np.int32).astype(np.int64) - gg.view(np.int32).astype(np.int64))
-        rep.gumbel_ulp_outliers = int((gdiff == 1).sum())
+        rep.gumbel_ulp_outliers += int((gdiff == 1).sum())
         if (gdiff > 1).any():
             rep.failures.append(f"{where}: gumbel values differ by more than 1 ULP")
+        if len(orc_state) == 5:
+            oV, gV = orc_state[4], gpu_state[4]
+            if oV.shape != gV.shape or not np.array_equal(oV, gV):
+                rep.failures.append(f"{where}: value rows differ")
 
 
-def _replay_steps(orc, prm, head, keys, gpu_ev, rep, what, checkpoints=None):
+def _state(head):
+    st = head.state()
+    return st + (head.values(),) if head.V is not None else st
+
+
+def _replay_steps(orc, prm, head, keys, gpu_ev, rep, what, checkpoints=None, values=None):
     for t in range(int(keys.shape[0])):
-        head.accumulate(keys[t])
+        head.accumulate(keys[t], None if values is None else values[t])
         rep.steps += 1
         eg = int(gpu_ev[t])
         if not head.over_budget():
@@ -127,13 +156,23 @@ def _replay_steps(orc, prm, head, keys, gpu_ev, rep, what, checkpoints=None):
         tau = orc.tau(prm.tau_init, prm.tau_end, prm.anneal_steps, head.next_pos - 1)
         head.regularised()
         ties, gap = _tie_set(head, tau, prm.n_sink, prm.recent)
+        plain = ties   # the plain rule's set is a prefix of the wide rule's
         if len(ties) > 1:
             rep.ties += 1
+            plain = _tie_set(head, tau, prm.n_sink, prm.recent, plain=True)[0]
+            if len(plain) > 1:
+                rep.ties_plain += 1
         e = ties[0]
         if eg != e:
-            if eg in ties:
+            if eg in plain:
                 rep.tie_divergences += 1
                 e = eg
+            elif eg in ties:
+                rep.tie_divergences_wide_only += 1
+                rep.failures.append(
+                    f"{what} {t} (pos {head.next_pos - 1}): gpu evicted {eg} (r={head.r[eg]}), "
+                    f"oracle {e} (r={head.r[e]}): a tie only under the wider rule")
+                return
             else:
                 rep.failures.append(
                     f"{what} {t} (pos {head.next_pos - 1}): gpu evicted {eg} "
@@ -149,22 +188,25 @@ def _replay_steps(orc, prm, head, keys, gpu_ev, rep, what, checkpoints=None):
             rep.evicted_mid += 1
         head.evict(e)
         if checkpoints and (t + 1) in checkpoints:
-            compare_state(rep, f"after step {t + 1}", head.state(), checkpoints[t + 1])
+            compare_state(rep, f"after step {t + 1}", _state(head), checkpoints[t + 1])
             if rep.failures:
                 return
 
 
 def run_row(orc, prm, prefill_keys, decode_keys, gpu_ev, gpu_after_prefill=None,
-            gpu_final=None, checkpoints=None, gpu_prompt_ev=None) -> RowReport:
+            gpu_final=None, checkpoints=None, gpu_prompt_ev=None, values=None) -> RowReport:
     """Replay one cache row on the oracle and compare it with the CUDA path.
 
     gpu_ev: int32 [T] evicted slots the CUDA path reported per decode step.
-    gpu_after_prefill / gpu_final: (keys, scores, gumbel, positions) read back
-    from the CUDA path after the prompt and at the end. checkpoints: optional
-    {step_index: state} read back after that many decode steps.
+    gpu_after_prefill / gpu_final: (keys, scores, gumbel, positions[, values])
+    read back from the CUDA path after the prompt and at the end. checkpoints:
+    optional {step_index: state} read back after that many decode steps.
+    values: (prompt value rows [S, D] or None, decode value rows [T, D]) for a
+    value-carrying cache; the oracle then carries them too.
     """
     rep = RowReport()
-    head = orc.OracleHead(prm)
+    head = orc.OracleHead(prm, values=values is not None)
+    pre_v, dec_v = values if values is not None else (None, None)
     S = 0 if prefill_keys is None else int(prefill_keys.shape[0])
     if S > 0 and getattr(prm, "prefill_mode", 0) == 1:
         # one step per prompt token: replay them like decode steps against the
@@ -172,11 +214,11 @@ def run_row(orc, prm, prefill_keys, decode_keys, gpu_ev, gpu_after_prefill=None,
         if gpu_prompt_ev is None:
             rep.failures.append("sequential prompt needs the CUDA path's prompt eviction log")
             return rep
-        _replay_steps(orc, prm, head, prefill_keys, gpu_prompt_ev, rep, "prompt step")
+        _replay_steps(orc, prm, head, prefill_keys, gpu_prompt_ev, rep, "prompt step", values=pre_v)
         if rep.failures:
             return rep
         if gpu_after_prefill is not None:
-            compare_state(rep, "after prefill", head.state(), gpu_after_prefill)
+            compare_state(rep, "after prefill", _state(head), gpu_after_prefill)
             if rep.failures:
                 return rep
         S = 0   # the prompt is done
@@ -200,20 +242,37 @@ def run_row(orc, prm, prefill_keys, decode_keys, gpu_ev, gpu_after_prefill=None,
                          and np.all(gpu_only < S - prm.recent)
                          and np.all(r[gpu_only] - rs[k - 1] <= TIE_REL * scale[gpu_only])
                          and np.all(rs[k] - r[orc_only] <= TIE_REL * scale[orc_only]))
-                if not valid:
+                plain_ok = valid and (np.all(r[gpu_only] - rs[k - 1] <= TIE_REL * np.abs(r[gpu_only]))
+                                      and np.all(rs[k] - r[orc_only] <= TIE_REL * np.abs(r[orc_only])))
+                if not plain_ok:
+                    rep.prefill_tie_wide_only = valid
                     diff = np.nonzero(gmask != mask)[0]
-                    rep.failures.append(f"prefill selection differs at rows {diff[:8].tolist()}")
+                    rep.failures.append(f"prefill selection differs at rows {diff[:8].tolist()}"
+                                        + (" (a tie only under the wider rule)" if valid else ""))
                     return rep
                 rep.prefill_tie = True
                 mask = gmask
-        head.prefill_apply(prefill_keys, colsum, g, mask)
+        head.prefill_apply(prefill_keys, colsum, g, mask, pre_v)
         if gpu_after_prefill is not None:
-            compare_state(rep, "after prefill", head.state(), gpu_after_prefill)
+            compare_state(rep, "after prefill", _state(head), gpu_after_prefill)
             if rep.failures:
                 return rep
-    _replay_steps(orc, prm, head, decode_keys, gpu_ev, rep, "step", checkpoints)
+    _replay_steps(orc, prm, head, decode_keys, gpu_ev, rep, "step", checkpoints, values=dec_v)
     if rep.failures:
         return rep
     if gpu_final is not None:
-        compare_state(rep, "final", head.state(), gpu_final)
+        compare_state(rep, "final", _state(head), gpu_final)
     return rep
+
+
+def summarise(reports) -> dict:
+    """Totals over many rows' reports (for the tests' printed summaries)."""
+    reps = list(reports)
+    tot = lambda f: sum(getattr(r, f) for r in reps)
+    return {"rows": len(reps), "evictions": tot("evictions"), "ties": tot("ties"),
+            "ties_plain": tot("ties_plain"), "tie_divergences": tot("tie_divergences"),
+            "tie_divergences_wide_only": tot("tie_divergences_wide_only"),
+            "prefill_ties": tot("prefill_tie"), "prefill_ties_wide_only": tot("prefill_tie_wide_only"),
+            "gumbel_ulp_outliers": tot("gumbel_ulp_outliers"),
+            "max_key_ulp": max((r.max_key_ulp for r in reps), default=0),
+            "max_score_rel": max((r.max_score_rel for r in reps), default=0.0)}

@@ -90,3 +90,34 @@ def test_stall_hook_is_one_shot():
     h.decode(dec)          # no hook armed now: runs clean
     h.check()
     h.close()
+
+
+def test_prompt_scorer_wait_that_runs_out_is_reported():
+    """The same for the tensor-core prompt scorer: with a null handle the hook
+    makes the next scorer launch leave one copy unissued, so the MMA issuer's
+    bounded wait runs out; the prompt's handle reports DEVICE_CHECK and, after
+    a reset, reproduces a fresh handle's results."""
+    import kv_cache_attention_02_gb300 as kvx
+    from workloads import gpu as wgpu
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pre, dec = wgpu.device_inputs(WL)
+    h = kvx.from_workload(WL)
+    assert kvx.lib().kvevict_test_stall_next_step(None) == kvx.OK
+    t0 = time.perf_counter()
+    h.prefill(pre)
+    with pytest.raises(kvx.KVEvictError) as err:
+        h.check()
+    elapsed = time.perf_counter() - t0
+    assert err.value.code == kvx.ERR_DEVICE_CHECK
+    assert elapsed < 10.0, f"the stalled prompt took {elapsed:.1f} s"
+    ref = kvx.from_workload(WL)
+    want_ev, want = _run(kvx, ref, pre, dec)
+    ref.close()
+    h.reset()
+    got_ev, got = _run(kvx, h, pre, dec)
+    h.close()
+    assert np.array_equal(got_ev, want_ev)
+    for r in _rows(WL):
+        for x, y in zip(got[r], want[r]):
+            assert np.array_equal(x, y), f"row {r}"

@@ -3,9 +3,12 @@
 Small configurations compare every cache row over the whole run (several TMA
 tiles, ragged tails, every edge case the method has); the five full-size
 workloads run exactly as the benchmark launches them (prompt, then one launch
-of all decode steps) and compare sampled rows over the whole run.
+of all decode steps) and compare, over the whole run, every row of
+keyformer_llama3.2-3b and at least one row of every layer of the others.
 """
 import concurrent.futures as cf
+import json
+import os
 
 import numpy as np
 import pytest
@@ -42,53 +45,77 @@ def head_params(orc, wl, l, h):
                           mode=wl.score_mode, prefill_mode=wl.prefill_mode)
 
 
-def run_gpu(kvx, wgpu, wl, rows, segments=None, mode="multi"):
-    """Run the workload on the GPU; read back the sampled rows."""
-    h = kvx.from_workload(wl)
+def value_workload(wl):
+    """The value rows fed alongside wl's keys: any distinct fp16 payload; the
+    key generator with another seed gives one, on the host and the device."""
+    return wl.scaled(key_seed=wl.key_seed + 1000)
+
+
+def run_gpu(kvx, wgpu, wl, rows, segments=None, mode="multi", with_values=False, decode_kernel=0):
+    """Run the workload on the GPU; read back the sampled rows (with their
+    value rows, as a fifth element, on a value-carrying handle). decode_kernel:
+    0 the library's choice, 1 the streaming step, 2 the shared-memory-resident
+    step."""
+    h = kvx.from_workload(wl, with_values=with_values, decode_kernel=decode_kernel)
     pre, dec = wgpu.device_inputs(wl)
+    vpre, vdec = wgpu.device_inputs(value_workload(wl)) if with_values else (None, None)
+
+    def read(r):
+        st = h.read_state(*r)
+        return st + (h.read_values(*r),) if with_values else st
+
     after_prefill = {}
     pev = None
     if pre is not None:
         if wl.prefill_mode == 1:
             pev = torch.full((wl.prefill, wl.batch, wl.n_layers, wl.n_kv_heads), -7,
                              dtype=torch.int32, device="cuda")
-        h.prefill(pre, pev)
-        after_prefill = {r: h.read_state(*r) for r in rows}
+        h.prefill(pre, pev, values=vpre)
+        after_prefill = {r: read(r) for r in rows}
     T = wl.decode
     ev = torch.full((T, wl.batch, wl.n_layers, wl.n_kv_heads), -7, dtype=torch.int32, device="cuda")
     bounds = sorted(set([0, T] + list(segments or [])))
     checkpoints = {r: {} for r in rows}
     for t0, t1 in zip(bounds, bounds[1:]):
         if mode == "multi":
-            h.decode(dec[t0:t1], ev[t0:t1])
+            h.decode(dec[t0:t1], ev[t0:t1], values=vdec[t0:t1] if with_values else None)
         else:
             for t in range(t0, t1):
-                h.step(dec[t], ev[t])
+                h.step(dec[t], ev[t], v_new=vdec[t] if with_values else None)
         if t1 != T:
             for r in rows:
-                checkpoints[r][t1] = h.read_state(*r)
-    final = {r: h.read_state(*r) for r in rows}
+                checkpoints[r][t1] = read(r)
+    final = {r: read(r) for r in rows}
     h.check()
     evh = ev.cpu().numpy()
     pevh = pev.cpu().numpy() if pev is not None else None
     h.close()
-    del pre, dec, ev
+    del pre, dec, ev, vpre, vdec
     torch.cuda.empty_cache()
     return after_prefill, evh, final, checkpoints, pevh
 
 
-def compare_rows(orc, wl, rows, after_prefill, evh, final, checkpoints, pevh=None, threads=8):
+def compare_rows(orc, wl, rows, after_prefill, evh, final, checkpoints, pevh=None, threads=None,
+                 with_values=False):
+    """Replay each row on the oracle (threads: the oracle's C calls release the
+    interpreter lock) and require every row to agree."""
     import parity
+    vwl = value_workload(wl) if with_values else None
 
     def one(r):
         b, l, hh = r
         keys = wl.head_keys(b, l, hh, 0, wl.positions)
+        vals = None
+        if with_values:
+            v = vwl.head_keys(b, l, hh, 0, wl.positions)
+            vals = (v[: wl.prefill] if wl.prefill else None, v[wl.prefill:])
         prm = head_params(orc, wl, l, hh)
         return r, parity.run_row(orc, prm, keys[: wl.prefill] if wl.prefill else None,
                                  keys[wl.prefill:], evh[:, b, l, hh], after_prefill.get(r), final[r],
                                  checkpoints.get(r),
-                                 pevh[:, b, l, hh] if pevh is not None else None)
+                                 pevh[:, b, l, hh] if pevh is not None else None, values=vals)
 
+    threads = threads or min(16, os.cpu_count() or 4)
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
         reports = dict(ex.map(one, rows))
     bad = {r: rep.failures for r, rep in reports.items() if not rep.ok()}
@@ -156,11 +183,15 @@ SMALL = [
 _SLOT_KINDS = {"first": 0, "last": 0, "mid": 0}
 
 
+KERNELS = {"stream": 1, "resident": 2}
+
+
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
 @pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
-def test_small_all_rows(kvx, wgpu, orc, wl):
+def test_small_all_rows(kvx, wgpu, orc, wl, kernel):
     rows = all_rows(wl)
     seg = [wl.decode // 3]
-    res = run_gpu(kvx, wgpu, wl, rows, segments=seg)
+    res = run_gpu(kvx, wgpu, wl, rows, segments=seg, decode_kernel=KERNELS[kernel])
     reps = compare_rows(orc, wl, rows, *res)
     assert sum(r.evictions for r in reps.values()) > 0
     for r in reps.values():
@@ -178,15 +209,46 @@ def test_small_runs_evicted_first_mid_and_last_slots():
     assert all(v > 0 for v in _SLOT_KINDS.values()), _SLOT_KINDS
 
 
+def assert_same_run(a, b):
+    """Two run_gpu results agree bit for bit: eviction logs, prompt logs and
+    every read-back state (prompt, checkpoints, final)."""
+    assert np.array_equal(a[1], b[1])
+    if a[4] is not None or b[4] is not None:
+        assert np.array_equal(a[4], b[4])
+    for k in (0, 2):
+        assert a[k].keys() == b[k].keys()
+        for r in a[k]:
+            for x, y in zip(a[k][r], b[k][r]):
+                assert np.array_equal(x, y), f"row {r}"
+    for r in a[3]:
+        assert a[3][r].keys() == b[3][r].keys()
+        for t in a[3][r]:
+            for x, y in zip(a[3][r][t], b[3][r][t]):
+                assert np.array_equal(x, y), f"row {r} after step {t}"
+
+
 def test_step_path_equals_multistep_path(kvx, wgpu):
+    # one launch of every step (the resident kernel) against one launch per
+    # step (the streaming kernel): the two kernels visit rows in the same
+    # order and agree bit for bit
     wl = SMALL[0]
     rows = all_rows(wl)
     a = run_gpu(kvx, wgpu, wl, rows, mode="multi")
     b = run_gpu(kvx, wgpu, wl, rows, mode="step")
-    assert np.array_equal(a[1], b[1])
-    for r in rows:
-        for x, y in zip(a[2][r], b[2][r]):
-            assert np.array_equal(x, y)
+    assert_same_run(a, b)
+
+
+@pytest.mark.parametrize("wl", [w for w in SMALL if w.decode >= 8][:6] + [workloads.LATE_RISER_ANNEAL.scaled(
+    name="late_riser_short", batch=2, n_layers=3, decode=600)], ids=lambda w: w.name)
+def test_resident_kernel_equals_streaming_kernel(kvx, wgpu, wl):
+    """The shared-memory-resident decode step and the streaming one give the
+    same eviction logs, keys, scores, Gumbel values and positions, bit for bit,
+    with checkpoints cutting the run into several calls."""
+    rows = all_rows(wl)
+    seg = [1, wl.decode // 3, wl.decode // 3 + 5]
+    a = run_gpu(kvx, wgpu, wl, rows, segments=seg, decode_kernel=KERNELS["stream"])
+    b = run_gpu(kvx, wgpu, wl, rows, segments=seg, decode_kernel=KERNELS["resident"])
+    assert_same_run(a, b)
 
 
 def test_batched_equals_single_row(kvx, wgpu):
@@ -367,15 +429,56 @@ FULL = [workloads.KEYFORMER_3B, workloads.PYRAMIDKV, workloads.LATE_RISER_TAU0,
         workloads.LATE_RISER_ANNEAL, workloads.LARGE_CONTEXT]
 
 
+def full_size_rows(wl):
+    """The rows the full-size parity replays on the oracle: all of them when
+    there are at most 256 (keyformer_llama3.2-3b's 224); otherwise every layer
+    (each has its own budget, so its own tile count and metadata layout),
+    with the batch and head indices varied from layer to layer: one row per
+    layer from 32 layers up (pyramidkv, large_context), four per layer below
+    (the late-riser runs: 64 rows), plus the first and last row."""
+    if wl.n_heads <= 256:
+        return all_rows(wl)
+    per_layer = 1 if wl.n_layers >= 32 else max(1, 64 // wl.n_layers)
+    rows = {(0, 0, 0), (wl.batch - 1, wl.n_layers - 1, wl.n_kv_heads - 1)}
+    for l in range(wl.n_layers):
+        for k in range(per_layer):
+            rows.add(((5 * l + 3 * k + 1) % wl.batch, l, (3 * l + 2 * k + 1) % wl.n_kv_heads))
+    return sorted(rows)
+
+
+def _report(name, reps):
+    import parity
+    summary = dict(workload=name, **parity.summarise(reps.values()))
+    print("PARITY " + json.dumps(summary))
+    return summary
+
+
 @pytest.mark.parametrize("wl", FULL, ids=lambda w: w.name)
-def test_full_size_sampled_rows(kvx, wgpu, orc, wl):
-    rows = sampled_rows(wl, k=8)
+def test_full_size_rows(kvx, wgpu, orc, wl):
+    rows = full_size_rows(wl)
     res = run_gpu(kvx, wgpu, wl, rows, segments=[wl.decode // 2])
-    reps = compare_rows(orc, wl, rows, *res, threads=8)
-    total = sum(r.evictions for r in reps.values())
-    ties = sum(r.ties for r in reps.values())
-    div = sum(r.tie_divergences for r in reps.values())
-    print(f"{wl.name}: rows {len(rows)} evictions {total} ties {ties} tie-divergences {div} "
-          f"max key ulp {max(r.max_key_ulp for r in reps.values())} "
-          f"max score rel {max(r.max_score_rel for r in reps.values()):.2e}")
-    assert total > 0
+    reps = compare_rows(orc, wl, rows, *res)
+    summary = _report(wl.name, reps)
+    assert summary["evictions"] > 0
+    assert len({l for _, l, _ in rows}) == wl.n_layers
+
+
+@pytest.mark.parametrize("wl", [workloads.KEYFORMER_3B, workloads.LATE_RISER_ANNEAL], ids=lambda w: w.name)
+def test_full_size_streaming_kernel(kvx, wgpu, wl):
+    """Where the library picks the resident decode kernel at full size, the
+    streaming kernel gives the same run bit for bit (sampled rows)."""
+    rows = sampled_rows(wl, k=16, seed=4)
+    a = run_gpu(kvx, wgpu, wl, rows, segments=[wl.decode // 2], decode_kernel=KERNELS["stream"])
+    b = run_gpu(kvx, wgpu, wl, rows, segments=[wl.decode // 2], decode_kernel=KERNELS["resident"])
+    assert_same_run(a, b)
+
+
+def test_full_size_value_rows(kvx, wgpu, orc):
+    """keyformer_llama3.2-3b with value rows: 64 seeded rows (of 224) replayed
+    on the oracle carrying the same value rows; value rows bit-exact."""
+    wl = workloads.KEYFORMER_3B
+    rows = sampled_rows(wl, k=64, seed=3)
+    res = run_gpu(kvx, wgpu, wl, rows, segments=[wl.decode // 2], with_values=True)
+    reps = compare_rows(orc, wl, rows, *res, with_values=True)
+    summary = _report(wl.name + "+values", reps)
+    assert summary["evictions"] > 0

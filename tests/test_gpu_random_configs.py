@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 
-from test_gpu_parity import all_rows, compare_rows, run_gpu, sampled_rows  # noqa: E402
+from test_gpu_parity import all_rows, assert_same_run, compare_rows, run_gpu, sampled_rows  # noqa: E402
 
 _EDGES = [1, 2, 63, 64, 65, 127, 128, 129, 191, 192]
 
@@ -76,6 +76,9 @@ def test_random_config_all_rows(wl):
     rows = all_rows(wl)
     res = run_gpu(kvx, wgpu, wl, rows, segments=[wl.decode // 2])
     compare_rows(orc, wl, rows, *res)
+    # the streaming decode kernel gives the same run bit for bit (the library's
+    # choice above is the resident one wherever the rows fit)
+    assert_same_run(res, run_gpu(kvx, wgpu, wl, rows, segments=[wl.decode // 2], decode_kernel=1))
 
 
 def _medium_cases(n=_N_MEDIUM, seed=int(_SEED) + 1 if _SEED else 4051):
@@ -119,3 +122,4 @@ def test_random_medium_config_sampled_rows(wl):
     rows = sampled_rows(wl, k=12, seed=5)
     res = run_gpu(kvx, wgpu, wl, rows, segments=[wl.decode // 2])
     compare_rows(orc, wl, rows, *res)
+    assert_same_run(res, run_gpu(kvx, wgpu, wl, rows, segments=[wl.decode // 2], decode_kernel=1))

@@ -1,9 +1,14 @@
-"""Value rows move with their keys (keyformer page, KeyformerState.values;
-keyformer_update step 3: survivors keep their temporal order) and are never
-rotated, so the value rows a cache row keeps are exactly the input value rows
-of its kept positions, in slot order. The positions themselves are checked
-against the oracle by the parity tests; here the values are checked bit for
-bit against that closed form, and the decisions against a key-only run."""
+"""Value rows on the CUDA path against the oracle carrying the same value rows.
+
+Page "veloxquant_mlx.quantizers.keyformer module": KeyformerState.values holds
+one fp16 value row per kept token, keyformer_update appends it with its key and
+moves it with the key when an earlier row is evicted (step 3), and
+keyformer_get_kv returns keys and values together. A value row is never
+rotated. Each case runs a value-carrying handle and replays every row on the
+oracle with the same value rows: eviction logs and positions as in the key-only
+parity, value rows bit-exact. The decisions must also equal a key-only run's
+(values never influence them).
+"""
 import numpy as np
 import pytest
 
@@ -40,51 +45,41 @@ def _random_cases(k=8):
     return out
 
 
-@pytest.mark.parametrize("wl", CASES + _random_cases(), ids=lambda w: w.name)
-@pytest.mark.parametrize("path", ["multi", "step"])
-def test_values_follow_positions(wl, path):
-    import kv_cache_attention_02_gb300 as kvx
-    from workloads import gpu as wgpu
+@pytest.fixture(scope="module")
+def kvx():
+    import kv_cache_attention_02_gb300 as k
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    pre, dec = wgpu.device_inputs(wl)
-    vwl = wl.scaled(key_seed=wl.key_seed + 1000)        # any distinct fp16 payload
-    vpre, vdec = wgpu.device_inputs(vwl)
-    shape = (wl.decode, wl.batch, wl.n_layers, wl.n_kv_heads)
-    runs = {}
-    for with_values in (False, True):
-        h = kvx.from_workload(wl, with_values=with_values)
-        ev = torch.full(shape, -7, dtype=torch.int32, device="cuda")
-        pev = None
-        if pre is not None:
-            pev = torch.full((wl.prefill,) + shape[1:], -7, dtype=torch.int32, device="cuda")
-            h.prefill(pre, pev, values=vpre)
-        if path == "multi":
-            h.decode(dec, ev, values=vdec)
-        else:
-            for t in range(wl.decode):
-                h.step(dec[t], ev[t], v_new=vdec[t])
-        rows = [(b, l, hh) for b in range(wl.batch) for l in range(wl.n_layers)
-                for hh in range(wl.n_kv_heads)]
-        st = {r: h.read_state(*r) for r in rows}
-        vals = {r: h.read_values(*r) for r in rows} if with_values else None
-        runs[with_values] = (ev.cpu().numpy(), pev.cpu().numpy() if pev is not None else None, st,
-                             vals)
-        h.close()
-    ev0, pev0, st0, _ = runs[False]
-    ev1, pev1, st1, vals = runs[True]
-    assert np.array_equal(ev0, ev1)
-    if pev0 is not None:
-        assert np.array_equal(pev0, pev1)
-    vin_dec = vdec.cpu().numpy().view(np.uint16)
-    vin_pre = vpre.cpu().numpy().view(np.uint16) if vpre is not None else None
-    moved = 0
-    for r, (K, sc, g, pos) in st1.items():
-        for x, y in zip(st0[r], st1[r]):
-            assert np.array_equal(x, y)
-        b, l, hh = r
-        allv = np.concatenate(([vin_pre[b, l, hh]] if vin_pre is not None else [])
-                              + [vin_dec[:, b, l, hh]])
-        assert np.array_equal(vals[r], allv[pos]), f"row {r}"
-        moved += int(np.sum(pos != np.arange(len(pos))))
+    k.lib()
+    return k
+
+
+@pytest.fixture(scope="module")
+def wgpu():
+    from workloads import gpu
+    gpu.lib()
+    return gpu
+
+
+@pytest.mark.parametrize("wl", CASES + _random_cases(), ids=lambda w: w.name)
+@pytest.mark.parametrize("path", ["multi", "step"])
+def test_values_match_oracle(kvx, wgpu, orc, wl, path):
+    from test_gpu_parity import all_rows, compare_rows, run_gpu
+    rows = all_rows(wl)
+    seg = [wl.decode // 3]
+    res = run_gpu(kvx, wgpu, wl, rows, segments=seg, mode=path, with_values=True)
+    reps = compare_rows(orc, wl, rows, *res, with_values=True)
+    assert sum(r.evictions for r in reps.values()) > 0
+    moved = sum(int(np.sum(st[3] != np.arange(len(st[3])))) for st in res[2].values())
     assert moved > 0
+    # the same decisions, bit for bit, as a key-only handle run the same way (a
+    # launch boundary and the checkpoint reads, which apply the pending
+    # compaction, change which threads sum which rows, so the scores of runs
+    # cut differently may differ in the last bit)
+    plain = run_gpu(kvx, wgpu, wl, rows, segments=seg, mode=path)
+    assert np.array_equal(plain[1], res[1])
+    if res[4] is not None:
+        assert np.array_equal(plain[4], res[4])
+    for r in rows:
+        for x, y in zip(plain[2][r], res[2][r][:4]):
+            assert np.array_equal(x, y)
