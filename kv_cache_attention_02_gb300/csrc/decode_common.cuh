@@ -96,15 +96,6 @@ __device__ __forceinline__ float dot_chunks(const typename std::conditional<CH =
   return s0 + s1;
 }
 
-__device__ __forceinline__ void warp_argmin(float& r, int& i) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float r2 = __shfl_xor_sync(0xffffffffu, r, o);
-    const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
-    if (r2 < r || (r2 == r && i2 < i)) { r = r2; i = i2; }
-  }
-}
-
 // 2^x on the MUFU (ex2.approx: relative error below 2^-22; a result below the
 // smallest normal flushes to zero, which only drops terms smaller than 2^-126
 // of the row's largest from a softmax sum).
@@ -115,46 +106,60 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // Block-wide (max, sum of 2^(x - max)) over the 256 consumer threads, logits
-// in base-2 units: the block max first (warp shuffles, then every thread
-// combines the eight warp maxima itself), then each thread's running sum
-// rescaled to it once and the sums added the same way. One barrier per half;
-// a row's step waits on this, so the few-row shapes feel every round.
+// in base-2 units, with one barrier: each warp takes its max (one redux) and
+// the sum of its threads' running sums rescaled to it (a butterfly), then
+// every thread combines the eight warps' (max, sum) pairs itself, in warp
+// order. A row's step waits on this, so the few-row shapes feel every round.
 __device__ void block_lse(float& m, float& l, float* red) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float wm = m;
+  float wm;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(wm) : "f"(m));
+  float ls = m == -INFINITY ? 0.f : l * ex2(m - wm);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
-  if (lane == 0) red[w] = wm;
+  for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+  if (lane == 0) {
+    red[w] = wm;
+    red[kConsumerWarps + w] = ls;
+  }
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
   float M = red[0];
 #pragma unroll
   for (int k = 1; k < kConsumerWarps; ++k) M = fmaxf(M, red[k]);
-  float ls = m == -INFINITY ? 0.f : l * ex2(m - M);
+  float L = 0.f;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-  if (lane == 0) red[16 + w] = ls;
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-  float L = red[16];
-#pragma unroll
-  for (int k = 1; k < kConsumerWarps; ++k) L += red[16 + k];
+  for (int k = 0; k < kConsumerWarps; ++k) {
+    const float mk = red[k];
+    L += mk == -INFINITY ? 0.f : red[kConsumerWarps + k] * ex2(mk - M);
+  }
   m = M;
   l = L;
 }
 
-// Block-wide (r, slot) argmin, lowest slot on ties: warp shuffles, then every
+// Order-preserving map of a float onto an unsigned key (-0 taken as +0).
+__device__ __forceinline__ uint32_t float_key(float f) {
+  const uint32_t u = __float_as_uint(f + 0.f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Block-wide (r, slot) argmin, lowest slot on ties: per warp two redux
+// minima (the key of r, then the slot among the lanes holding it), then every
 // thread merges the eight warp candidates itself.
 __device__ int block_argmin(float r, int i, float* redf, int* redi) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  warp_argmin(r, i);
-  if (lane == 0) { redf[40 + w] = r; redi[40 + w] = i; }
+  const uint32_t key = float_key(r);
+  uint32_t kmin, imin;
+  asm("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(kmin) : "r"(key));
+  const uint32_t cand = key == kmin ? (uint32_t)i : 0xffffffffu;
+  asm("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(imin) : "r"(cand));
+  if (lane == 0) { redf[40 + w] = __uint_as_float(kmin); redi[40 + w] = (int)imin; }
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-  float rb = redf[40];
+  uint32_t kb = __float_as_uint(redf[40]);
   int ib = redi[40];
 #pragma unroll
   for (int k = 1; k < kConsumerWarps; ++k) {
-    const float r2 = redf[40 + k];
+    const uint32_t k2 = __float_as_uint(redf[40 + k]);
     const int i2 = redi[40 + k];
-    if (r2 < rb || (r2 == rb && i2 < ib)) { rb = r2; ib = i2; }
+    if (k2 < kb || (k2 == kb && i2 < ib)) { kb = k2; ib = i2; }
   }
   return ib;
 }

@@ -52,7 +52,8 @@ struct StepIn {
 static_assert(sizeof(StepIn) == 16, "step input header");
 
 struct ResLayout {
-  size_t keys, score, gum, pos, perm, logit, queue, bars, redf, redi, total;
+  size_t keys, meta, logit, rope, queue, bars, redf, redi, total;
+  size_t arr_stride;   // words between consecutive slot arrays
 };
 
 template <int D>
@@ -64,13 +65,14 @@ __host__ __device__ inline ResLayout resident_layout(int cap) {
   ResLayout L{};
   const size_t c4 = ((size_t)cap + 3) / 4 * 4;
   size_t o = 0;
+  L.arr_stride = c4;
   L.keys = o;  o += c4 * D * 2;
-  L.score = o; o += c4 * 4;
-  L.gum = o;   o += c4 * 4;
-  L.pos = o;   o += c4 * 4;
-  L.perm = o;  o += c4 * 4;
+  // two copies of the four slot arrays (score, Gumbel value, position,
+  // physical row), each copy the four arrays back to back
+  L.meta = o;  o += 2 * 4 * c4 * 4;
   L.logit = o; o += (c4 + 4) * 4;
   o = (o + 15) / 16 * 16;
+  L.rope = o;  o += (size_t)D * 4;   // cos then sin of the shift by -1, D/2 each
   L.queue = o; o += (size_t)kQ * res_slot_bytes<D>();
   o = (o + 7) / 8 * 8;
   L.bars = o;  o += (size_t)8 * (2 * kQ + 1);
@@ -81,6 +83,8 @@ __host__ __device__ inline ResLayout resident_layout(int cap) {
 }
 
 template <int D>
+// Two CTAs (18 warps) fit on an SM at up to 96 registers a thread; at 104 the
+// register file of the SM sub-partition holding a CTA's ninth warp runs out.
 __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const DecodeArgs a) {
   using G = Geo<D>;
   using Chunk = typename G::Chunk;
@@ -92,10 +96,6 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
   const int warp = tid >> 5, lane = tid & 31;
   const ResLayout SL = resident_layout<D>(a.capm_max);
   __half* Ks = reinterpret_cast<__half*>(smem + SL.keys);
-  float* sc = reinterpret_cast<float*>(smem + SL.score);
-  float* gm = reinterpret_cast<float*>(smem + SL.gum);
-  int* ps = reinterpret_cast<int*>(smem + SL.pos);
-  int* pm = reinterpret_cast<int*>(smem + SL.perm);
   float* lg = reinterpret_cast<float*>(smem + SL.logit);
   unsigned char* queue = smem + SL.queue;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SL.bars);
@@ -174,52 +174,62 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
   // -------------------------------------------------------------- consumers
   const int c = tid & (kTPR - 1);   // chunk index within a row
   const int rg = tid >> 3;          // row within a pass
-  const int64_t kbase = li.row_base + (int64_t)rem * li.cap;
-  const int64_t mbase = li.meta_base + (int64_t)rem * li.capm;
-  __half* Kg = a.K + kbase * D;
-  float* scg = a.score + mbase;
-  float* gg = a.gum + mbase;
-  int32_t* pg = a.pos + mbase;
+  // the row in the arena (recomputed where used, to keep registers free)
+  auto arena_keys = [&]() { return a.K + (li.row_base + (int64_t)rem * li.cap) * D; };
+  auto arena_meta = [&]() { return li.meta_base + (int64_t)rem * li.capm; };
+
+  // The per-slot arrays are double-buffered: a step reads one copy and writes
+  // the other, so the compaction needs no barrier between its reads and writes.
+  // Copy `cur` holds, at word offsets 0, c4, 2 c4, 3 c4: scores, Gumbel values,
+  // positions and the physical row of each logical slot.
+  const int c4 = (int)SL.arr_stride;
+  uint32_t* meta0 = reinterpret_cast<uint32_t*>(smem + SL.meta);
+  int cur = 0;
+  auto sc_at = [&](int j) -> float& { return reinterpret_cast<float*>(meta0)[cur + j]; };
+  auto gm_at = [&](int j) -> float& { return reinterpret_cast<float*>(meta0)[cur + c4 + j]; };
+  auto ps_at = [&](int j) -> int& { return reinterpret_cast<int*>(meta0)[cur + 2 * c4 + j]; };
+  auto pm_at = [&](int j) -> int& { return reinterpret_cast<int*>(meta0)[cur + 3 * c4 + j]; };
 
   // the row as the arena holds it: n kept rows, plus the slot e0 the last
   // step evicted and left in place (rows after it not yet moved or rotated)
   int n = (int)(a.p0 < (int64_t)budget ? a.p0 : (int64_t)budget);
   const int e0 = __ldcg(a.pend + row);
-  const int nphys = n + (e0 >= 0 ? 1 : 0);
+  const int nphys0 = n + (e0 >= 0 ? 1 : 0);
   if (tid == 0) {
     const bool stall = a.stall && blockIdx.x == 0;   // test hook: a barrier nothing completes
-    const uint32_t lo_rows = (uint32_t)(e0 >= 0 ? e0 : nphys);
-    const uint32_t hi_rows = (uint32_t)(e0 >= 0 ? nphys - e0 - 1 : 0);
+    const uint32_t lo_rows = (uint32_t)(e0 >= 0 ? e0 : nphys0);
+    const uint32_t hi_rows = (uint32_t)(e0 >= 0 ? nphys0 - e0 - 1 : 0);
     const uint32_t bytes = (lo_rows + hi_rows) * ROWB;
     if (!stall) {   // one arrival, completing once the copies' bytes have landed
       mbar_expect_tx(loaded, bytes);
+      const __half* Kg = arena_keys();
       if (lo_rows) bulk_g2s(smem_addr(Ks), Kg, lo_rows * ROWB, loaded);
       if (hi_rows) bulk_g2s(smem_addr(Ks + (size_t)e0 * D), Kg + (size_t)(e0 + 1) * D, hi_rows * ROWB, loaded);
     }
   }
-  for (int j = tid; j < n; j += kConsumers) {
-    const int src = (e0 >= 0 && j >= e0) ? j + 1 : j;
-    sc[j] = scg[src];
-    gm[j] = gg[src];
-    ps[j] = pg[src];
-    pm[j] = j;
+  {
+    const int64_t mb = arena_meta();
+    for (int j = tid; j < n; j += kConsumers) {
+      const int src = (e0 >= 0 && j >= e0) ? j + 1 : j;
+      sc_at(j) = a.score[mb + src];
+      gm_at(j) = a.gum[mb + src];
+      ps_at(j) = a.pos[mb + src];
+      pm_at(j) = j;
+    }
   }
-  float2 rc[CH / 2], rs[CH / 2];   // shift-by-one RoPE constants of this thread's pairs
-#pragma unroll
-  for (int k = 0; k < CH / 2; ++k) {
-    rc[k] = make_float2(a.rope_c[c * CH + 2 * k], a.rope_c[c * CH + 2 * k + 1]);
-    rs[k] = make_float2(a.rope_s[c * CH + 2 * k], a.rope_s[c * CH + 2 * k + 1]);
-  }
-  const bool got_row = wait_watch(loaded, 0, abort_flag, a.err);
-  bool aborted = consumers_any(!got_row || *abort_flag);   // also publishes the metadata
+  // shift-by-one RoPE constants, read from shared memory where a row moved
+  // (registers are the resident step's scarcest resource)
+  float* rope_s_c = reinterpret_cast<float*>(smem + SL.rope);
+  for (int i = tid; i < D; i += kConsumers) rope_s_c[i] = i < HALF ? a.rope_c[i] : a.rope_s[i - HALF];
+  bool got = wait_watch(loaded, 0, abort_flag, a.err);
+  if (got && a.T > 0) got = wait_watch(kfull(0), 0, abort_flag, a.err);
+  bool aborted = consumers_any(!got || *abort_flag);   // also publishes the slot arrays
 
-  int e_prev = e0;     // logical rows >= e_prev still owe their -1 rotation
+  int e_prev = e0;     // physical slot the last step evicted (left in place), or -1
   int fr = n;          // the physical row the next new key goes to
   int t = 0;
   for (; t < a.T && !aborted; ++t) {
     const int q = t % kQ;
-    const bool got = wait_watch(kfull(q), (uint32_t)((t / kQ) & 1), abort_flag, a.err);
-    if ((aborted = consumers_any(!got || *abort_flag))) break;
     const unsigned char* slot = queue + (size_t)q * res_slot_bytes<D>();
     const StepIn si = *reinterpret_cast<const StepIn*>(slot);
     const unsigned char* qs = slot + sizeof(StepIn);
@@ -234,8 +244,9 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
     }
     // Rows are visited in the streaming kernel's numbering: "physical" index R
     // runs over the kept rows with the slot the last step evicted still in
-    // place (dead, skipped) and the new row last, so every thread takes the
-    // same rows in the same order as there and the results agree bit for bit.
+    // place (dead, skipped) and the new row last, and every row's logit is
+    // summed, and accumulated into the softmax statistics, by the same thread
+    // in the same order as there, so the two kernels agree bit for bit.
     const bool shift = e_prev >= 0;
     const int nphys = n + (shift ? 1 : 0);
     const int NR = nphys + 1;
@@ -254,29 +265,42 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
         run_l = 1.f;
       }
     }
-    for (int r0 = 0; r0 < nphys; r0 += 2 * kRowsPerPass) {
-      Chunk lo[2], hi[2];
-      bool live[2];
-      int Rr[2], ph[2];
+    // Four rows per thread per round: R = r0 + 32u + rg, u = 0..3. The thread
+    // the streaming kernel gives row R (chunk c = (R / 32) & 1 of its group)
+    // is the one that accumulates it here too, rows ascending.
+    for (int r0 = 0; r0 < nphys; r0 += 4 * kRowsPerPass) {
+      Chunk lo[4], hi[4];
+      bool live[4];
+      int Rr[4], ph[4];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {   // both rows' loads first
+      for (int u = 0; u < 4; ++u) {
         Rr[u] = r0 + u * kRowsPerPass + rg;
         live[u] = Rr[u] < nphys && Rr[u] != e_prev;
-        ph[u] = live[u] ? pm[(shift && Rr[u] > e_prev) ? Rr[u] - 1 : Rr[u]] : 0;
+        ph[u] = live[u] ? pm_at((shift && Rr[u] > e_prev) ? Rr[u] - 1 : Rr[u]) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {   // every row's loads before any arithmetic
         const __half* src = Ks + (size_t)ph[u] * D;
         lo[u] = *reinterpret_cast<const Chunk*>(src + c * CH);
         hi[u] = *reinterpret_cast<const Chunk*>(src + HALF + c * CH);
       }
-      float dot[2];
+      float dot[4];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < 4; ++u) {
         if (live[u] && shift && Rr[u] > e_prev) {   // moved last step: re-rotate in place
-          float2 fa[CH / 2], fb[CH / 2];
-          unpack2<CH>(lo[u], fa);
-          unpack2<CH>(hi[u], fb);
-          rotate2<CH>(fa, fb, rc, rs);
-          lo[u] = pack2<CH>(fa);
-          hi[u] = pack2<CH>(fb);
+          // one half2 pair at a time (the same operations, in the same order, as
+          // unpack2 + rotate2 + pack2), so few values are live at once
+          __half2* la = reinterpret_cast<__half2*>(&lo[u]);
+          __half2* hb = reinterpret_cast<__half2*>(&hi[u]);
+#pragma unroll
+          for (int k = 0; k < CH / 2; ++k) {
+            float2 fa = __half22float2(la[k]), fb = __half22float2(hb[k]);
+            const float2 rc = *reinterpret_cast<const float2*>(rope_s_c + c * CH + 2 * k);
+            const float2 rs = *reinterpret_cast<const float2*>(rope_s_c + HALF + c * CH + 2 * k);
+            rotate2<2>(&fa, &fb, &rc, &rs);
+            la[k] = __float22half2_rn(fa);
+            hb[k] = __float22half2_rn(fb);
+          }
           __half* dst = Ks + (size_t)ph[u] * D;
           *reinterpret_cast<Chunk*>(dst + c * CH) = lo[u];
           *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = hi[u];
@@ -284,23 +308,33 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
         dot[u] = live[u] ? dot_chunks<CH>(lo[u], hi[u], q_lo, q_hi) : 0.f;
       }
       {
-        // reduce-scatter of the two rows' partial sums over the 8 threads of
-        // a row group (as in the streaming kernel)
+        // Reduce-scatter of the four rows' partial sums over the 8 threads of a
+        // row group, with the streaming kernel's association ((c, c^1), then
+        // (c, c^2), then (c, c^4)): after the first exchange even threads hold
+        // rows 0 and 2, odd threads rows 1 and 3; after the second thread c
+        // holds row (c & 1) + 2 ((c >> 1) & 1); threads 0 and 1 then fetch
+        // rows 2 and 3 from threads 2 and 3.
         const bool odd = (c & 1) != 0;
-        float mine = odd ? dot[1] : dot[0];
-        mine += __shfl_xor_sync(0xffffffffu, odd ? dot[0] : dot[1], 1);
-        mine += __shfl_xor_sync(0xffffffffu, mine, 2);
+        const bool b1 = (c & 2) != 0;
+        const float p0 = (odd ? dot[1] : dot[0]) + __shfl_xor_sync(0xffffffffu, odd ? dot[0] : dot[1], 1);
+        const float p1 = (odd ? dot[3] : dot[2]) + __shfl_xor_sync(0xffffffffu, odd ? dot[2] : dot[3], 1);
+        float mine = (b1 ? p1 : p0) + __shfl_xor_sync(0xffffffffu, b1 ? p0 : p1, 2);
         mine += __shfl_xor_sync(0xffffffffu, mine, 4);
-        const bool lv = odd ? live[1] : live[0];
-        const int Rw = odd ? Rr[1] : Rr[0];
-        if (lv && c < 2) {
-          const float sv = mine * a.scale2;   // base-2 logit
-          lg[Rw] = sv;
-          if (sv > run_m) {
-            run_l = run_l * ex2(run_m - sv) + 1.f;
-            run_m = sv;
-          } else {
-            run_l += ex2(sv - run_m);
+        const float other = __shfl_xor_sync(0xffffffffu, mine, 2);
+        if (c < 2) {
+          const bool lv0 = odd ? live[1] : live[0], lv1 = odd ? live[3] : live[2];
+          const int R0 = odd ? Rr[1] : Rr[0], R1 = odd ? Rr[3] : Rr[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            if (k == 0 ? !lv0 : !lv1) continue;
+            const float sv = (k == 0 ? mine : other) * a.scale2;   // base-2 logit
+            lg[k == 0 ? R0 : R1] = sv;
+            if (sv > run_m) {
+              run_l = run_l * ex2(run_m - sv) + 1.f;
+              run_m = sv;
+            } else {
+              run_l += ex2(sv - run_m);
+            }
           }
         }
       }
@@ -312,16 +346,27 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
     const float inv_l = 1.f / run_l;
     float best_r = INFINITY;
     int best_R = INT_MAX;
-    for (int R = tid; R < NR; R += kConsumers) {
-      if (R == e_prev) continue;
-      const int j = (shift && R > e_prev) ? R - 1 : R;                 // logical slot (the new row: n)
-      const float attn = ex2(lg[R] - m) * inv_l;
-      const float ns = a.mode ? attn : (j < n ? sc[j] : 0.f) + attn;   // current-step or cumulative
-      lg[R] = ns;
-      if (evict && R >= a.n_sink && j < n + 1 - a.recent) {
-        const float gv = j < n ? gm[j] : si.gnew;
-        const float r = fmaf(si.tau, gv, ns);
-        if (r < best_r) { best_r = r; best_R = R; }
+    for (int R0 = tid; R0 < NR; R0 += 2 * kConsumers) {   // two rows per thread per round
+      float ns[2], rr[2];
+      bool ok[2], cand[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int R = R0 + k * kConsumers;
+        ok[k] = R < NR && R != e_prev;
+        const int j = (shift && R > e_prev) ? R - 1 : R;   // logical slot (the new row: n)
+        const float lgv = ok[k] ? lg[R] : 0.f;
+        const float old = (ok[k] && j < n) ? sc_at(j) : 0.f;
+        const float gv = (ok[k] && j < n) ? gm_at(j) : si.gnew;
+        const float attn = ex2(lgv - m) * inv_l;
+        ns[k] = a.mode ? attn : old + attn;   // current-step or cumulative
+        cand[k] = ok[k] && evict && R >= a.n_sink && j < n + 1 - a.recent;
+        rr[k] = fmaf(si.tau, gv, ns[k]);
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int R = R0 + k * kConsumers;
+        if (ok[k]) lg[R] = ns[k];
+        if (cand[k] && rr[k] < best_r) { best_r = rr[k]; best_R = R; }
       }
     }
     int e = -1;   // the evicted slot, numbered over the n + 1 rows after the append
@@ -338,39 +383,27 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
 
     // ------------------------------------------------ compaction of the slot arrays
     // Slot j of the kept rows takes logical slot src = j (+1 from the evicted
-    // slot on); read everything first, then write, so no thread reads a slot
-    // another has already overwritten.
+    // slot on) of the rows after the append; written to the other copy.
     const int NK = evict ? n : n + 1;
-    const int fr_next = !evict ? n + 1 : (e < n ? pm[e] : fr);
-    float vs[kMaxPerThread], vg[kMaxPerThread];
-    int vp[kMaxPerThread], vm[kMaxPerThread];
-#pragma unroll
-    for (int k = 0; k < kMaxPerThread; ++k) {
-      const int j = tid + k * kConsumers;
-      if (j < NK) {
-        const int src = (evict && j >= e) ? j + 1 : j;
-        const bool old = src < n;
-        vs[k] = lg[(shift && src >= e_prev) ? src + 1 : src];
-        vg[k] = old ? gm[src] : si.gnew;
-        vp[k] = old ? ps[src] : (int)si.p;
-        vm[k] = old ? pm[src] : fr;
-      }
+    const int fr_next = !evict ? n + 1 : (e < n ? pm_at(e) : fr);
+    const int nxt = cur ^ (4 * c4);   // the other copy
+    for (int j = tid; j < NK; j += kConsumers) {
+      const int src = (evict && j >= e) ? j + 1 : j;
+      const bool old = src < n;
+      reinterpret_cast<float*>(meta0)[nxt + j] = lg[(shift && src >= e_prev) ? src + 1 : src];
+      reinterpret_cast<float*>(meta0)[nxt + c4 + j] = old ? gm_at(src) : si.gnew;
+      reinterpret_cast<int*>(meta0)[nxt + 2 * c4 + j] = old ? ps_at(src) : (int)si.p;
+      reinterpret_cast<int*>(meta0)[nxt + 3 * c4 + j] = old ? pm_at(src) : fr;
     }
-    consumers_sync();
-#pragma unroll
-    for (int k = 0; k < kMaxPerThread; ++k) {
-      const int j = tid + k * kConsumers;
-      if (j < NK) {
-        sc[j] = vs[k];
-        gm[j] = vg[k];
-        ps[j] = vp[k];
-        pm[j] = vm[k];
-      }
-    }
-    consumers_sync();
+    cur = nxt;
     fr = fr_next;
     n = NK;
     e_prev = evict ? e : -1;
+    // the next step's inputs, and the barrier that publishes this step's
+    // slot arrays (and frees lg and the reduction scratch) before it
+    got = true;
+    if (t + 1 < a.T) got = wait_watch(kfull((t + 1) % kQ), (uint32_t)(((t + 1) / kQ) & 1), abort_flag, a.err);
+    aborted = consumers_any(!got || *abort_flag);
   }
 
   if (aborted) {
@@ -383,21 +416,23 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
   // place, dead, and the rows after it keep their slots and their
   // un-re-rotated keys; the next step (or a flush) applies that compaction.
   const int gshift = e_prev;   // -1: nothing pending
+  __half* Kg = arena_keys();
   for (int j0 = 0; j0 < n; j0 += kRowsPerPass) {
     const int j = j0 + rg;
     if (j < n) {
       const int gs = (gshift >= 0 && j >= gshift) ? j + 1 : j;
-      const __half* src = Ks + (size_t)pm[j] * D;
+      const __half* src = Ks + (size_t)pm_at(j) * D;
       __half* dst = Kg + (size_t)gs * D;
       *reinterpret_cast<Chunk*>(dst + c * CH) = *reinterpret_cast<const Chunk*>(src + c * CH);
       *reinterpret_cast<Chunk*>(dst + HALF + c * CH) = *reinterpret_cast<const Chunk*>(src + HALF + c * CH);
     }
   }
+  const int64_t mb = arena_meta();
   for (int j = tid; j < n; j += kConsumers) {
     const int gs = (gshift >= 0 && j >= gshift) ? j + 1 : j;
-    scg[gs] = sc[j];
-    gg[gs] = gm[j];
-    pg[gs] = ps[j];
+    a.score[mb + gs] = sc_at(j);
+    a.gum[mb + gs] = gm_at(j);
+    a.pos[mb + gs] = ps_at(j);
   }
   if (tid == 0) {
     a.pend[row] = gshift;
@@ -410,6 +445,11 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
 size_t resident_step_smem(int D, int capm_max) {
   if (capm_max > kResidentMaxCap) return (size_t)-1;
   return D == 64 ? resident_layout<64>(capm_max).total : resident_layout<128>(capm_max).total;
+}
+
+cudaError_t resident_step_ctas_per_sm(int D, size_t smem, int* ctas) {
+  if (D == 64) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, resident_step_kernel<64>, kRThreads, smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, resident_step_kernel<128>, kRThreads, smem);
 }
 
 cudaError_t resident_step_setup(int D, size_t smem) {

@@ -144,6 +144,7 @@ cudaError_t launch_flush(const FlushArgs& a, int D, int heads, cudaStream_t s);
 // row of capm_max slots does not fit its layout.
 size_t resident_step_smem(int D, int capm_max);
 cudaError_t resident_step_setup(int D, size_t smem);
+cudaError_t resident_step_ctas_per_sm(int D, size_t smem, int* ctas);
 cudaError_t launch_resident_step(const DecodeArgs& a, int D, size_t smem, cudaStream_t s);
 
 // Page-locked host memory (staging.cu). mapped_host: the device address of the

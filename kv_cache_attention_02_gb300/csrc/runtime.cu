@@ -123,6 +123,7 @@ struct kvevict {
   int decode_grid = 0;      // persistent decode CTAs
   size_t resident_smem = 0; // the resident decode step's shared memory
   bool resident_ok = false; // rows fit the resident decode step (key-only handle)
+  bool resident_auto = false; // the automatic choice takes the resident step (long enough calls)
   int sms = 0;              // SMs on the device
   int64_t next_pos = 0;
   bool stepped = false;
@@ -194,7 +195,8 @@ int enqueue_steps(kvevict* h, const uint16_t* keys, const uint16_t* values, int6
   a.stall = h->stall_next ? 1 : 0;
   h->stall_next = false;
   const int kind = h->cfg.decode_kernel;
-  if (h->resident_ok && kind != KVEVICT_DECODE_STREAM && (kind == KVEVICT_DECODE_RESIDENT || T >= kResidentMinSteps))
+  if (h->resident_ok && kind != KVEVICT_DECODE_STREAM &&
+      (kind == KVEVICT_DECODE_RESIDENT || (h->resident_auto && T >= kResidentMinSteps)))
     KV_CUDA(kvx::launch_resident_step(a, h->D, h->resident_smem, s));
   else
     KV_CUDA(kvx::launch_decode_step(a, h->D, h->decode_grid, h->decode_smem, s));
@@ -451,7 +453,21 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
                        "the resident decode kernel needs a key-only handle whose rows fit in shared memory"));
   }
   KV_CUDA_CREATE(kvx::decode_step_setup(h->D, h->decode_smem));
-  if (h->resident_ok) KV_CUDA_CREATE(kvx::resident_step_setup(h->D, h->resident_smem));
+  if (h->resident_ok) {
+    KV_CUDA_CREATE(kvx::resident_step_setup(h->D, h->resident_smem));
+    // The resident step runs one CTA per row, in waves when the rows outnumber
+    // the CTAs that fit; each wave runs every step. Measured on GB300 it beats
+    // the streaming step when the rows fit in one wave, or in two waves at two
+    // or more CTAs an SM (keys up to about 400 rows of head_dim 128); a row of
+    // 513 keys at one CTA an SM in two waves was slower (8.3 against 7.4 us).
+    int per_sm = 0, sms = 0;
+    KV_CUDA_CREATE(kvx::resident_step_ctas_per_sm(h->D, h->resident_smem, &per_sm));
+    KV_CUDA_CREATE(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device));
+    const int64_t slots = (int64_t)per_sm * sms;
+    const int64_t waves = slots > 0 ? (h->heads + slots - 1) / slots : INT64_MAX;
+    h->resident_auto = per_sm > 0 && (waves <= 1 || (waves <= 2 && per_sm >= 2));
+    if (per_sm < 1) h->resident_ok = false;
+  }
   {
     int per_sm = 0, sms = 0;
     KV_CUDA_CREATE(kvx::decode_step_ctas_per_sm(h->D, h->decode_smem, &per_sm));
