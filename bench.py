@@ -329,6 +329,8 @@ def main():
     h = kvx.from_workload(wl)
     state_bytes = h.device_bytes()   # the cache arena and prompt scratch (before any host staging)
     budgets = h.budgets
+    decode_kernel = ("resident_step_kernel" if h.decode_kernel_for(T) == kvx.DECODE_RESIDENT
+                     else "decode_step_kernel")
     ev = torch.empty((T, B, L, H), dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
 
@@ -431,9 +433,10 @@ def main():
                    "input_gb": round(heads * wl.positions * D * 2 / 1e9, 3)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": profiled_traffic(wl, os.path.join(ROOT, "kv_cache_attention_02_gb300", "csrc",
-                                                                  "decode.cu"), step_bytes),
-                     "kernel": "decode_step_kernel<128>" if D == 128 else "decode_step_kernel<64>",
+                     "traffic": (profiled_traffic(wl, os.path.join(ROOT, "kv_cache_attention_02_gb300", "csrc",
+                                                                   "decode.cu"), step_bytes)
+                                 if decode_kernel == "decode_step_kernel" else None),
+                     "kernel": f"{decode_kernel}<{D}>",
                      "bytes_per_launch": step_bytes, "launch_us": decode_ms * 1e3,
                      "steps_per_launch": T, "us_per_step": launch_ms * 1e3,
                      "peak_kind": f"of {peak_kind}"},

@@ -264,6 +264,12 @@ int kvevict_test_stall_next_step(kvevict_t* h);
  * keyformer_update_batched). *p: host int64. Errors: INVALID_ARG (null). */
 int kvevict_next_pos(const kvevict_t* h, int64_t* p);
 
+/* Which decode kernel a call of T steps runs on this handle (the choice
+ * kvevict_decode / kvevict_step make, see KVEVICT_DECODE_*): *kernel is
+ * KVEVICT_DECODE_STREAM or KVEVICT_DECODE_RESIDENT. Host only. Errors:
+ * INVALID_ARG (null pointers, T < 0). */
+int kvevict_decode_kernel_for(const kvevict_t* h, int32_t T, int32_t* kernel);
+
 /* Budget of layer l as resolved at create time. */
 int kvevict_layer_budget(const kvevict_t* h, int32_t l, int32_t* budget);
 

@@ -68,6 +68,7 @@ SIGNATURES = {
     "kvevict_flush": (ctypes.c_int, [P, P]),
     "kvevict_next_pos": (ctypes.c_int, [P, P]),
     "kvevict_layer_budget": (ctypes.c_int, [P, i32, P]),
+    "kvevict_decode_kernel_for": (ctypes.c_int, [P, i32, P]),
     "kvevict_layer_stats": (ctypes.c_int, [P, i32, P, P, P, P]),
     "kvevict_device_bytes": (ctypes.c_int, [P, P]),
     "kvevict_state_bytes": (ctypes.c_int, [P, P]),
@@ -259,6 +260,12 @@ class KVEvict:
         p = i64(0)
         _check(lib().kvevict_next_pos(self._h, ctypes.addressof(p)))
         return p.value
+
+    def decode_kernel_for(self, T: int) -> int:
+        """DECODE_STREAM or DECODE_RESIDENT: the kernel a call of T steps runs."""
+        k = i32(0)
+        _check(lib().kvevict_decode_kernel_for(self._h, T, ctypes.addressof(k)))
+        return k.value
 
     def layer_budget(self, l: int) -> int:
         b = i32(0)

@@ -147,6 +147,13 @@ namespace {
 // and writes each row once per call, the streaming step once per step).
 constexpr int kResidentMinSteps = 4;
 
+// The decode kernel a call of T steps runs (kvevict_config.decode_kernel).
+bool uses_resident(const kvevict* h, int64_t T) {
+  const int kind = h->cfg.decode_kernel;
+  return h->resident_ok && kind != KVEVICT_DECODE_STREAM &&
+         (kind == KVEVICT_DECODE_RESIDENT || (h->resident_auto && T >= kResidentMinSteps));
+}
+
 int64_t BLHD(const kvevict* h) { return (int64_t)h->B * h->L * h->H * h->D; }
 int64_t BLH(const kvevict* h) { return (int64_t)h->B * h->L * h->H; }
 
@@ -194,9 +201,7 @@ int enqueue_steps(kvevict* h, const uint16_t* keys, const uint16_t* values, int6
   a.seed = h->cfg.seed;
   a.stall = h->stall_next ? 1 : 0;
   h->stall_next = false;
-  const int kind = h->cfg.decode_kernel;
-  if (h->resident_ok && kind != KVEVICT_DECODE_STREAM &&
-      (kind == KVEVICT_DECODE_RESIDENT || (h->resident_auto && T >= kResidentMinSteps)))
+  if (uses_resident(h, T))
     KV_CUDA(kvx::launch_resident_step(a, h->D, h->resident_smem, s));
   else
     KV_CUDA(kvx::launch_decode_step(a, h->D, h->decode_grid, h->decode_smem, s));
@@ -838,6 +843,13 @@ int kvevict_check(kvevict_t* h, void* stream) {
   KV_RANGE();
   if (!h) return fail(KVEVICT_ERR_INVALID_ARG, "null handle");
   return check_error_word(h, (cudaStream_t)stream);
+}
+
+int kvevict_decode_kernel_for(const kvevict_t* h, int32_t T, int32_t* kernel) {
+  if (!h || !kernel) return fail(KVEVICT_ERR_INVALID_ARG, "null argument");
+  if (T < 0) return fail(KVEVICT_ERR_INVALID_ARG, "T must be >= 0");
+  *kernel = uses_resident(h, T) ? KVEVICT_DECODE_RESIDENT : KVEVICT_DECODE_STREAM;
+  return KVEVICT_OK;
 }
 
 int kvevict_next_pos(const kvevict_t* h, int64_t* p) {

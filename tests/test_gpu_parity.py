@@ -371,6 +371,31 @@ def test_reset_replays_identically(kvx, wgpu):
             assert np.array_equal(x, y)
 
 
+def test_decode_kernel_choice(kvx):
+    """The automatic choice: the resident step for calls of 4+ steps when the
+    rows fit in one wave, or two at two CTAs an SM; the streaming step
+    otherwise (long rows, value rows, short calls)."""
+    cases = [(workloads.TINY_H2O, 256, kvx.DECODE_RESIDENT),
+             (workloads.LATE_RISER_ANNEAL, 4096, kvx.DECODE_RESIDENT),
+             (workloads.KEYFORMER_3B, 2048, kvx.DECODE_STREAM),   # 513-key rows: 1 CTA an SM, 2 waves
+             (workloads.PYRAMIDKV, 2048, kvx.DECODE_STREAM),      # budget 1019: too long to be resident
+             (workloads.TINY_H2O, 3, kvx.DECODE_STREAM),          # a short call
+             (workloads.TINY_H2O, 1, kvx.DECODE_STREAM)]
+    for wl, T, want in cases:
+        h = kvx.from_workload(wl.scaled(prefill=0))
+        assert h.decode_kernel_for(T) == want, (wl.name, T)
+        h.close()
+    h = kvx.from_workload(workloads.TINY_H2O, with_values=True)
+    assert h.decode_kernel_for(256) == kvx.DECODE_STREAM
+    h.close()
+    h = kvx.from_workload(workloads.TINY_H2O, decode_kernel=kvx.DECODE_RESIDENT)
+    assert h.decode_kernel_for(1) == kvx.DECODE_RESIDENT
+    h.close()
+    with pytest.raises(kvx.KVEvictError) as err:   # rows too long to be resident
+        kvx.from_workload(workloads.PYRAMIDKV.scaled(prefill=0), decode_kernel=kvx.DECODE_RESIDENT)
+    assert err.value.code == kvx.ERR_INVALID_ARG
+
+
 def test_state_errors(kvx, wgpu):
     wl = SMALL[3]
     pre, dec = wgpu.device_inputs(wl)
