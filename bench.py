@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.ALL))
     ap.add_argument("--batch", type=int, default=None, help="override the batch (profiling)")
     ap.add_argument("--decode", type=int, default=None, help="override the decode steps (profiling)")
+    ap.add_argument("--decode-kernel", choices=["auto", "stream", "resident"], default="auto",
+                    help="decode kernel (the library's choice by default)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     return ap.parse_args()
@@ -326,7 +328,8 @@ def main():
     wl = workload_of(args)
     B, L, H, D, T = wl.batch, wl.n_layers, wl.n_kv_heads, wl.head_dim, wl.decode
     pre, dec = wgpu.device_inputs(wl)
-    h = kvx.from_workload(wl)
+    h = kvx.from_workload(wl, decode_kernel={"auto": kvx.DECODE_AUTO, "stream": kvx.DECODE_STREAM,
+                                             "resident": kvx.DECODE_RESIDENT}[args.decode_kernel])
     state_bytes = h.device_bytes()   # the cache arena and prompt scratch (before any host staging)
     budgets = h.budgets
     decode_kernel = ("resident_step_kernel" if h.decode_kernel_for(T) == kvx.DECODE_RESIDENT

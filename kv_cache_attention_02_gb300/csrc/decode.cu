@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
       const int32_t* s_pos =
           reinterpret_cast<const int32_t*>(P.packed ? mtile + 2 * arr : P.staged ? ring + (size_t)((um + 2) % kStages) * G::TILEB : ring + 2 * arr);
 
-      float run_m = -INFINITY, run_l = 0.f;   // this thread's share of the softmax statistics
+      float run_m = -INFINITY;   // the largest logit this thread wrote
       if (tid < 32) {   // logit of the new row against itself
         float d = dot_chunks<CH>(q_lo, q_hi, q_lo, q_hi);
         d += __shfl_xor_sync(0xffffffffu, d, 1);
@@ -416,7 +416,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
         if (tid == 0) {
           s_log[nphys] = d * a.scale2;
           run_m = d * a.scale2;
-          run_l = 1.f;
         }
       }
       for (int t = 0; t < P.ntiles; ++t) {
@@ -470,12 +469,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
           if (lv && c < 2) {
             const float sv = mine * a.scale2;   // base-2 logit
             s_log[Rw] = sv;
-            if (sv > run_m) {
-              run_l = run_l * ex2(run_m - sv) + 1.f;
-              run_m = sv;
-            } else {
-              run_l += ex2(sv - run_m);
-            }
+            run_m = fmaxf(run_m, sv);
           }
         }
         // Hand the stage back only after the arithmetic has consumed every
@@ -511,9 +505,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
       if (consumers_any(*abort_flag)) break;
 
       // -------------------------------------------------------------- softmax
-      block_lse(run_m, run_l, redf);
-      const float m = run_m;
-      const float inv_l = 1.f / run_l;
+      const float m = block_max(run_m, redf);
+      const float inv_l = 1.f / block_expsum(s_log, NR, e_prev, m, redf);   // s_log now holds the terms
 
       // --------------------------- accumulate, write back, select (one pass)
       // Every source is in shared memory, so each row's new score, its moved
@@ -523,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_step_kernel(const DecodeAr
       int best_R = INT_MAX;
       for (int R = tid; R < NR; R += kConsumers) {
         if (R == e_prev) continue;
-        const float attn = ex2(s_log[R] - m) * inv_l;
+        const float attn = s_log[R] * inv_l;
         const float ns = a.mode ? attn : (R < nphys ? s_sc[R] : 0.f) + attn;   // current-step or cumulative
         const bool moved = shift && R > e_prev;
         const int j = R - (moved ? 1 : 0);                                     // slot after compaction

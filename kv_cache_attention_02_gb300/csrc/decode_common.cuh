@@ -105,34 +105,46 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Block-wide (max, sum of 2^(x - max)) over the 256 consumer threads, logits
-// in base-2 units, with one barrier: each warp takes its max (one redux) and
-// the sum of its threads' running sums rescaled to it (a butterfly), then
-// every thread combines the eight warps' (max, sum) pairs itself, in warp
-// order. A row's step waits on this, so the few-row shapes feel every round.
-__device__ void block_lse(float& m, float& l, float* red) {
+// The softmax statistics of a step, in two block-wide passes over the logits
+// in shared memory (base-2 units). First the block max of every thread's
+// running max (one redux per warp, one barrier; a max is exact, so which
+// thread saw which logit does not matter). Then each thread sums
+// 2^(logit - max) over the rows R = tid, tid + 256, ... in ascending order,
+// storing each term back in place (the score update reuses it), and the block
+// adds the threads' sums with a butterfly per warp and the eight warp sums in
+// warp order (one barrier). Both decode kernels use exactly these two
+// functions and this row-to-thread assignment, so their sums agree bit for bit
+// whichever threads computed the dot products.
+__device__ float block_max(float m, float* red) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float wm;
   asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(wm) : "f"(m));
-  float ls = m == -INFINITY ? 0.f : l * ex2(m - wm);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-  if (lane == 0) {
-    red[w] = wm;
-    red[kConsumerWarps + w] = ls;
-  }
+  if (lane == 0) red[w] = wm;
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
   float M = red[0];
 #pragma unroll
   for (int k = 1; k < kConsumerWarps; ++k) M = fmaxf(M, red[k]);
-  float L = 0.f;
-#pragma unroll
-  for (int k = 0; k < kConsumerWarps; ++k) {
-    const float mk = red[k];
-    L += mk == -INFINITY ? 0.f : red[kConsumerWarps + k] * ex2(mk - M);
+  return M;
+}
+
+// Sum of 2^(lg[R] - M) over R < NR, R != skip; the terms replace the logits.
+__device__ float block_expsum(float* lg, int NR, int skip, float M, float* red) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float ls = 0.f;
+  for (int R = threadIdx.x; R < NR; R += kConsumers) {
+    if (R == skip) continue;
+    const float e = ex2(lg[R] - M);
+    lg[R] = e;
+    ls += e;
   }
-  m = M;
-  l = L;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+  if (lane == 0) red[kConsumerWarps + w] = ls;
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+  float L = red[kConsumerWarps];
+#pragma unroll
+  for (int k = 1; k < kConsumerWarps; ++k) L += red[kConsumerWarps + k];
+  return L;
 }
 
 // Order-preserving map of a float onto an unsigned key (-0 taken as +0).

@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
     const bool evict = n + 1 > budget;
 
     // ------------------------------------------------ logits (and pending rotations)
-    float run_m = -INFINITY, run_l = 0.f;
+    float run_m = -INFINITY;   // the largest logit this thread wrote
     if (tid < 32) {   // the new row against itself
       float d = dot_chunks<CH>(q_lo, q_hi, q_lo, q_hi);
       d += __shfl_xor_sync(0xffffffffu, d, 1);
@@ -262,12 +262,11 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
       if (tid == 0) {
         lg[nphys] = d * a.scale2;
         run_m = d * a.scale2;
-        run_l = 1.f;
       }
     }
-    // Four rows per thread per round: R = r0 + 32u + rg, u = 0..3. The thread
-    // the streaming kernel gives row R (chunk c = (R / 32) & 1 of its group)
-    // is the one that accumulates it here too, rows ascending.
+    // Four rows per thread per round: R = r0 + 32u + rg, u = 0..3. Which thread
+    // writes a logit does not matter: the softmax statistics are a block max and
+    // a sum in a fixed row order (block_max, block_expsum).
     for (int r0 = 0; r0 < nphys; r0 += 4 * kRowsPerPass) {
       Chunk lo[4], hi[4];
       bool live[4];
@@ -310,40 +309,31 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
       {
         // Reduce-scatter of the four rows' partial sums over the 8 threads of a
         // row group, with the streaming kernel's association ((c, c^1), then
-        // (c, c^2), then (c, c^4)): after the first exchange even threads hold
-        // rows 0 and 2, odd threads rows 1 and 3; after the second thread c
-        // holds row (c & 1) + 2 ((c >> 1) & 1); threads 0 and 1 then fetch
-        // rows 2 and 3 from threads 2 and 3.
+        // (c, c^2), then (c, c^4)), so each logit is bit for bit the one the
+        // streaming kernel computes: after the first exchange even threads hold
+        // rows 0 and 2, odd threads rows 1 and 3; after the second, thread c
+        // holds row (c & 1) + 2 ((c >> 1) & 1), and threads 0..3 write one each.
         const bool odd = (c & 1) != 0;
         const bool b1 = (c & 2) != 0;
         const float p0 = (odd ? dot[1] : dot[0]) + __shfl_xor_sync(0xffffffffu, odd ? dot[0] : dot[1], 1);
         const float p1 = (odd ? dot[3] : dot[2]) + __shfl_xor_sync(0xffffffffu, odd ? dot[2] : dot[3], 1);
         float mine = (b1 ? p1 : p0) + __shfl_xor_sync(0xffffffffu, b1 ? p0 : p1, 2);
         mine += __shfl_xor_sync(0xffffffffu, mine, 4);
-        const float other = __shfl_xor_sync(0xffffffffu, mine, 2);
-        if (c < 2) {
-          const bool lv0 = odd ? live[1] : live[0], lv1 = odd ? live[3] : live[2];
-          const int R0 = odd ? Rr[1] : Rr[0], R1 = odd ? Rr[3] : Rr[2];
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            if (k == 0 ? !lv0 : !lv1) continue;
-            const float sv = (k == 0 ? mine : other) * a.scale2;   // base-2 logit
-            lg[k == 0 ? R0 : R1] = sv;
-            if (sv > run_m) {
-              run_l = run_l * ex2(run_m - sv) + 1.f;
-              run_m = sv;
-            } else {
-              run_l += ex2(sv - run_m);
-            }
+        if (c < 4) {   // thread c holds row u = (c & 1) + 2 ((c >> 1) & 1)
+          const int u = (c & 1) + 2 * ((c >> 1) & 1);
+          const bool lv = u == 0 ? live[0] : u == 1 ? live[1] : u == 2 ? live[2] : live[3];
+          if (lv) {
+            const float sv = mine * a.scale2;   // base-2 logit
+            lg[r0 + u * kRowsPerPass + rg] = sv;
+            run_m = fmaxf(run_m, sv);
           }
         }
       }
     }
 
     // ------------------------------------------------ softmax, scores, selection
-    block_lse(run_m, run_l, redf);
-    const float m = run_m;
-    const float inv_l = 1.f / run_l;
+    const float m = block_max(run_m, redf);
+    const float inv_l = 1.f / block_expsum(lg, NR, e_prev, m, redf);   // lg now holds the terms
     float best_r = INFINITY;
     int best_R = INT_MAX;
     for (int R0 = tid; R0 < NR; R0 += 2 * kConsumers) {   // two rows per thread per round
@@ -357,7 +347,7 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
         const float lgv = ok[k] ? lg[R] : 0.f;
         const float old = (ok[k] && j < n) ? sc_at(j) : 0.f;
         const float gv = (ok[k] && j < n) ? gm_at(j) : si.gnew;
-        const float attn = ex2(lgv - m) * inv_l;
+        const float attn = lgv * inv_l;
         ns[k] = a.mode ? attn : old + attn;   // current-step or cumulative
         cand[k] = ok[k] && evict && R >= a.n_sink && j < n + 1 - a.recent;
         rr[k] = fmaf(si.tau, gv, ns[k]);
