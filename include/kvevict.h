@@ -82,14 +82,16 @@ typedef struct kvevict_config {
                              KVEVICT_DECODE_RESIDENT: which kernel runs the decode steps */
 } kvevict_config;
 
-/* Decode kernels; both compute the same steps and agree with each other up to
- * the order of floating-point sums. STREAM: every step streams each row's
- * keys from device memory through shared memory, any row length. RESIDENT: a
- * call of several steps keeps each row in one CTA's shared memory for all of
- * them (rows up to 1023 keys, key-only handles; the rows of a large cache run
- * in waves). AUTO takes RESIDENT for key-only handles whose rows fit and for
- * calls of at least 4 steps, STREAM otherwise; asking for RESIDENT on a handle
- * whose rows do not fit, or that carries values, is INVALID_ARG at create. */
+/* Decode kernels; both compute the same steps and give the same results bit
+ * for bit. STREAM: every step streams each row's keys from device memory
+ * through shared memory, any row length. RESIDENT: a call of several steps
+ * keeps each row in one CTA's shared memory for all of them (key-only handles
+ * whose rows fit: about 780 keys at head_dim 128, 1023 at 64; the rows of a
+ * large cache run in waves). AUTO takes RESIDENT for calls of at least 4
+ * steps on key-only handles whose rows fit in one wave of CTAs, or in two at
+ * two CTAs an SM, and STREAM otherwise (kvevict_decode_kernel_for reports the
+ * choice); asking for RESIDENT on a handle whose rows do not fit, or that
+ * carries values, is INVALID_ARG at create. */
 #define KVEVICT_DECODE_AUTO 0
 #define KVEVICT_DECODE_STREAM 1
 #define KVEVICT_DECODE_RESIDENT 2

@@ -115,35 +115,45 @@ __device__ __forceinline__ float ex2(float x) {
 // warp order (one barrier). Both decode kernels use exactly these two
 // functions and this row-to-thread assignment, so their sums agree bit for bit
 // whichever threads computed the dot products.
+//
+// NT is the number of consumer threads taking part (256 in the streaming
+// kernel; 256 or 512 in the resident one). The sum's assignment is the 256-
+// thread one whatever NT is: threads beyond 256 add nothing. Scratch: red[w]
+// holds warp maxima (w < 16), red[16 + w] warp sums (w < 8).
+template <int NT = kConsumers>
 __device__ float block_max(float m, float* red) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float wm;
   asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(wm) : "f"(m));
   if (lane == 0) red[w] = wm;
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
   float M = red[0];
 #pragma unroll
-  for (int k = 1; k < kConsumerWarps; ++k) M = fmaxf(M, red[k]);
+  for (int k = 1; k < NT / 32; ++k) M = fmaxf(M, red[k]);
   return M;
 }
 
 // Sum of 2^(lg[R] - M) over R < NR, R != skip; the terms replace the logits.
+template <int NT = kConsumers>
 __device__ float block_expsum(float* lg, int NR, int skip, float M, float* red) {
+  static_assert(NT >= kConsumers, "the sum's row assignment needs 256 threads");
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float ls = 0.f;
-  for (int R = threadIdx.x; R < NR; R += kConsumers) {
-    if (R == skip) continue;
-    const float e = ex2(lg[R] - M);
-    lg[R] = e;
-    ls += e;
+  if (threadIdx.x < kConsumers) {   // whole warps
+    float ls = 0.f;
+    for (int R = threadIdx.x; R < NR; R += kConsumers) {
+      if (R == skip) continue;
+      const float e = ex2(lg[R] - M);
+      lg[R] = e;
+      ls += e;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+    if (lane == 0) red[16 + w] = ls;
   }
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+  float L = red[16];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-  if (lane == 0) red[kConsumerWarps + w] = ls;
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-  float L = red[kConsumerWarps];
-#pragma unroll
-  for (int k = 1; k < kConsumerWarps; ++k) L += red[kConsumerWarps + k];
+  for (int k = 1; k < kConsumerWarps; ++k) L += red[16 + k];
   return L;
 }
 
@@ -156,6 +166,7 @@ __device__ __forceinline__ uint32_t float_key(float f) {
 // Block-wide (r, slot) argmin, lowest slot on ties: per warp two redux
 // minima (the key of r, then the slot among the lanes holding it), then every
 // thread merges the eight warp candidates itself.
+template <int NT = kConsumers>
 __device__ int block_argmin(float r, int i, float* redf, int* redi) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t key = float_key(r);
@@ -164,11 +175,11 @@ __device__ int block_argmin(float r, int i, float* redf, int* redi) {
   const uint32_t cand = key == kmin ? (uint32_t)i : 0xffffffffu;
   asm("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(imin) : "r"(cand));
   if (lane == 0) { redf[40 + w] = __uint_as_float(kmin); redi[40 + w] = (int)imin; }
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
   uint32_t kb = __float_as_uint(redf[40]);
   int ib = redi[40];
 #pragma unroll
-  for (int k = 1; k < kConsumerWarps; ++k) {
+  for (int k = 1; k < NT / 32; ++k) {
     const uint32_t k2 = __float_as_uint(redf[40 + k]);
     const int i2 = redi[40 + k];
     if (k2 < kb || (k2 == kb && i2 < ib)) { kb = k2; ib = i2; }
@@ -197,9 +208,11 @@ __device__ __forceinline__ float tau_at(const DecodeArgs& a, int64_t p) {
 
 // Named barrier 1 over the consumer warps only (the producer and scheduler
 // warps run ahead on their own): a plain sync, and one that ORs a predicate.
+template <int NT = kConsumers>
 __device__ __forceinline__ void consumers_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
 }
+template <int NT = kConsumers>
 __device__ __forceinline__ bool consumers_any(bool pred) {
   uint32_t r;
   asm volatile(
@@ -208,7 +221,7 @@ __device__ __forceinline__ bool consumers_any(bool pred) {
       "bar.red.or.pred q, 1, %2, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"((uint32_t)pred), "n"(kConsumers)
+      : "r"((uint32_t)pred), "n"(NT)
       : "memory");
   return r != 0;
 }

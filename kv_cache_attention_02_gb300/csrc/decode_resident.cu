@@ -36,12 +36,18 @@
 namespace kvx {
 namespace {
 
-constexpr int kHelperWarp = kConsumerWarps;   // stages each step's inputs
-constexpr int kRThreads = kConsumers + 32;
+// NW consumer warps (8, or 16 when a row's shared memory leaves room for one
+// CTA an SM only) and one helper warp that stages each step's inputs.
+template <int NW>
+struct Res {
+  static constexpr int NT = NW * 32;           // consumer threads
+  static constexpr int HELPER = NW;            // the helper's warp index
+  static constexpr int THREADS = NT + 32;
+  static constexpr int RPP = NT / kTPR;        // rows per pass (8 threads a row)
+};
 constexpr int kQ = 16;                        // input slots (steps the helper may run ahead)
 constexpr int kGroup = 8;                     // steps the helper prepares at once
-constexpr int kMaxPerThread = 4;              // logical slots per consumer thread in the shift pass
-constexpr int kResidentMaxCap = kConsumers * kMaxPerThread;   // 1024 rows
+constexpr int kResidentMaxCap = 1024;         // rows a CTA holds
 
 // One step's inputs as the helper leaves them in a slot; the new key follows.
 struct StepIn {
@@ -82,10 +88,14 @@ __host__ __device__ inline ResLayout resident_layout(int cap) {
   return L;
 }
 
-template <int D>
-// Two CTAs (18 warps) fit on an SM at up to 96 registers a thread; at 104 the
-// register file of the SM sub-partition holding a CTA's ninth warp runs out.
-__global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const DecodeArgs a) {
+// With 8 consumer warps two CTAs (18 warps) fit on an SM at up to 96 registers
+// a thread; at 104 the register file of the SM sub-partition holding a CTA's
+// ninth warp runs out. With 16 (17 warps, one CTA an SM) 96 registers keep the
+// busiest sub-partition's five warps within its share.
+template <int D, int NW>
+__global__ void __launch_bounds__(Res<NW>::THREADS, NW == 8 ? 2 : 1) resident_step_kernel(const DecodeArgs a) {
+  using RC = Res<NW>;
+  constexpr int NT = RC::NT, RPP = RC::RPP;
   using G = Geo<D>;
   using Chunk = typename G::Chunk;
   using Word = typename G::Word;
@@ -109,7 +119,7 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
   if (tid == 0) {
     for (int q = 0; q < kQ; ++q) {
       mbar_init(kfull(q), 32);               // every helper lane
-      mbar_init(kempty(q), kConsumerWarps);  // each consumer warp
+      mbar_init(kempty(q), NW);  // each consumer warp
     }
     mbar_init(loaded, 1);
     fence_mbar_init();
@@ -128,7 +138,7 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
   const int budget = li.budget;
   const int64_t in_off = (((int64_t)b * a.L + l) * a.H + hh);
 
-  if (warp == kHelperWarp) {
+  if (warp == RC::HELPER) {
     // ------------------------------------------------------------ helper
     // Eight steps at a time: their keys are read together (eight loads in
     // flight per lane) and lanes 0..7 take one step's Gumbel value each.
@@ -209,7 +219,7 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
   }
   {
     const int64_t mb = arena_meta();
-    for (int j = tid; j < n; j += kConsumers) {
+    for (int j = tid; j < n; j += NT) {
       const int src = (e0 >= 0 && j >= e0) ? j + 1 : j;
       sc_at(j) = a.score[mb + src];
       gm_at(j) = a.gum[mb + src];
@@ -220,10 +230,10 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
   // shift-by-one RoPE constants, read from shared memory where a row moved
   // (registers are the resident step's scarcest resource)
   float* rope_s_c = reinterpret_cast<float*>(smem + SL.rope);
-  for (int i = tid; i < D; i += kConsumers) rope_s_c[i] = i < HALF ? a.rope_c[i] : a.rope_s[i - HALF];
+  for (int i = tid; i < D; i += NT) rope_s_c[i] = i < HALF ? a.rope_c[i] : a.rope_s[i - HALF];
   bool got = wait_watch(loaded, 0, abort_flag, a.err);
   if (got && a.T > 0) got = wait_watch(kfull(0), 0, abort_flag, a.err);
-  bool aborted = consumers_any(!got || *abort_flag);   // also publishes the slot arrays
+  bool aborted = consumers_any<NT>(!got || *abort_flag);   // also publishes the slot arrays
 
   int e_prev = e0;     // physical slot the last step evicted (left in place), or -1
   int fr = n;          // the physical row the next new key goes to
@@ -267,13 +277,13 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
     // Four rows per thread per round: R = r0 + 32u + rg, u = 0..3. Which thread
     // writes a logit does not matter: the softmax statistics are a block max and
     // a sum in a fixed row order (block_max, block_expsum).
-    for (int r0 = 0; r0 < nphys; r0 += 4 * kRowsPerPass) {
+    for (int r0 = 0; r0 < nphys; r0 += 4 * RPP) {
       Chunk lo[4], hi[4];
       bool live[4];
       int Rr[4], ph[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        Rr[u] = r0 + u * kRowsPerPass + rg;
+        Rr[u] = r0 + u * RPP + rg;
         live[u] = Rr[u] < nphys && Rr[u] != e_prev;
         ph[u] = live[u] ? pm_at((shift && Rr[u] > e_prev) ? Rr[u] - 1 : Rr[u]) : 0;
       }
@@ -324,7 +334,7 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
           const bool lv = u == 0 ? live[0] : u == 1 ? live[1] : u == 2 ? live[2] : live[3];
           if (lv) {
             const float sv = mine * a.scale2;   // base-2 logit
-            lg[r0 + u * kRowsPerPass + rg] = sv;
+            lg[r0 + u * RPP + rg] = sv;
             run_m = fmaxf(run_m, sv);
           }
         }
@@ -332,16 +342,16 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
     }
 
     // ------------------------------------------------ softmax, scores, selection
-    const float m = block_max(run_m, redf);
-    const float inv_l = 1.f / block_expsum(lg, NR, e_prev, m, redf);   // lg now holds the terms
+    const float m = block_max<NT>(run_m, redf);
+    const float inv_l = 1.f / block_expsum<NT>(lg, NR, e_prev, m, redf);   // lg now holds the terms
     float best_r = INFINITY;
     int best_R = INT_MAX;
-    for (int R0 = tid; R0 < NR; R0 += 2 * kConsumers) {   // two rows per thread per round
+    for (int R0 = tid; R0 < NR; R0 += 2 * NT) {   // two rows per thread per round
       float ns[2], rr[2];
       bool ok[2], cand[2];
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const int R = R0 + k * kConsumers;
+        const int R = R0 + k * NT;
         ok[k] = R < NR && R != e_prev;
         const int j = (shift && R > e_prev) ? R - 1 : R;   // logical slot (the new row: n)
         const float lgv = ok[k] ? lg[R] : 0.f;
@@ -354,17 +364,17 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
       }
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const int R = R0 + k * kConsumers;
+        const int R = R0 + k * NT;
         if (ok[k]) lg[R] = ns[k];
         if (cand[k] && rr[k] < best_r) { best_r = rr[k]; best_R = R; }
       }
     }
     int e = -1;   // the evicted slot, numbered over the n + 1 rows after the append
     if (evict) {
-      const int R_e = block_argmin(best_r, best_R, redf, redi);   // its barrier also publishes lg
+      const int R_e = block_argmin<NT>(best_r, best_R, redf, redi);   // its barrier also publishes lg
       e = (shift && R_e > e_prev) ? R_e - 1 : R_e;
     } else {
-      consumers_sync();
+      consumers_sync<NT>();
     }
     if (tid == 0) {
       if (a.evicted) a.evicted[(int64_t)t * a.ev_step + in_off] = e;
@@ -377,7 +387,7 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
     const int NK = evict ? n : n + 1;
     const int fr_next = !evict ? n + 1 : (e < n ? pm_at(e) : fr);
     const int nxt = cur ^ (4 * c4);   // the other copy
-    for (int j = tid; j < NK; j += kConsumers) {
+    for (int j = tid; j < NK; j += NT) {
       const int src = (evict && j >= e) ? j + 1 : j;
       const bool old = src < n;
       reinterpret_cast<float*>(meta0)[nxt + j] = lg[(shift && src >= e_prev) ? src + 1 : src];
@@ -393,7 +403,7 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
     // slot arrays (and frees lg and the reduction scratch) before it
     got = true;
     if (t + 1 < a.T) got = wait_watch(kfull((t + 1) % kQ), (uint32_t)(((t + 1) / kQ) & 1), abort_flag, a.err);
-    aborted = consumers_any(!got || *abort_flag);
+    aborted = consumers_any<NT>(!got || *abort_flag);
   }
 
   if (aborted) {
@@ -407,7 +417,7 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
   // un-re-rotated keys; the next step (or a flush) applies that compaction.
   const int gshift = e_prev;   // -1: nothing pending
   __half* Kg = arena_keys();
-  for (int j0 = 0; j0 < n; j0 += kRowsPerPass) {
+  for (int j0 = 0; j0 < n; j0 += RPP) {
     const int j = j0 + rg;
     if (j < n) {
       const int gs = (gshift >= 0 && j >= gshift) ? j + 1 : j;
@@ -418,7 +428,7 @@ __global__ void __launch_bounds__(kRThreads, 2) resident_step_kernel(const Decod
     }
   }
   const int64_t mb = arena_meta();
-  for (int j = tid; j < n; j += kConsumers) {
+  for (int j = tid; j < n; j += NT) {
     const int gs = (gshift >= 0 && j >= gshift) ? j + 1 : j;
     a.score[mb + gs] = sc_at(j);
     a.gum[mb + gs] = gm_at(j);
@@ -437,23 +447,37 @@ size_t resident_step_smem(int D, int capm_max) {
   return D == 64 ? resident_layout<64>(capm_max).total : resident_layout<128>(capm_max).total;
 }
 
-cudaError_t resident_step_ctas_per_sm(int D, size_t smem, int* ctas) {
-  if (D == 64) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, resident_step_kernel<64>, kRThreads, smem);
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, resident_step_kernel<128>, kRThreads, smem);
+namespace {
+template <int D, int NW>
+cudaError_t resident_setup_one(size_t smem, int* ctas) {
+  cudaError_t e = cudaFuncSetAttribute(resident_step_kernel<D, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, resident_step_kernel<D, NW>, Res<NW>::THREADS, smem);
+  return e;
+}
+}  // namespace
+
+cudaError_t resident_step_setup(int D, size_t smem, int* ctas8, int* ctas16) {
+  cudaError_t e = D == 64 ? resident_setup_one<64, 8>(smem, ctas8) : resident_setup_one<128, 8>(smem, ctas8);
+  if (e == cudaSuccess)
+    e = D == 64 ? resident_setup_one<64, 16>(smem, ctas16) : resident_setup_one<128, 16>(smem, ctas16);
+  return e;
 }
 
-cudaError_t resident_step_setup(int D, size_t smem) {
-  if (D == 64)
-    return cudaFuncSetAttribute(resident_step_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  return cudaFuncSetAttribute(resident_step_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-}
-
-cudaError_t launch_resident_step(const DecodeArgs& a, int D, size_t smem, cudaStream_t s) {
+cudaError_t launch_resident_step(const DecodeArgs& a, int D, int warps, size_t smem, cudaStream_t s) {
   if (a.rows <= 0 || a.T <= 0) return cudaSuccess;
-  if (D == 64)
-    resident_step_kernel<64><<<a.rows, kRThreads, smem, s>>>(a);
-  else
-    resident_step_kernel<128><<<a.rows, kRThreads, smem, s>>>(a);
+  if (warps == 16) {
+    if (D == 64)
+      resident_step_kernel<64, 16><<<a.rows, Res<16>::THREADS, smem, s>>>(a);
+    else
+      resident_step_kernel<128, 16><<<a.rows, Res<16>::THREADS, smem, s>>>(a);
+  } else {
+    if (D == 64)
+      resident_step_kernel<64, 8><<<a.rows, Res<8>::THREADS, smem, s>>>(a);
+    else
+      resident_step_kernel<128, 8><<<a.rows, Res<8>::THREADS, smem, s>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -142,10 +142,11 @@ cudaError_t launch_flush(const FlushArgs& a, int D, int heads, cudaStream_t s);
 // The shared-memory-resident decode step (decode_resident.cu): one CTA per row
 // for every step of the call. resident_step_smem returns (size_t)-1 when a
 // row of capm_max slots does not fit its layout.
+// It comes with 8 or 16 consumer warps: setup sets both variants' shared
+// memory attribute and reports how many CTAs of each fit an SM.
 size_t resident_step_smem(int D, int capm_max);
-cudaError_t resident_step_setup(int D, size_t smem);
-cudaError_t resident_step_ctas_per_sm(int D, size_t smem, int* ctas);
-cudaError_t launch_resident_step(const DecodeArgs& a, int D, size_t smem, cudaStream_t s);
+cudaError_t resident_step_setup(int D, size_t smem, int* ctas8, int* ctas16);
+cudaError_t launch_resident_step(const DecodeArgs& a, int D, int warps, size_t smem, cudaStream_t s);
 
 // Page-locked host memory (staging.cu). mapped_host: the device address of the
 // host buffer [p, p + bytes) when both its ends are page-locked and mapped into

@@ -124,6 +124,7 @@ struct kvevict {
   size_t resident_smem = 0; // the resident decode step's shared memory
   bool resident_ok = false; // rows fit the resident decode step (key-only handle)
   bool resident_auto = false; // the automatic choice takes the resident step (long enough calls)
+  int resident_warps = 8;     // its consumer warps: 8, or 16 where only one CTA fits an SM
   int sms = 0;              // SMs on the device
   int64_t next_pos = 0;
   bool stepped = false;
@@ -202,7 +203,7 @@ int enqueue_steps(kvevict* h, const uint16_t* keys, const uint16_t* values, int6
   a.stall = h->stall_next ? 1 : 0;
   h->stall_next = false;
   if (uses_resident(h, T))
-    KV_CUDA(kvx::launch_resident_step(a, h->D, h->resident_smem, s));
+    KV_CUDA(kvx::launch_resident_step(a, h->D, h->resident_warps, h->resident_smem, s));
   else
     KV_CUDA(kvx::launch_decode_step(a, h->D, h->decode_grid, h->decode_smem, s));
   h->dsteps += T;
@@ -459,19 +460,23 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
   }
   KV_CUDA_CREATE(kvx::decode_step_setup(h->D, h->decode_smem));
   if (h->resident_ok) {
-    KV_CUDA_CREATE(kvx::resident_step_setup(h->D, h->resident_smem));
     // The resident step runs one CTA per row, in waves when the rows outnumber
     // the CTAs that fit; each wave runs every step. Measured on GB300 it beats
     // the streaming step when the rows fit in one wave, or in two waves at two
-    // or more CTAs an SM (keys up to about 400 rows of head_dim 128); a row of
-    // 513 keys at one CTA an SM in two waves was slower (8.3 against 7.4 us).
-    int per_sm = 0, sms = 0;
-    KV_CUDA_CREATE(kvx::resident_step_ctas_per_sm(h->D, h->resident_smem, &per_sm));
+    // or more CTAs an SM (keys up to about 400 rows of head_dim 128). Where a
+    // row's shared memory leaves room for one CTA an SM, it runs 16 consumer
+    // warps instead of 8.
+    int per8 = 0, per16 = 0, sms = 0;
+    KV_CUDA_CREATE(kvx::resident_step_setup(h->D, h->resident_smem, &per8, &per16));
     KV_CUDA_CREATE(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device));
+    h->resident_warps = (per8 < 2 && per16 >= 1) ? 16 : 8;
+    const int per_sm = h->resident_warps == 16 ? per16 : per8;
     const int64_t slots = (int64_t)per_sm * sms;
     const int64_t waves = slots > 0 ? (h->heads + slots - 1) / slots : INT64_MAX;
     h->resident_auto = per_sm > 0 && (waves <= 1 || (waves <= 2 && per_sm >= 2));
     if (per_sm < 1) h->resident_ok = false;
+    if (c.decode_kernel == KVEVICT_DECODE_RESIDENT && !h->resident_ok)
+      return bail(fail(KVEVICT_ERR_INVALID_ARG, "the resident decode kernel does not fit on an SM"));
   }
   {
     int per_sm = 0, sms = 0;

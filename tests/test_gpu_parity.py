@@ -177,6 +177,11 @@ SMALL = [
              avg_budget=20, beta=1.0, n_sink=2, tau_init=0.0, tau_end=0.0, anneal_steps=0,
              rope_theta=10000.0, gumbel_seed=0, key_seed=14, prefill=50, decode=30, recent=2,
              score_mode=1, prefill_mode=1),
+    # rows long enough (661 keys) that one resident CTA fills an SM's shared
+    # memory: the resident step then runs its sixteen-warp form
+    Workload("long_rows_sixteen_warps", batch=1, n_layers=2, n_kv_heads=2, head_dim=128,
+             avg_budget=600, beta=1.1, n_sink=4, tau_init=1.0, tau_end=2.0, anneal_steps=900,
+             rope_theta=500000.0, gumbel_seed=31, key_seed=31, prefill=700, decode=200),
 ]
 
 
@@ -238,7 +243,7 @@ def test_step_path_equals_multistep_path(kvx, wgpu):
     assert_same_run(a, b)
 
 
-@pytest.mark.parametrize("wl", [w for w in SMALL if w.decode >= 8][:6] + [workloads.LATE_RISER_ANNEAL.scaled(
+@pytest.mark.parametrize("wl", [w for w in SMALL if w.decode >= 8][:6] + [SMALL[-1], workloads.LATE_RISER_ANNEAL.scaled(
     name="late_riser_short", batch=2, n_layers=3, decode=600)], ids=lambda w: w.name)
 def test_resident_kernel_equals_streaming_kernel(kvx, wgpu, wl):
     """The shared-memory-resident decode step and the streaming one give the
