@@ -156,6 +156,40 @@ int main(void) {
   }
   CUDA(cudaMemcpy(ev_dev_path, dev, nev * 4, cudaMemcpyDeviceToHost));
 
+  /* the decode kernel the library chose, and the other one forced: the same log */
+  {
+    int32_t kind = -1;
+    CHECK(kvevict_decode_kernel_for(h, T, &kind));
+    if (kind != KVEVICT_DECODE_STREAM && kind != KVEVICT_DECODE_RESIDENT) {
+      fprintf(stderr, "decode_kernel_for returned %d\n", kind);
+      return 1;
+    }
+    kvevict_config cfg2 = cfg;
+    cfg2.decode_kernel = kind == KVEVICT_DECODE_STREAM ? KVEVICT_DECODE_RESIDENT : KVEVICT_DECODE_STREAM;
+    kvevict_t* h2 = NULL;
+    CHECK(kvevict_create(&cfg2, NULL, &h2));
+    int32_t kind2 = -1;
+    CHECK(kvevict_decode_kernel_for(h2, T, &kind2));
+    if (kind2 != cfg2.decode_kernel) {
+      fprintf(stderr, "forced decode kernel %d, got %d\n", cfg2.decode_kernel, kind2);
+      return 1;
+    }
+    int32_t* ev_other = (int32_t*)malloc(nev * 4);
+    if (!ev_other) return 1;
+    CHECK(kvevict_prefill(h2, dpre, S, NULL));
+    CHECK(kvevict_decode(h2, ddec, T, dev, NULL));
+    CHECK(kvevict_check(h2, NULL));
+    CUDA(cudaMemcpy(ev_other, dev, nev * 4, cudaMemcpyDeviceToHost));
+    if (memcmp(ev_other, ev_dev_path, nev * 4) != 0) {
+      fprintf(stderr, "the two decode kernels gave different eviction logs\n");
+      return 1;
+    }
+    free(ev_other);
+    CHECK(kvevict_destroy(h2));
+    printf("decode kernels: the library's choice %s, the other one agrees\n",
+           kind == KVEVICT_DECODE_RESIDENT ? "resident" : "streaming");
+  }
+
   const size_t rowbuf = (size_t)cap;
   uint16_t* k1 = (uint16_t*)malloc(rowbuf * D * 2);
   uint16_t* k2 = (uint16_t*)malloc(rowbuf * D * 2);
