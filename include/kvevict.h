@@ -251,8 +251,9 @@ int kvevict_check(kvevict_t* h, void* stream);
 
 /* Test hook for the failure path, with no counterpart on the pages. With a
  * handle: in its next decode launch, the first CTA's copy of its first key
- * tile is never issued, so a wait on it runs out (1 s) and the kernel sets the
- * handle's error word (wait timeout) and returns. With h = NULL: the next
+ * tile (the resident step: of its row) is never issued, so a wait on it runs
+ * out (1 s) and the kernel sets the handle's error word (wait timeout) and
+ * returns. With h = NULL: the next
  * launch of the tensor-core prompt scorer in this process (kvevict_prefill of
  * any handle in a cumulative score mode, or kvevict_prefill_scores_noalloc)
  * never issues its first CTA's query-tile copy, with the same outcome: a

@@ -121,3 +121,37 @@ def test_prompt_scorer_wait_that_runs_out_is_reported():
     for r in _rows(WL):
         for x, y in zip(got[r], want[r]):
             assert np.array_equal(x, y), f"row {r}"
+
+
+def test_resident_decode_wait_that_runs_out_is_reported():
+    """The same for the resident decode step (a call of several steps on rows
+    that fit in shared memory): the hook leaves the first CTA's row load
+    unissued, its consumers' bounded wait runs out, the helper warp leaves its
+    loop on the abort flag, and the handle reports DEVICE_CHECK and recovers
+    after a reset."""
+    import kv_cache_attention_02_gb300 as kvx
+    from workloads import gpu as wgpu
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pre, dec = wgpu.device_inputs(WL)
+    h = kvx.from_workload(WL)
+    assert h.decode_kernel_for(WL.decode) == kvx.DECODE_RESIDENT
+    h.prefill(pre)
+    h.test_stall_next_step()
+    t0 = time.perf_counter()
+    h.decode(dec)
+    with pytest.raises(kvx.KVEvictError) as err:
+        h.check()
+    elapsed = time.perf_counter() - t0
+    assert err.value.code == kvx.ERR_DEVICE_CHECK
+    assert elapsed < 10.0, f"the stalled launch took {elapsed:.1f} s"
+    ref = kvx.from_workload(WL)
+    want_ev, want = _run(kvx, ref, pre, dec)
+    ref.close()
+    h.reset()
+    got_ev, got = _run(kvx, h, pre, dec)
+    h.close()
+    assert np.array_equal(got_ev, want_ev)
+    for r in _rows(WL):
+        for x, y in zip(got[r], want[r]):
+            assert np.array_equal(x, y), f"row {r}"
