@@ -20,7 +20,9 @@
 //   warps 2..9  two epilogue warpgroups, one per accumulator (alternate tiles):
 //               tcgen05.ld, causal mask on diagonal tiles only, exp2 on the MUFU,
 //               online row max/sum (pass 1) or column sums (pass 2); the two
-//               combine their per-row results at the end.
+//               combine their per-row results at the end. An accumulator goes
+//               back to the MMA issuer as soon as its last 64 columns are in
+//               registers, before their exponentials run.
 // Every mbarrier wait is bounded; on expiry the CTA sets the error word, drains
 // and frees its TMEM.
 #include "kvevict_internal.cuh"
@@ -369,6 +371,13 @@ __global__ void __launch_bounds__(kTCThreads, 2)
           tmem_ld64(taddr, v);
         else
           tmem_ld32(taddr, v);
+        if (c == kTB / CW - 1) {
+          // the whole accumulator has reached registers: hand it back to the
+          // MMA issuer before the last chunk's exponentials run
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty(b));
+        }
         const int c0 = colB0 + c * CW;
         if (!COLSUM) {
           if (!full_tile) {
@@ -436,9 +445,6 @@ __global__ void __launch_bounds__(kTCThreads, 2)
           csum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty(b));
       if (COLSUM) wg_bar(wg);                     // lse_s[b] free for this warpgroup's next tile
     }
     // warpgroup 1 hands its per-row results to warpgroup 0
