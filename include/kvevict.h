@@ -256,7 +256,8 @@ int kvevict_check(kvevict_t* h, void* stream);
  * returns. With h = NULL: the next
  * launch of the tensor-core prompt scorer in this process (kvevict_prefill of
  * any handle in a cumulative score mode, or kvevict_prefill_scores_noalloc)
- * never issues its first CTA's query-tile copy, with the same outcome: a
+ * never issues the query-tile copy of its first work item, with the same
+ * outcome: a
  * handle then reports DEVICE_CHECK, the allocation-free call writes NaN
  * scores. Nothing faults or hangs. One-shot. Errors: none. */
 int kvevict_test_stall_next_step(kvevict_t* h);
@@ -344,8 +345,9 @@ int kvevict_load_state(kvevict_t* h, const void* buf, size_t bytes, void* stream
  * the GPU runs the call: if one of the scorer's bounded waits runs out (1 s),
  * the call writes NaN to every entry of colsum instead of scores, so a caller
  * that must know checks colsum for NaN after the stream has passed the call.
- * (A device error word beside the array records it; each call clears the word
- * first with cudaMemsetAsync, which allocates nothing.)
+ * (A device error word beside the array records it. It and the scorer's two
+ * work-item counters, also beside the array, are cleared by each call first
+ * with cudaMemsetAsync, which allocates nothing.)
  * The first call on each device (and head_dim) looks up the device addresses
  * of the array and the error word, the device's multiprocessor count, and sets
  * the kernels' shared-memory attribute, with that device current; make that

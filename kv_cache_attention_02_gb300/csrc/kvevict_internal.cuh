@@ -98,7 +98,8 @@ struct PrefillScoreArgs {
   int heads;
   float scale2;            // log2(e) / sqrt(D)
   int* err;                // error word for bounded waits, or null
-  int stall;               // test hook: pass 1's first CTA never issues its query tile's copy
+  int stall;               // test hook: in pass 1 the copy of item 0's query tile is never issued
+  int* work;               // [2] work-item counters of the two passes (zeroed by the launch)
 };
 
 // Test hook (kvevict_test_stall_next_step with a null handle): the next prompt
@@ -163,7 +164,7 @@ cudaError_t launch_prefill_lastrow(const PrefillScoreArgs& a, int D, cudaStream_
 constexpr int kPrefillRowPad = 128;
 size_t prefill_tc_smem(int D);
 cudaError_t prefill_tc_setup(int D);
-cudaError_t launch_prefill_tc(const PrefillScoreArgs& a, int D, cudaStream_t s);
+cudaError_t launch_prefill_tc(const PrefillScoreArgs& a, int D, int sms, cudaStream_t s);
 size_t prefill_select_smem(int S);
 // The prompt's Gumbel values depend on (layer, head, position) only, not on the
 // batch row: out[(l*H + h)*Sp + j] = g(seed, l, h, j) for j < S.

@@ -10,9 +10,10 @@
 // caller passes the keys and the output buffer; nothing is allocated.
 //
 // The array costs kNoAllocScratchFloats * 4 bytes (16 MiB) on every GPU that
-// loads this library, for as long as the process lives. Every call shares it:
-// calls whose work overlaps on the GPU (different streams, or other threads)
-// race on it and must be serialised by the caller.
+// loads this library, for as long as the process lives. Every call shares it
+// and the scorer's two work-item counters beside it: calls whose work overlaps
+// on the GPU (different streams, or other threads) race on them and must be
+// serialised by the caller.
 //
 // A bounded wait in the scorer that runs out (1 s) cannot be reported through
 // the return code, which the call gives before the GPU runs. The scorer sets a
@@ -40,12 +41,15 @@ constexpr int kMaxDevices = 64;
 // Working memory of the allocation-free scorer: [2, heads, Sp] floats (the
 // row log-sum-exps, then the padded column sums).
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+// the scorer's two work-item counters, cleared by each call before its launches
+static __device__ __align__(256) int g_noalloc_work[2];
 // Error word of the allocation-free scorer's bounded waits (cleared by each call).
 static __device__ __align__(256) int g_noalloc_err;
 
 struct DeviceSetup {
   float* scratch = nullptr;   // device address of g_noalloc_scratch
   int* err = nullptr;         // device address of g_noalloc_err
+  int* work = nullptr;        // device address of g_noalloc_work
   int sms = 0;                // multiprocessors, to size the gather's grid
   bool tc_ready[2] = {false, false};   // scorer's shared-memory attribute set (D = 64, 128)
 };
@@ -88,12 +92,15 @@ int setup_device(int D, DeviceSetup* out) {
     int sms = 0;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e == cudaSuccess) e = cudaGetSymbolAddress(&q, g_noalloc_err);
+    void* w = nullptr;
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&w, g_noalloc_work);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) {
       kvx::set_last_error(std::string("device set-up: ") + cudaGetErrorString(e));
       return KVEVICT_ERR_CUDA;
     }
     st.err = static_cast<int*>(q);
+    st.work = static_cast<int*>(w);
     st.sms = sms > 0 ? sms : 1;
     st.scratch = static_cast<float*>(p);
   }
@@ -153,8 +160,9 @@ int prefill_scores_noalloc(const uint16_t* keys, int32_t heads, int32_t S, int32
   a.scale2 = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
   a.err = dev.err;
   a.stall = kvx::take_scorer_stall() ? 1 : 0;
+  a.work = dev.work;
   cudaError_t e = cudaMemsetAsync(dev.err, 0, sizeof(int), s);   // writes, allocates nothing
-  if (e == cudaSuccess) e = kvx::launch_prefill_tc(a, head_dim, s);
+  if (e == cudaSuccess) e = kvx::launch_prefill_tc(a, head_dim, dev.sms, s);
   if (e == cudaSuccess) {
     const int64_t total = (int64_t)heads * S;
     const int64_t blocks = std::min<int64_t>((total + 255) / 256, (int64_t)dev.sms * 16);

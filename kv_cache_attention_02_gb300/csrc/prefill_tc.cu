@@ -5,24 +5,31 @@
 // steps without eviction (page "veloxquant_mlx.quantizers.keyformer module",
 // keyformer_update, "For each of the S incoming tokens", steps 1-2).
 //
-//   pass 1 (COLSUM = false): CTA = (row, 128-query block I); tiles J = 0..I;
+//   pass 1 (COLSUM = false): work item = (row, 128-query block I); tiles J = 0..I;
 //            per query row i: lse2_i = log2 sum_{j<=i} 2^(s_ij), s = K_i.K_j*log2e/sqrt(D)
-//   pass 2 (COLSUM = true):  CTA = (row, 128-key block J); tiles I = J..nb-1 of the
-//            transposed product (TMEM lanes = key j, columns = query i);
+//   pass 2 (COLSUM = true):  work item = (row, 128-key block J); tiles I = J..nb-1 of
+//            the transposed product (TMEM lanes = key j, columns = query i);
 //            colsum_j = sum_{i>=j} 2^(s_ij - lse2_i), summed per lane in registers.
 //
-// Roles in a 320-thread CTA (two per SM):
-//   warp 0      one thread issues TMA loads (3-D tensor map [heads, S, D], 128-byte
-//               swizzle, two 64-element halves per 128-row tile) into a 2-stage ring;
-//   warp 1      allocates 256 TMEM columns (two 128x128 fp32 accumulators) and one
-//               thread issues tcgen05.mma (M=128, N=128, K=16, f16 in, f32 out);
-//               tcgen05.commit releases the smem stage and publishes the accumulator;
-//   warps 2..9  two epilogue warpgroups, one per accumulator (alternate tiles):
-//               tcgen05.ld, causal mask on diagonal tiles only, exp2 on the MUFU,
-//               online row max/sum (pass 1) or column sums (pass 2); the two
-//               combine their per-row results at the end. An accumulator goes
-//               back to the MMA issuer as soon as its last 64 columns are in
-//               registers, before their exponentials run.
+// Persistent CTAs, two per SM, take work items in row-major order (a row's
+// blocks together, so its keys are reused from L2; each row's blocks heaviest
+// first) from a launch-wide counter; TMEM, the barriers and the tile ring stay
+// live from one item to the next. Roles in a 320-thread CTA:
+//   warp 0      one thread claims the items and issues TMA loads (3-D tensor map
+//               [heads, S, D], 128-byte swizzle, two 64-element halves per 128-row
+//               tile): an item's stationary tile once the previous item's MMAs are
+//               done with it, then its streamed tiles into a 2-stage ring;
+//   warp 1      allocates 256 TMEM columns (two 128x128 fp32 accumulators, used in
+//               turn by the CTA's running tile count) and one thread issues
+//               tcgen05.mma (M=128, N=128, K=16, f16 in, f32 out); tcgen05.commit
+//               releases the ring stage and publishes the accumulator;
+//   warps 2..9  two epilogue warpgroups; warpgroup w takes tiles k = w, w + 2, ...
+//               of every item (so a row's result does not depend on which CTA
+//               ran it): tcgen05.ld, causal mask on diagonal tiles only, exp2 on
+//               the MUFU, online row max/sum (pass 1) or column sums (pass 2); the
+//               two combine their per-row results at the end of the item. An
+//               accumulator goes back to the MMA issuer as soon as its last 64
+//               columns are in registers, before their exponentials run.
 // Every mbarrier wait is bounded; on expiry the CTA sets the error word, drains
 // and frees its TMEM.
 #include "kvevict_internal.cuh"
@@ -30,6 +37,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 namespace kvx {
@@ -59,9 +67,9 @@ __host__ __device__ constexpr TCSmem tc_layout() {
   L.a = o;    o += TCGeo<D>::TILEB;
   L.b = o;    o += (size_t)kStagesTC * TCGeo<D>::TILEB;
   L.lse = o;  o += 2 * kTB * sizeof(float);
-  L.comb = o; o += 2 * kTB * sizeof(float);
+  L.comb = o; o += 2 * 2 * kTB * sizeof(float);   // per item parity: WG 1's (m, l) or sum
   L.bars = o; o += 16 * 8;
-  L.tmem = o; o += 16;
+  L.tmem = o; o += 16;                            // TMEM base, then the two queued items
   L.total = o + 1024;  // slack to align the tile region to 1024 bytes
   return L;
 }
@@ -174,8 +182,18 @@ __device__ __forceinline__ void wg_bar(int w) {
   else
     asm volatile("bar.sync 2, 128;" ::: "memory");
 }
-__device__ __forceinline__ void epi_all_bar() {
-  asm volatile("bar.sync 3, 256;" ::: "memory");
+// Barrier of both epilogue warpgroups (256 threads) that also ORs a predicate.
+__device__ __forceinline__ bool epi_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 3, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
 }
 
 // Barrier of warpgroup w that also ORs a predicate across it, so the whole
@@ -253,21 +271,32 @@ __global__ void __launch_bounds__(kTCThreads, 2)
   float* lse_s = reinterpret_cast<float*>(smem + SL.lse);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SL.bars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL.tmem);
+  volatile int* item_s = reinterpret_cast<volatile int*>(smem + SL.tmem + 4);   // [2]
   __shared__ int s_abort;
   auto full = [&](int s) { return smem_addr(&bars[s]); };
   auto empty = [&](int s) { return smem_addr(&bars[2 + s]); };
   auto acc_full = [&](int b) { return smem_addr(&bars[4 + b]); };
   auto acc_empty = [&](int b) { return smem_addr(&bars[6 + b]); };
   const uint32_t a_full = smem_addr(&bars[8]);
+  const uint32_t drain = smem_addr(&bars[9]);
+  const uint32_t a_empty = smem_addr(&bars[10]);
+  auto item_full = [&](int q) { return smem_addr(&bars[11 + q]); };
+  auto item_empty = [&](int q) { return smem_addr(&bars[13 + q]); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = a.S;
   const int nb = (S + kTB - 1) / kTB;
-  const int head = (int)(blockIdx.x / (unsigned)nb);
-  const int bidx = (int)(blockIdx.x - (unsigned)head * (unsigned)nb);
-  const int ablk = COLSUM ? bidx : nb - 1 - bidx;   // heaviest causal block first
-  const int first = COLSUM ? ablk : 0;
-  const int nblk = (COLSUM ? nb - 1 : ablk) - first + 1;
+  const int total = a.heads * nb;   // work items (row, 128-row block), row-major
+  int* work = a.work + (COLSUM ? 1 : 0);
+  // Item x: row x / nb, block x % nb taken heaviest first; the CTA keeps one
+  // query (pass 1) or key (pass 2) tile and streams the other operand's tiles.
+  auto item_geom = [&](int x, int& head, int& ablk, int& first, int& nblk) {
+    head = x / nb;
+    const int bidx = x - head * nb;
+    ablk = COLSUM ? bidx : nb - 1 - bidx;
+    first = COLSUM ? ablk : 0;
+    nblk = (COLSUM ? nb - 1 : ablk) - first + 1;
+  };
 
   if (tid == 0) {
     for (int s = 0; s < kStagesTC; ++s) {
@@ -277,9 +306,12 @@ __global__ void __launch_bounds__(kTCThreads, 2)
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full(b), 1);
       mbar_init(acc_empty(b), 4);
+      mbar_init(item_full(b), 1);
+      mbar_init(item_empty(b), 2);   // the MMA issuer and the epilogue
     }
     mbar_init(a_full, 1);
-    mbar_init(smem_addr(&bars[9]), 1);   // drain barrier (abort path only)
+    mbar_init(drain, 1);             // abort path only
+    mbar_init(a_empty, 1);
     fence_mbar_init();
     s_abort = 0;
   }
@@ -291,178 +323,229 @@ __global__ void __launch_bounds__(kTCThreads, 2)
   volatile int* abort_flag = &s_abort;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ scheduler + TMA producer
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
-      // test hook: pass 1's first CTA leaves the query tile's barrier incomplete,
-      // so the MMA issuer's bounded wait on it runs out
-      const bool stall = !COLSUM && a.stall && blockIdx.x == 0;
-      if (!stall) {
-        mbar_expect_tx(a_full, G::TILEB);
-        for (int kh = 0; kh < G::KH; ++kh)
-          tma_load_3d(sA + kh * G::HALFB, &kmap, kh * 64, ablk * kTB, head, a_full);
-      }
-      int issued = 0;
-      for (int k = 0; k < nblk; ++k) {
-        const int s = k % kStagesTC;
-        if (k >= kStagesTC &&
-            !wait_or_abort(empty(s), (uint32_t)((k / kStagesTC - 1) & 1), abort_flag, a.err))
+      int gb = 0;            // B tiles issued over all items
+      int a_issued = 0;      // query/key tiles issued
+      for (int it = 0;; ++it) {
+        const int q = it & 1;
+        if (it >= 2 && !wait_or_abort(item_empty(q), (uint32_t)(((it >> 1) - 1) & 1), abort_flag, a.err))
           break;
-        mbar_expect_tx(full(s), G::TILEB);
-        for (int kh = 0; kh < G::KH; ++kh)
-          tma_load_3d(sB + s * G::TILEB + kh * G::HALFB, &kmap, kh * 64, (first + k) * kTB, head,
-                      full(s));
-        issued = k + 1;
+        const int x = atomicAdd(work, 1);
+        item_s[q] = x < total ? x : -1;
+        mbar_arrive(item_full(q));
+        if (x >= total) break;
+        int head, ablk, first, nblk;
+        item_geom(x, head, ablk, first, nblk);
+        // the stationary tile, once the previous item's MMAs are done with it;
+        // test hook: in pass 1 the CTA that claims item 0 leaves that tile's
+        // barrier incomplete
+        if (it >= 1 && !wait_or_abort(a_empty, (uint32_t)((it - 1) & 1), abort_flag, a.err)) break;
+        if (!(!COLSUM && a.stall && x == 0)) {
+          mbar_expect_tx(a_full, G::TILEB);
+          for (int kh = 0; kh < G::KH; ++kh)
+            tma_load_3d(sA + kh * G::HALFB, &kmap, kh * 64, ablk * kTB, head, a_full);
+        }
+        a_issued = it + 1;
+        bool ok = true;
+        for (int k = 0; k < nblk; ++k, ++gb) {
+          const int s = gb % kStagesTC;
+          if (gb >= kStagesTC &&
+              !wait_or_abort(empty(s), (uint32_t)((gb / kStagesTC - 1) & 1), abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(full(s), G::TILEB);
+          for (int kh = 0; kh < G::KH; ++kh)
+            tma_load_3d(sB + s * G::TILEB + kh * G::HALFB, &kmap, kh * 64, (first + k) * kTB, head,
+                        full(s));
+        }
+        if (!ok) break;
       }
       if (*abort_flag) {  // give copies still in flight a moment to land before exit
-        (void)mbar_wait_bounded(a_full, 0, 10000000ull);
-        for (int k = issued > kStagesTC ? issued - kStagesTC : 0; k < issued; ++k)
+        if (a_issued > 0) (void)mbar_wait_bounded(a_full, (uint32_t)((a_issued - 1) & 1), 10000000ull);
+        for (int k = gb > kStagesTC ? gb - kStagesTC : 0; k < gb; ++k)
           (void)mbar_wait_bounded(full(k % kStagesTC), (uint32_t)((k / kStagesTC) & 1), 10000000ull);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && wait_or_abort(a_full, 0, abort_flag, a.err)) {
-      for (int k = 0; k < nblk; ++k) {
-        const int s = k % kStagesTC, b = k & 1;
-        if (!wait_or_abort(full(s), (uint32_t)((k / kStagesTC) & 1), abort_flag, a.err)) break;
-        if (k >= 2 && !wait_or_abort(acc_empty(b), (uint32_t)((k / 2 - 1) & 1), abort_flag, a.err))
-          break;
-        tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(b * kTB);
+    if (lane == 0) {
+      int gb = 0, g = 0;     // B tiles consumed, accumulator tiles issued
+      for (int it = 0;; ++it) {
+        const int q = it & 1;
+        if (!wait_or_abort(item_full(q), (uint32_t)((it >> 1) & 1), abort_flag, a.err)) break;
+        const int x = item_s[q];
+        mbar_arrive(item_empty(q));
+        if (x < 0) break;
+        int head, ablk, first, nblk;
+        item_geom(x, head, ablk, first, nblk);
+        if (!wait_or_abort(a_full, (uint32_t)(it & 1), abort_flag, a.err)) break;
+        bool ok = true;
+        for (int k = 0; k < nblk; ++k, ++gb, ++g) {
+          const int s = gb % kStagesTC, b = g & 1;
+          if (!wait_or_abort(full(s), (uint32_t)((gb / kStagesTC) & 1), abort_flag, a.err) ||
+              (g >= 2 && !wait_or_abort(acc_empty(b), (uint32_t)((g / 2 - 1) & 1), abort_flag, a.err))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + (uint32_t)(b * kTB);
 #pragma unroll
-        for (int kk = 0; kk < G::KSTEPS; ++kk) {
-          const uint32_t off = (uint32_t)((kk >> 2) * G::HALFB + (kk & 3) * 32);
-          tc_mma(d, sw128_desc(sA + off), sw128_desc(sB + s * G::TILEB + off), kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < G::KSTEPS; ++kk) {
+            const uint32_t off = (uint32_t)((kk >> 2) * G::HALFB + (kk & 3) * 32);
+            tc_mma(d, sw128_desc(sA + off), sw128_desc(sB + s * G::TILEB + off), kk > 0 ? 1u : 0u);
+          }
+          tc_commit(empty(s));
+          tc_commit(acc_full(b));
         }
-        tc_commit(empty(s));
-        tc_commit(acc_full(b));
+        if (!ok) break;
+        tc_commit(a_empty);   // the stationary tile is free once these MMAs finish
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue warpgroups
-    // Warpgroup wg (warps 2..5: 0, warps 6..9: 1) owns TMEM accumulator wg and
-    // the tiles k = wg, wg + 2, ...; the two combine their per-row results at
-    // the end. A warp reaches TMEM lanes 32 * (warp % 4) .. + 31.
+    // Warpgroup wg (warps 2..5: 0, warps 6..9: 1) takes tiles k = wg, wg + 2, ...
+    // of every item, whichever accumulator the CTA's running tile count puts
+    // them in, so each row's result does not depend on the schedule; the two
+    // combine their per-row results at the end of the item. A warp reaches
+    // TMEM lanes 32 * (warp % 4) .. + 31.
     const int wg = (warp - 2) >> 2;
-    const int b = wg;
     const int q = warp & 3;
     const int r = q * 32 + lane;                  // tile row = TMEM lane
-    const int rowA = ablk * kTB + r;              // query row i (pass 1) / key row j (pass 2)
     const int et = tid - 64 - wg * kTB;           // 0..127 within the warpgroup
-    const float* lse_h = a.lse2 + (size_t)head * a.Sp;
+    float* comb = reinterpret_cast<float*>(smem + SL.comb);
     constexpr int CW = 64;                        // accumulator columns per TMEM read
-    float run_m = -INFINITY, run_l = 0.f, csum = 0.f;
-    for (int k = wg; k < nblk; k += 2) {
-      const int colB0 = (first + k) * kTB;
-      if (COLSUM) lse_s[b * kTB + et] = -lse_h[colB0 + et];   // this tile's 128 query -lse values
-      const bool ok = wait_or_abort(acc_full(b), (uint32_t)((k / 2) & 1), abort_flag, a.err);
-      if (wg_any(wg, !ok)) break;                 // also publishes lse_s to the warpgroup
-      tc_fence_after();
-      const bool full_tile = COLSUM ? (colB0 > ablk * kTB + kTB - 1 && colB0 + kTB <= S)
-                                    : (colB0 + kTB - 1 < ablk * kTB && ablk * kTB + kTB <= S);
-      // Interior tiles take no mask; the scale rides in one FMA per element
-      // (max over the raw dot products: scale2 > 0 keeps the order).
-#pragma unroll 1
-      for (int c = 0; c < kTB / CW; ++c) {
-        float v[CW];
-        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * kTB + c * CW);
-        if (CW == 64)
-          tmem_ld64(taddr, v);
-        else
-          tmem_ld32(taddr, v);
-        if (c == kTB / CW - 1) {
-          // the whole accumulator has reached registers: hand it back to the
-          // MMA issuer before the last chunk's exponentials run
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(acc_empty(b));
+    int g = 0;                                    // the CTA's tiles before this item
+    for (int it = 0;; ++it) {
+      const int qi = it & 1;
+      const bool got = wait_or_abort(item_full(qi), (uint32_t)((it >> 1) & 1), abort_flag, a.err);
+      const int x = got ? item_s[qi] : -1;
+      if (epi_any(x < 0)) break;
+      int head, ablk, first, nblk;
+      item_geom(x, head, ablk, first, nblk);
+      const int rowA = ablk * kTB + r;            // query row i (pass 1) / key row j (pass 2)
+      float run_m = -INFINITY, run_l = 0.f, csum = 0.f;
+      bool aborted = false;
+      float* lsb = lse_s + wg * kTB;
+      const int tend = first + nblk;
+      for (int tb = first + wg, gt = g + wg; tb < tend; tb += 2, gt += 2) {
+        const int b = gt & 1;
+        const int colB0 = tb * kTB;
+        // the tile's 128 query -lse values (0 past S, where the scratch holds no
+        // value and the masked -inf products must still give exp2 = +0)
+        if (COLSUM) lsb[et] = colB0 + et < S ? -a.lse2[(size_t)head * a.Sp + colB0 + et] : 0.f;
+        const bool ok = wait_or_abort(acc_full(b), (uint32_t)((gt >> 1) & 1), abort_flag, a.err);
+        if (wg_any(wg, !ok)) {                    // also publishes lsb to the warpgroup
+          aborted = true;
+          break;
         }
-        const int c0 = colB0 + c * CW;
-        if (!COLSUM) {
-          if (!full_tile) {
-#pragma unroll
-            for (int e = 0; e < CW; ++e) {
-              const int j = c0 + e;
-              v[e] = (j <= rowA && j < S) ? v[e] : -INFINITY;
-            }
+        tc_fence_after();
+        const bool full_tile = COLSUM ? (colB0 > ablk * kTB + kTB - 1 && colB0 + kTB <= S)
+                                      : (colB0 + kTB - 1 < ablk * kTB && ablk * kTB + kTB <= S);
+        // Interior tiles take no mask; the scale rides in one FMA per element
+        // (max over the raw dot products: scale2 > 0 keeps the order).
+#pragma unroll 1
+        for (int c = 0; c < kTB / CW; ++c) {
+          float v[CW];
+          const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * kTB + c * CW);
+          if (CW == 64)
+            tmem_ld64(taddr, v);
+          else
+            tmem_ld32(taddr, v);
+          if (c == kTB / CW - 1) {
+            // the whole accumulator has reached registers: hand it back to the
+            // MMA issuer before the last chunk's exponentials run
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty(b));
           }
-          float m8[8];   // independent max chains
+          const int c0 = colB0 + c * CW;
+          if (!COLSUM) {
+            if (!full_tile) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) m8[e] = v[e];
-#pragma unroll
-          for (int e = 8; e < CW; ++e) m8[e & 7] = fmaxf(m8[e & 7], v[e]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) m8[e] = fmaxf(m8[e], m8[e + 4]);
-          const float cm = fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3]));
-          if (cm != -INFINITY) {
-            const float mn = fmaxf(run_m, cm * a.scale2);
-            const float nm = -mn;
-            const float2 sc2 = make_float2(a.scale2, a.scale2), nm2 = make_float2(nm, nm);
-            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);   // sums of e % 4 = 0, 1 | 2, 3
-#pragma unroll
-            for (int e = 0; e < CW; e += 4) {
-              const float2 t0 = ffma2(make_float2(v[e], v[e + 1]), sc2, nm2);
-              const float2 t1 = ffma2(make_float2(v[e + 2], v[e + 3]), sc2, nm2);
-              acc0 = fadd2(acc0, make_float2(ex2(t0.x), ex2(t0.y)));
-              acc1 = fadd2(acc1, make_float2(ex2(t1.x), ex2(t1.y)));
-            }
-            run_l = run_l * ex2(run_m - mn) + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
-            run_m = mn;
-          }
-        } else {
-          // -lse2 of the chunk's queries, read as 16-byte broadcasts where used
-          const float* nlp = lse_s + b * kTB + c * CW;
-          float s4[4] = {0.f, 0.f, 0.f, 0.f};
-          if (full_tile) {
-            const float2 sc2 = make_float2(a.scale2, a.scale2);
-            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int e = 0; e < CW; e += 4) {
-              const float4 nl = *reinterpret_cast<const float4*>(nlp + e);
-              const float2 t0 = ffma2(make_float2(v[e], v[e + 1]), sc2, make_float2(nl.x, nl.y));
-              const float2 t1 = ffma2(make_float2(v[e + 2], v[e + 3]), sc2, make_float2(nl.z, nl.w));
-              acc0 = fadd2(acc0, make_float2(ex2(t0.x), ex2(t0.y)));
-              acc1 = fadd2(acc1, make_float2(ex2(t1.x), ex2(t1.y)));
-            }
-            s4[0] = acc0.x;
-            s4[1] = acc0.y;
-            s4[2] = acc1.x;
-            s4[3] = acc1.y;
-          } else {
-#pragma unroll
-            for (int e = 0; e < CW; e += 4) {
-              const float4 nl = *reinterpret_cast<const float4*>(nlp + e);
-              const float n4[4] = {nl.x, nl.y, nl.z, nl.w};
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int i = c0 + e + u;
-                const float p = ex2(fmaf(v[e + u], a.scale2, n4[u]));
-                s4[u] += (i >= rowA && i < S) ? p : 0.f;
+              for (int e = 0; e < CW; ++e) {
+                const int j = c0 + e;
+                v[e] = (j <= rowA && j < S) ? v[e] : -INFINITY;
               }
             }
+            float m8[8];   // independent max chains
+#pragma unroll
+            for (int e = 0; e < 8; ++e) m8[e] = v[e];
+#pragma unroll
+            for (int e = 8; e < CW; ++e) m8[e & 7] = fmaxf(m8[e & 7], v[e]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) m8[e] = fmaxf(m8[e], m8[e + 4]);
+            const float cm = fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3]));
+            if (cm != -INFINITY) {
+              const float mn = fmaxf(run_m, cm * a.scale2);
+              const float nm = -mn;
+              const float2 sc2 = make_float2(a.scale2, a.scale2), nm2 = make_float2(nm, nm);
+              float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);   // sums of e % 4 = 0, 1 | 2, 3
+#pragma unroll
+              for (int e = 0; e < CW; e += 4) {
+                const float2 t0 = ffma2(make_float2(v[e], v[e + 1]), sc2, nm2);
+                const float2 t1 = ffma2(make_float2(v[e + 2], v[e + 3]), sc2, nm2);
+                acc0 = fadd2(acc0, make_float2(ex2(t0.x), ex2(t0.y)));
+                acc1 = fadd2(acc1, make_float2(ex2(t1.x), ex2(t1.y)));
+              }
+              run_l = run_l * ex2(run_m - mn) + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
+              run_m = mn;
+            }
+          } else {
+            // -lse2 of the chunk's queries, read as 16-byte broadcasts where used
+            const float* nlp = lsb + c * CW;
+            if (!full_tile) {
+              // queries outside i >= j, i < S: -inf, whose exp2 adds +0
+#pragma unroll
+              for (int e = 0; e < CW; ++e) {
+                const int i = c0 + e;
+                v[e] = (i >= rowA && i < S) ? v[e] : -INFINITY;
+              }
+            }
+            float s4[4];
+            {
+              const float2 sc2 = make_float2(a.scale2, a.scale2);
+              float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int e = 0; e < CW; e += 4) {
+                const float4 nl = *reinterpret_cast<const float4*>(nlp + e);
+                const float2 t0 = ffma2(make_float2(v[e], v[e + 1]), sc2, make_float2(nl.x, nl.y));
+                const float2 t1 = ffma2(make_float2(v[e + 2], v[e + 3]), sc2, make_float2(nl.z, nl.w));
+                acc0 = fadd2(acc0, make_float2(ex2(t0.x), ex2(t0.y)));
+                acc1 = fadd2(acc1, make_float2(ex2(t1.x), ex2(t1.y)));
+              }
+              s4[0] = acc0.x;
+              s4[1] = acc0.y;
+              s4[2] = acc1.x;
+              s4[3] = acc1.y;
+            }
+            csum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
           }
-          csum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
         }
+        if (COLSUM) wg_bar(wg);                   // lsb free for this warpgroup's next tile
       }
-      if (COLSUM) wg_bar(wg);                     // lse_s[b] free for this warpgroup's next tile
-    }
-    // warpgroup 1 hands its per-row results to warpgroup 0
-    float* comb = reinterpret_cast<float*>(smem + SL.comb);
-    if (wg == 1) {
-      comb[r] = COLSUM ? csum : run_m;
-      comb[kTB + r] = run_l;
-    }
-    epi_all_bar();
-    if (wg == 0 && !*abort_flag && rowA < S) {
-      if (COLSUM) {
-        a.colsum[(size_t)head * a.Sp + rowA] = csum + comb[r];
-      } else {
-        const float m2 = comb[r], l2 = comb[kTB + r];
-        const float m = fmaxf(run_m, m2);
-        const float l = (run_m == -INFINITY ? 0.f : run_l * exp2f(run_m - m)) +
-                        (m2 == -INFINITY ? 0.f : l2 * exp2f(m2 - m));
-        a.lse2[(size_t)head * a.Sp + rowA] = m + log2f(l);
+      g += nblk;
+      // warpgroup 1 hands its per-row results to warpgroup 0 (buffers alternate
+      // by item, so warpgroup 1 may run one item ahead)
+      float* cb = comb + qi * 2 * kTB;
+      if (wg == 1) {
+        cb[r] = COLSUM ? csum : run_m;
+        cb[kTB + r] = run_l;
+      }
+      if (epi_any(aborted || *abort_flag)) break;
+      if (tid == 64) mbar_arrive(item_empty(qi));   // every epilogue thread has read the item
+      if (wg == 0 && rowA < S) {
+        if (COLSUM) {
+          a.colsum[(size_t)head * a.Sp + rowA] = csum + cb[r];
+        } else {
+          const float m2 = cb[r], l2 = cb[kTB + r];
+          const float m = fmaxf(run_m, m2);
+          const float l = (run_m == -INFINITY ? 0.f : run_l * exp2f(run_m - m)) +
+                          (m2 == -INFINITY ? 0.f : l2 * exp2f(m2 - m));
+          a.lse2[(size_t)head * a.Sp + rowA] = m + log2f(l);
+        }
       }
     }
   }
@@ -471,8 +554,8 @@ __global__ void __launch_bounds__(kTCThreads, 2)
   __syncthreads();
   if (*abort_flag && tid == 32) {
     // let any MMA still in flight finish before the accumulators are freed
-    tc_commit(smem_addr(&bars[9]));
-    (void)mbar_wait_bounded(smem_addr(&bars[9]), 0, 10000000ull);
+    tc_commit(drain);
+    (void)mbar_wait_bounded(drain, 0, 10000000ull);
   }
   __syncwarp();
   if (warp == 1) {
@@ -514,8 +597,9 @@ cudaError_t prefill_tc_setup(int D) {
 }
 
 // Both passes over a.heads rows of S keys; a.Sp must be S rounded up to 128.
-cudaError_t launch_prefill_tc(const PrefillScoreArgs& a, int D, cudaStream_t s) {
+cudaError_t launch_prefill_tc(const PrefillScoreArgs& a, int D, int sms, cudaStream_t s) {
   if (a.S <= 0 || a.heads <= 0) return cudaSuccess;
+  if (!a.work) return cudaErrorInvalidValue;
   auto enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   // keys as a 3-D tensor [heads, S, D] (rows S_buf apart): box = 64 elements (128 bytes)
@@ -529,9 +613,11 @@ cudaError_t launch_prefill_tc(const PrefillScoreArgs& a, int D, cudaStream_t s) 
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  const int nb = (a.S + kTB - 1) / kTB;
-  const dim3 grid((unsigned)(a.heads * nb));
+  const int64_t items = (int64_t)a.heads * ((a.S + kTB - 1) / kTB);
+  const dim3 grid((unsigned)std::min<int64_t>(items, (int64_t)2 * std::max(sms, 1)));   // two CTAs an SM
   const size_t smem = prefill_tc_smem(D);
+  const cudaError_t z = cudaMemsetAsync(a.work, 0, 2 * sizeof(int), s);
+  if (z != cudaSuccess) return z;
   if (D == 64) {
     prefill_tc_kernel<64, false><<<grid, kTCThreads, smem, s>>>(map, a);
     prefill_tc_kernel<64, true><<<grid, kTCThreads, smem, s>>>(map, a);

@@ -116,6 +116,7 @@ struct kvevict {
   float* rope_s = nullptr;
   int max_delta = 1;
   float* lse2 = nullptr;    // prefill scratch [heads, Sp_max]
+  int* tc_work = nullptr;   // the prompt scorer's two work-item counters
   float* colsum = nullptr;
   float* gtab = nullptr;    // [L*H, Sp_max] the prompt's Gumbel values
   int64_t Sp_max = 0;
@@ -230,7 +231,8 @@ int enqueue_prompt_scores(kvevict* h, const uint16_t* keys, const uint16_t* valu
     KV_CUDA(kvx::launch_prefill_lastrow(sa, h->D, s));
   } else {
     sa.stall = kvx::take_scorer_stall() ? 1 : 0;
-    KV_CUDA(kvx::launch_prefill_tc(sa, h->D, s));
+    sa.work = h->tc_work;
+    KV_CUDA(kvx::launch_prefill_tc(sa, h->D, h->sms, s));
   }
   kvx::PrefillSelectArgs pa{};
   pa.keys = sa.keys;
@@ -342,6 +344,7 @@ void free_all(kvevict* h) {
   cudaFree(h->rope_c);
   cudaFree(h->rope_s);
   cudaFree(h->lse2);
+  cudaFree(h->tc_work);
   cudaFree(h->colsum);
   cudaFree(h->gtab);
 }
@@ -503,6 +506,7 @@ int kvevict_create(const kvevict_config* cfg, void* stream, kvevict_t** out) {
   KV_CUDA_CREATE(dalloc(&h->rope_s, (size_t)(h->max_delta + 1) * half));
   if (c.max_prefill > 0) {
     KV_CUDA_CREATE(dalloc(&h->lse2, (size_t)h->heads * h->Sp_max));
+    KV_CUDA_CREATE(dalloc(&h->tc_work, 2));
     KV_CUDA_CREATE(dalloc(&h->colsum, (size_t)h->heads * h->Sp_max));
     KV_CUDA_CREATE(dalloc(&h->gtab, (size_t)h->L * h->H * h->Sp_max));
   }
