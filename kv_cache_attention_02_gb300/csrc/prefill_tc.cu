@@ -411,6 +411,12 @@ __global__ void __launch_bounds__(kTCThreads, 2)
     // them in, so each row's result does not depend on the schedule; the two
     // combine their per-row results at the end of the item. A warp reaches
     // TMEM lanes 32 * (warp % 4) .. + 31.
+    // The parity waits on acc_full stay unambiguous because a warpgroup's
+    // consecutive tiles of an item use the same accumulator (it has seen that
+    // accumulator's previous phase itself) and both warpgroups meet at the end
+    // of every item (all earlier phases seen): no wait can be issued while its
+    // accumulator is two phases behind. More warpgroups than accumulators would
+    // break this and need the waits ordered explicitly.
     const int wg = (warp - 2) >> 2;
     const int q = warp & 3;
     const int r = q * 32 + lane;                  // tile row = TMEM lane
