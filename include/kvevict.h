@@ -252,7 +252,7 @@ int kvevict_check(kvevict_t* h, void* stream);
 /* Test hook for the failure path, with no counterpart on the pages. With a
  * handle: in its next decode launch, the first CTA's copy of its first key
  * tile (the resident step: of its row) is never issued, so a wait on it runs
- * out (1 s) and the kernel sets the handle's error word (wait timeout) and
+ * out (4 s) and the kernel sets the handle's error word (wait timeout) and
  * returns. With h = NULL: the next
  * launch of the tensor-core prompt scorer in this process (kvevict_prefill of
  * any handle in a cumulative score mode, or kvevict_prefill_scores_noalloc)
@@ -342,7 +342,7 @@ int kvevict_load_state(kvevict_t* h, const void* buf, size_t bytes, void* stream
  * (padding entries it reads are masked out). Calls whose work overlaps on the
  * GPU (other streams, other threads) race on the array: serialise them.
  * A failure on the GPU cannot reach the return code, which comes back before
- * the GPU runs the call: if one of the scorer's bounded waits runs out (1 s),
+ * the GPU runs the call: if one of the scorer's bounded waits runs out (4 s),
  * the call writes NaN to every entry of colsum instead of scores, so a caller
  * that must know checks colsum for NaN after the stream has passed the call.
  * (A device error word beside the array records it. It and the scorer's two

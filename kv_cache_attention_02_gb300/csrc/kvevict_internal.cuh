@@ -25,7 +25,11 @@
 namespace kvx {
 
 constexpr int kMaxLayers = 256;
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // bounded spin: 1 s, then error word
+// Bounded spin: 4 s of wall time, then the error word. Long enough that a
+// stall of the host link under a step that reads its keys from host memory
+// (one of about a second was seen) is not reported as a device error; short
+// enough that a wait that can never end returns within seconds.
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr int kErrWaitTimeout = 1;
 constexpr int kErrBadIndex = 2;
 

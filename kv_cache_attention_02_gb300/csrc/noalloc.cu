@@ -15,7 +15,7 @@
 // on the GPU (different streams, or other threads) race on them and must be
 // serialised by the caller.
 //
-// A bounded wait in the scorer that runs out (1 s) cannot be reported through
+// A bounded wait in the scorer that runs out (4 s) cannot be reported through
 // the return code, which the call gives before the GPU runs. The scorer sets a
 // file-scope error word instead, which each call clears first, and the last
 // kernel of the call then writes NaN to every output instead of the scores.

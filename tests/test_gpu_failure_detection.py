@@ -1,6 +1,6 @@
 """The failure path of the decode step, with no fault: a wait that runs out.
 
-Every wait in the kernels is bounded (1 s of %globaltimer); when one runs
+Every wait in the kernels is bounded (4 s of %globaltimer); when one runs
 out the kernel sets the handle's error word and its CTAs leave their loops,
 so the GPU context stays usable. kvevict_test_stall_next_step makes the next
 decode launch skip one copy, leaving a barrier that nothing completes. The
